@@ -1,0 +1,477 @@
+// api.cu -- the libengram C ABI: handles, host-side validation (before any
+// copy or launch, as spark_model/layers/engram_v41.rs checks `ensure!`s before
+// it uploads or launches), and the launch sequence of the forward.
+#include "common.cuh"
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+using namespace engram;
+
+struct engram_tables {
+    engram_geom g;
+    int64_t pad_id;
+    int device;
+    int64_t *token_map, *mult, *primes, *offsets;
+};
+
+struct engram_hasher {
+    const engram_tables *t;
+    int32_t batch;
+    int64_t max_seq;
+    int64_t *cache;
+    int device;
+};
+
+// The sticky error word, one per device (this module's copy on each GPU).
+static __device__ int g_err_word;
+
+namespace {
+
+std::mutex g_mu;
+int *g_err_ptr[64] = {};
+const uintptr_t *g_prof_events = nullptr;
+
+int *err_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+inline cudaStream_t S(uintptr_t s) { return reinterpret_cast<cudaStream_t>(s); }
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
+
+inline int cols(const engram_geom &g) { return (g.max_ngram - 1) * g.n_heads; }
+
+int check_geom(const engram_geom *g) {
+    if (!g) return ENGRAM_E_NULL;
+    if (g->hc < 1 || g->hc > 4) return ENGRAM_E_HC;
+    if (g->n_layers < 1 || g->n_layers > kMaxLayers) return ENGRAM_E_INVALID;
+    if (g->max_ngram < 2 || g->max_ngram > kMaxNgram) return ENGRAM_E_INVALID;
+    if (g->n_heads < 1 || g->n_heads > 1024) return ENGRAM_E_INVALID;
+    if (g->head_dim < 16 || g->head_dim > 1024 || g->head_dim % 16) return ENGRAM_E_INVALID;
+    if (g->scale_block < 16 || g->scale_block % 16 || g->head_dim % g->scale_block) return ENGRAM_E_INVALID;
+    if (g->dim < 8 || g->dim % 8 || g->dim > 16384) return ENGRAM_E_INVALID;
+    if (g->vocab < 1) return ENGRAM_E_INVALID;
+    const int64_t K = (int64_t)cols(*g) * g->head_dim;
+    if (K % 64 || K > (1 << 20)) return ENGRAM_E_UNSUPPORTED;
+    return ENGRAM_OK;
+}
+
+void record(int i, cudaStream_t s) {
+    if (g_prof_events) cudaEventRecord(reinterpret_cast<cudaEvent_t>(g_prof_events[i]), s);
+}
+
+inline int cuda_rc(cudaError_t e) { return e == cudaSuccess ? ENGRAM_OK : ENGRAM_E_CUDA; }
+
+template <class T>
+int dev_copy(T **dst, const T *src, size_t n) {
+    *dst = nullptr;
+    if (cudaMalloc(reinterpret_cast<void **>(dst), n * sizeof(T) + 16) != cudaSuccess) return ENGRAM_E_CUDA;
+    if (cudaMemcpy(*dst, src, n * sizeof(T), cudaMemcpyHostToDevice) != cudaSuccess) return ENGRAM_E_CUDA;
+    return ENGRAM_OK;
+}
+
+// The projection of one layer's x [M, K] (or of its fused gather) into kv.
+bool gemv_fits(int M, int K) {
+    return M >= 1 && M <= kSmallT && gemv_smem_bytes(M, K) <= 200 * 1024;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *engram_strerror(int code) {
+    switch (code) {
+        case ENGRAM_OK: return "ok";
+        case ENGRAM_E_INVALID: return "geometry or argument out of range";
+        case ENGRAM_E_NULL: return "a required pointer is null";
+        case ENGRAM_E_ALIGN: return "a pointer misses its required alignment";
+        case ENGRAM_E_CAPACITY: return "start_pos + T exceeds the hasher's max_seq";
+        case ENGRAM_E_WORKSPACE: return "workspace smaller than engram_workspace_bytes()";
+        case ENGRAM_E_HC: return "engram gate supports hc 1..4";
+        case ENGRAM_E_TOKEN: return "a token id outside the engram token_map";
+        case ENGRAM_E_ROW: return "a row id outside its engram table";
+        case ENGRAM_E_CUDA: return "a CUDA runtime call failed";
+        case ENGRAM_E_TIMEOUT: return "a bounded device wait gave up";
+        case ENGRAM_E_UNSUPPORTED: return "shape outside what the kernels handle";
+        default: return "unknown engram error";
+    }
+}
+
+int engram_tables_create(const engram_geom *geom, const int64_t *h_token_map, int64_t pad_token_id,
+                         const uint64_t *h_multipliers, const uint64_t *h_primes,
+                         const uint64_t *h_offsets, engram_tables **out) {
+    if (!out) return ENGRAM_E_NULL;
+    *out = nullptr;
+    int rc = check_geom(geom);
+    if (rc) return rc;
+    if (!h_token_map || !h_multipliers || !h_primes || !h_offsets) return ENGRAM_E_NULL;
+    const engram_geom g = *geom;
+    if (pad_token_id < 0 || pad_token_id >= g.vocab) return ENGRAM_E_INVALID;
+    const size_t nm = (size_t)g.n_layers * g.max_ngram, nc = (size_t)g.n_layers * cols(g);
+    for (size_t i = 0; i < nm; ++i)
+        if (h_multipliers[i] > (uint64_t)INT64_MAX) return ENGRAM_E_INVALID;
+    for (size_t i = 0; i < nc; ++i)
+        if (h_primes[i] == 0 || h_primes[i] > (uint64_t)INT64_MAX || h_offsets[i] > (uint64_t)INT64_MAX)
+            return ENGRAM_E_INVALID;
+    engram_tables *t = new engram_tables();
+    t->g = g;
+    t->pad_id = h_token_map[pad_token_id];
+    cudaGetDevice(&t->device);
+    rc = dev_copy(&t->token_map, h_token_map, (size_t)g.vocab);
+    if (!rc) rc = dev_copy(&t->mult, reinterpret_cast<const int64_t *>(h_multipliers), nm);
+    if (!rc) rc = dev_copy(&t->primes, reinterpret_cast<const int64_t *>(h_primes), nc);
+    if (!rc) rc = dev_copy(&t->offsets, reinterpret_cast<const int64_t *>(h_offsets), nc);
+    if (rc) {
+        engram_tables_destroy(t);
+        return rc;
+    }
+    *out = t;
+    return ENGRAM_OK;
+}
+
+void engram_tables_destroy(engram_tables *t) {
+    if (!t) return;
+    cudaFree(t->token_map);
+    cudaFree(t->mult);
+    cudaFree(t->primes);
+    cudaFree(t->offsets);
+    delete t;
+}
+
+int engram_hasher_create(const engram_tables *t, int32_t batch, int64_t max_seq, engram_hasher **out) {
+    if (!out || !t) return ENGRAM_E_NULL;
+    *out = nullptr;
+    if (batch < 1 || max_seq < 1 || max_seq > (int64_t(1) << 40) / batch) return ENGRAM_E_INVALID;
+    engram_hasher *h = new engram_hasher();
+    h->t = t;
+    h->batch = batch;
+    h->max_seq = max_seq;
+    cudaGetDevice(&h->device);
+    const size_t bytes = (size_t)batch * max_seq * sizeof(int64_t);
+    if (cudaMalloc(&h->cache, bytes) != cudaSuccess || cudaMemset(h->cache, 0, bytes) != cudaSuccess) {
+        engram_hasher_destroy(h);
+        return ENGRAM_E_CUDA;
+    }
+    if (!err_ptr()) {
+        engram_hasher_destroy(h);
+        return ENGRAM_E_CUDA;
+    }
+    *out = h;
+    return ENGRAM_OK;
+}
+
+int engram_hasher_reset(engram_hasher *hs, uintptr_t stream) {
+    if (!hs) return ENGRAM_E_NULL;
+    return cuda_rc(cudaMemsetAsync(hs->cache, 0, (size_t)hs->batch * hs->max_seq * sizeof(int64_t), S(stream)));
+}
+
+void engram_hasher_destroy(engram_hasher *hs) {
+    if (!hs) return;
+    cudaFree(hs->cache);
+    delete hs;
+}
+
+int engram_set_profile_events(const uintptr_t *events, int32_t n) {
+    if (events && n < 5) return ENGRAM_E_INVALID;
+    g_prof_events = events;
+    return ENGRAM_OK;
+}
+
+int engram_check(uintptr_t stream) {
+    if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return ENGRAM_E_CUDA;
+    int *p = err_ptr();
+    if (!p) return ENGRAM_E_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ENGRAM_E_CUDA;
+    if (v != 0 && cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return ENGRAM_E_CUDA;
+    return v;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Compute entry points
+// ---------------------------------------------------------------------------
+namespace {
+
+HashArgs hash_args(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t start_pos,
+                   int64_t *d_row_ids) {
+    const engram_tables *t = hs->t;
+    HashArgs a;
+    a.ids = d_ids;
+    a.B = hs->batch;
+    a.T = T;
+    a.start_pos = start_pos;
+    a.token_map = t->token_map;
+    a.vocab = t->g.vocab;
+    a.pad_id = t->pad_id;
+    a.mult = t->mult;
+    a.primes = t->primes;
+    a.offsets = t->offsets;
+    a.L = t->g.n_layers;
+    a.ng = t->g.max_ngram;
+    a.H = t->g.n_heads;
+    a.cache = hs->cache;
+    a.max_seq = hs->max_seq;
+    a.out = d_row_ids;
+    a.err = err_ptr();
+    return a;
+}
+
+int check_hash(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t start_pos, const void *out) {
+    if (!hs || !d_ids || !out) return ENGRAM_E_NULL;
+    if (T < 0 || start_pos < 0) return ENGRAM_E_INVALID;
+    if (start_pos + T > hs->max_seq) return ENGRAM_E_CAPACITY;
+    if (!aligned(d_ids, 4) || !aligned(out, 8)) return ENGRAM_E_ALIGN;
+    return ENGRAM_OK;
+}
+
+int check_rows(const uint8_t *table, const int64_t *ids, int64_t R, int64_t n_tok, int64_t id_stride,
+               int32_t C, const uint16_t *rows) {
+    if (!table || !ids || !rows) return ENGRAM_E_NULL;
+    if (R < 1 || n_tok < 0 || C < 1 || id_stride < C) return ENGRAM_E_INVALID;
+    if (!aligned(ids, 8) || !aligned(rows, 16)) return ENGRAM_E_ALIGN;
+    return ENGRAM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int engram_hash(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t start_pos,
+                int64_t *d_row_ids, uintptr_t stream) {
+    int rc = check_hash(hs, d_ids, T, start_pos, d_row_ids);
+    if (rc) return rc;
+    if (!err_ptr()) return ENGRAM_E_CUDA;
+    return cuda_rc(launch_hash(hash_args(hs, d_ids, T, start_pos, d_row_ids), S(stream)));
+}
+
+int engram_rows_fp8(const uint8_t *d_table, const float *d_scales, int64_t R, int32_t head_dim,
+                    int32_t scale_block, const int64_t *d_row_ids, int64_t n_tok, int64_t id_stride,
+                    int32_t C, uint16_t *d_rows, uintptr_t stream) {
+    int rc = check_rows(d_table, d_row_ids, R, n_tok, id_stride, C, d_rows);
+    if (rc) return rc;
+    if (!d_scales) return ENGRAM_E_NULL;
+    if (head_dim < 16 || head_dim > 1024 || head_dim % 16 || scale_block < 16 || scale_block % 16 ||
+        head_dim % scale_block)
+        return ENGRAM_E_INVALID;
+    if (!aligned(d_table, 16) || !aligned(d_scales, 4)) return ENGRAM_E_ALIGN;
+    RowsArgs a{d_table, d_scales, R, head_dim, scale_block, d_row_ids, n_tok, id_stride, C, d_rows, err_ptr()};
+    if (!a.err) return ENGRAM_E_CUDA;
+    return cuda_rc(launch_rows_fp8(a, S(stream)));
+}
+
+int engram_rows_q2k(const uint8_t *d_blocks, int64_t R, const int64_t *d_row_ids, int64_t n_tok,
+                    int64_t id_stride, int32_t C, uint16_t *d_rows, uintptr_t stream) {
+    int rc = check_rows(d_blocks, d_row_ids, R, n_tok, id_stride, C, d_rows);
+    if (rc) return rc;
+    if (!aligned(d_blocks, 4)) return ENGRAM_E_ALIGN;
+    RowsArgs a{d_blocks, nullptr, R, 256, 256, d_row_ids, n_tok, id_stride, C, d_rows, err_ptr()};
+    if (!a.err) return ENGRAM_E_CUDA;
+    return cuda_rc(launch_rows_q2k(a, S(stream)));
+}
+
+int engram_project(const uint16_t *d_x, const uint16_t *d_wkv, int32_t T, int32_t K, int32_t N,
+                   uint16_t *d_kv, uintptr_t stream) {
+    if (!d_x || !d_wkv || !d_kv) return ENGRAM_E_NULL;
+    if (T < 0 || K < 64 || K % 64 || N < 16 || N % 16) return ENGRAM_E_INVALID;
+    if (!aligned(d_x, 16) || !aligned(d_wkv, 16) || !aligned(d_kv, 16)) return ENGRAM_E_ALIGN;
+    if (T == 0) return ENGRAM_OK;
+    int *err = err_ptr();
+    if (!err) return ENGRAM_E_CUDA;
+    if (gemv_fits(T, K)) {
+        GemvArgs a{};
+        a.layer[0].wkv = d_wkv;
+        a.layer[0].kv = d_kv;
+        a.layer[0].x = d_x;
+        a.L = 1;
+        a.T = T;
+        a.K = K;
+        a.N = N;
+        a.gather = 0;
+        a.err = err;
+        return cuda_rc(launch_gemv(a, S(stream)));
+    }
+    return cuda_rc(launch_gemm(d_x, d_wkv, d_kv, T, N, K, err, S(stream)));
+}
+
+int engram_gate(float *d_h, const uint16_t *d_kv, const float *d_qk, int32_t T, int32_t hc, int32_t dim,
+                float eps, uintptr_t stream) {
+    if (!d_h || !d_kv || !d_qk) return ENGRAM_E_NULL;
+    if (hc < 1 || hc > 4) return ENGRAM_E_HC;
+    if (T < 0 || dim < 8 || dim % 8 || dim > 16384 || !(eps >= 0.0f)) return ENGRAM_E_INVALID;
+    if (!aligned(d_h, 16) || !aligned(d_kv, 16) || !aligned(d_qk, 16)) return ENGRAM_E_ALIGN;
+    GateArgs a{};
+    a.h = d_h;
+    a.kv[0] = d_kv;
+    a.qk[0] = d_qk;
+    a.L = 1;
+    a.M = T;
+    a.hc = hc;
+    a.D = dim;
+    a.eps = eps;
+    a.inv_sqrt_dim = powf((float)dim, -0.5f);
+    return cuda_rc(launch_gate(a, S(stream)));
+}
+
+int engram_workspace_layout(const engram_geom *geom, int64_t tokens, size_t *off) {
+    int rc = check_geom(geom);
+    if (rc) return rc;
+    if (!off) return ENGRAM_E_NULL;
+    if (tokens < 0) return ENGRAM_E_INVALID;
+    const engram_geom &g = *geom;
+    const size_t C = (size_t)cols(g), K = C * g.head_dim, N = (size_t)g.dim * (g.hc + 1);
+    size_t p = 0;
+    off[0] = p;
+    p += up256((size_t)tokens * g.n_layers * C * sizeof(int64_t));
+    for (int l = 0; l < g.n_layers; ++l) {
+        off[1 + l] = p;
+        p += up256((size_t)tokens * N * 2);
+    }
+    const bool need_x = !gemv_fits((int)(tokens > kSmallT ? kSmallT + 1 : tokens), (int)K);
+    for (int l = 0; l < g.n_layers; ++l) {
+        off[1 + g.n_layers + l] = p;
+        if (need_x) p += up256((size_t)tokens * K * 2);
+    }
+    off[1 + 2 * g.n_layers] = p;   // total (caller's array is sized 2 + 2 L by engram_workspace_bytes)
+    return ENGRAM_OK;
+}
+
+size_t engram_workspace_bytes(const engram_geom *geom, int64_t max_tokens) {
+    size_t off[2 + 2 * kMaxLayers];
+    if (engram_workspace_layout(geom, max_tokens, off) != ENGRAM_OK) return 0;
+    return off[1 + 2 * geom->n_layers];
+}
+
+int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
+                   int64_t start_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes, uintptr_t stream) {
+    if (!hs || !layers || !d_ids || !d_h || !d_ws) return ENGRAM_E_NULL;
+    int rc = check_hash(hs, d_ids, T, start_pos, d_ws);
+    if (rc) return rc;
+    const engram_geom &g = hs->t->g;
+    if (!(eps >= 0.0f)) return ENGRAM_E_INVALID;
+    if (!aligned(d_h, 16) || !aligned(d_ws, 256)) return ENGRAM_E_ALIGN;
+    const int L = g.n_layers, C = cols(g), hd = g.head_dim, K = C * hd, N = g.dim * (g.hc + 1);
+    for (int l = 0; l < L; ++l) {
+        const engram_layer &ly = layers[l];
+        if (!ly.table || !ly.wkv || !ly.qk) return ENGRAM_E_NULL;
+        if (ly.rows < 1) return ENGRAM_E_INVALID;
+        if (ly.fmt == ENGRAM_FMT_FP8) {
+            if (!ly.scales) return ENGRAM_E_NULL;
+            if (!aligned(ly.table, 16) || !aligned(ly.scales, 4)) return ENGRAM_E_ALIGN;
+        } else if (ly.fmt == ENGRAM_FMT_Q2K) {
+            if (hd != 256) return ENGRAM_E_INVALID;      // one Q2_K block per 256-wide row
+            if (!aligned(ly.table, 4)) return ENGRAM_E_ALIGN;
+        } else {
+            return ENGRAM_E_INVALID;
+        }
+        if (!aligned(ly.wkv, 16) || !aligned(ly.qk, 16)) return ENGRAM_E_ALIGN;
+    }
+    const int64_t M = (int64_t)hs->batch * T;
+    if (M > (int64_t)1 << 24) return ENGRAM_E_UNSUPPORTED;
+    if (ws_bytes < engram_workspace_bytes(&g, M)) return ENGRAM_E_WORKSPACE;
+    if (M == 0) return ENGRAM_OK;
+    int *err = err_ptr();
+    if (!err) return ENGRAM_E_CUDA;
+    cudaStream_t s = S(stream);
+    size_t off[2 + 2 * kMaxLayers];
+    engram_workspace_layout(&g, M, off);
+    uint8_t *ws = static_cast<uint8_t *>(d_ws);
+    int64_t *ids = reinterpret_cast<int64_t *>(ws + off[0]);
+
+    record(0, s);
+    cudaError_t e = launch_hash(hash_args(hs, d_ids, T, start_pos, ids), s);
+    if (e != cudaSuccess) return ENGRAM_E_CUDA;
+    record(1, s);
+
+    GateArgs ga{};
+    ga.h = d_h;
+    ga.L = L;
+    ga.M = (int32_t)M;
+    ga.hc = g.hc;
+    ga.D = g.dim;
+    ga.eps = eps;
+    ga.inv_sqrt_dim = powf((float)g.dim, -0.5f);
+    for (int l = 0; l < L; ++l) {
+        ga.kv[l] = reinterpret_cast<uint16_t *>(ws + off[1 + l]);
+        ga.qk[l] = layers[l].qk;
+    }
+
+    if (gemv_fits((int)M, K)) {
+        // Small step: one launch gathers every layer's rows into shared memory
+        // and streams every layer's wkv.
+        GemvArgs a{};
+        for (int l = 0; l < L; ++l) {
+            a.layer[l].wkv = layers[l].wkv;
+            a.layer[l].kv = reinterpret_cast<uint16_t *>(ws + off[1 + l]);
+            a.layer[l].table = static_cast<const uint8_t *>(layers[l].table);
+            a.layer[l].scales = layers[l].scales;
+            a.layer[l].rows = layers[l].rows;
+            a.layer[l].ids = ids + (int64_t)l * C;
+            a.layer[l].fmt = layers[l].fmt;
+        }
+        a.L = L;
+        a.T = (int32_t)M;
+        a.K = K;
+        a.N = N;
+        a.hd = hd;
+        a.blk = g.scale_block;
+        a.C = C;
+        a.id_stride = (int64_t)L * C;
+        a.gather = 1;
+        a.err = err;
+        record(2, s);
+        if (launch_gemv(a, s) != cudaSuccess) return ENGRAM_E_CUDA;
+        record(3, s);
+    } else {
+        for (int l = 0; l < L; ++l) {
+            RowsArgs ra{static_cast<const uint8_t *>(layers[l].table), layers[l].scales, layers[l].rows,
+                        hd, g.scale_block, ids + (int64_t)l * C, M, (int64_t)L * C, C,
+                        reinterpret_cast<uint16_t *>(ws + off[1 + L + l]), err};
+            e = layers[l].fmt == ENGRAM_FMT_FP8 ? launch_rows_fp8(ra, s) : launch_rows_q2k(ra, s);
+            if (e != cudaSuccess) return ENGRAM_E_CUDA;
+        }
+        record(2, s);
+        for (int l = 0; l < L; ++l) {
+            e = launch_gemm(reinterpret_cast<uint16_t *>(ws + off[1 + L + l]), layers[l].wkv,
+                            reinterpret_cast<uint16_t *>(ws + off[1 + l]), (int)M, N, K, err, s);
+            if (e != cudaSuccess) return ENGRAM_E_CUDA;
+        }
+        record(3, s);
+    }
+    if (launch_gate(ga, s) != cudaSuccess) return ENGRAM_E_CUDA;
+    record(4, s);
+    return ENGRAM_OK;
+}
+
+int engram_forward_host(engram_hasher *hs, const engram_layer *layers, const int32_t *h_ids, int32_t *d_ids,
+                        int32_t T, int64_t start_pos, float *h_h, float *d_h, float eps, void *d_ws,
+                        size_t ws_bytes, uintptr_t stream) {
+    if (!hs || !h_ids || !d_ids || !h_h || !d_h) return ENGRAM_E_NULL;
+    if (T < 0) return ENGRAM_E_INVALID;
+    const engram_geom &g = hs->t->g;
+    const size_t M = (size_t)hs->batch * T;
+    const size_t hbytes = M * g.hc * g.dim * sizeof(float);
+    cudaStream_t s = S(stream);
+    if (start_pos < 0 || start_pos + T > hs->max_seq) return ENGRAM_E_CAPACITY;
+    if (ws_bytes < engram_workspace_bytes(&g, (int64_t)M)) return ENGRAM_E_WORKSPACE;
+    if (cudaMemcpyAsync(d_ids, h_ids, M * sizeof(int32_t), cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return ENGRAM_E_CUDA;
+    if (cudaMemcpyAsync(d_h, h_h, hbytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return ENGRAM_E_CUDA;
+    int rc = engram_forward(hs, layers, d_ids, T, start_pos, d_h, eps, d_ws, ws_bytes, stream);
+    if (rc) return rc;
+    return cuda_rc(cudaMemcpyAsync(h_h, d_h, hbytes, cudaMemcpyDeviceToHost, s));
+}
+
+}  // extern "C"

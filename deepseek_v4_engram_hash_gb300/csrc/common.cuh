@@ -1,0 +1,136 @@
+// common.cuh -- device helpers and launcher declarations shared by the
+// libengram translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/engram.h"
+
+namespace engram {
+
+constexpr int kMaxLayers = 4;
+constexpr int kMaxNgram = 16;
+constexpr int kSmallT = 8;          // tokens at or below this run the fused GEMV
+
+// ---------------------------------------------------------------------------
+// Sticky device error word: the first error code wins; kernels never trap.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_err(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Number formats
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
+    return __uint_as_float(bits16 << 16);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Round-to-nearest-even f32 -> bf16 bits (cvt.rn.bf16.f32).
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float x) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Four e4m3 codes (one 32-bit word, little-endian) times a power-of-two
+// scale -> four bf16, packed in two words.  e4m3 -> f16 is exact (hardware
+// cvt), f16 -> f32 exact, the f32 multiply by 2^k is exact unless it leaves
+// the f32 range, and the final cvt.rn.bf16 is round-to-nearest-even: the
+// same value as bf16_rne(e4m3_to_f32(b) * scale) in the CPU reference.
+__device__ __forceinline__ void e4m3x4_scaled_to_bf16(uint32_t codes, float scale,
+                                                      uint32_t &out01, uint32_t &out23) {
+    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(codes & 0xFFFFu), __NV_E4M3);
+    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(codes >> 16), __NV_E4M3);
+    float2 a = __half22float2(*reinterpret_cast<__half2 *>(&lo));
+    float2 b = __half22float2(*reinterpret_cast<__half2 *>(&hi));
+    out01 = pack_bf16x2(__fmul_rn(a.x, scale), __fmul_rn(a.y, scale));
+    out23 = pack_bf16x2(__fmul_rn(b.x, scale), __fmul_rn(b.y, scale));
+}
+
+// One Q2_K value: d * (sc & 15) * q - dmin * (sc >> 4); every product is exact
+// in f32, so only the subtraction rounds.
+__device__ __forceinline__ float q2k_value(float d, float dmin, uint32_t sc, uint32_t q) {
+    return __fsub_rn(__fmul_rn(__fmul_rn(d, (float)(sc & 15u)), (float)q),
+                     __fmul_rn(dmin, (float)(sc >> 4)));
+}
+
+// ---------------------------------------------------------------------------
+// Launchers (host side, defined in the kernel translation units)
+// ---------------------------------------------------------------------------
+struct HashArgs {
+    const int32_t *ids;
+    int32_t B, T;
+    int64_t start_pos;
+    const int64_t *token_map;
+    int64_t vocab, pad_id;
+    const int64_t *mult, *primes, *offsets;
+    int32_t L, ng, H;
+    int64_t *cache;
+    int64_t max_seq;
+    int64_t *out;
+    int *err;
+};
+cudaError_t launch_hash(const HashArgs &a, cudaStream_t s);
+
+struct RowsArgs {
+    const uint8_t *table;   // fp8 codes [R, hd] or q2k blocks [R, 84]
+    const float *scales;    // fp8 only
+    int64_t R;
+    int32_t hd, blk;
+    const int64_t *ids;     // ids[t * id_stride + c]
+    int64_t n_tok, id_stride;
+    int32_t C;
+    uint16_t *out;          // [n_tok * C, hd] bf16
+    int *err;
+};
+cudaError_t launch_rows_fp8(const RowsArgs &a, cudaStream_t s);
+cudaError_t launch_rows_q2k(const RowsArgs &a, cudaStream_t s);
+
+// Small-T GEMV, optionally with the row gather fused into the x staging.
+struct GemvLayer {
+    const uint16_t *wkv;    // [N, K]
+    uint16_t *kv;           // [T, N]
+    const uint16_t *x;      // plain x [T, K] (gather == 0)
+    const uint8_t *table;   // gather source (gather == 1)
+    const float *scales;
+    int64_t rows;
+    const int64_t *ids;     // ids[t * id_stride + c] of this layer
+    int32_t fmt;
+};
+struct GemvArgs {
+    GemvLayer layer[kMaxLayers];
+    int32_t L, T, K, N;
+    int32_t hd, blk, C;
+    int64_t id_stride;
+    int32_t gather;
+    int *err;
+};
+cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t s);
+size_t gemv_smem_bytes(int T, int K);
+
+// GEMM: kv [M, N] = bf16(x [M, K] . wkv [N, K]^T).
+cudaError_t launch_gemm(const uint16_t *x, const uint16_t *wkv, uint16_t *kv, int M, int N, int K,
+                        int *err, cudaStream_t s);
+cudaError_t launch_gemm_simt(const uint16_t *x, const uint16_t *wkv, uint16_t *kv, int M, int N,
+                             int K, cudaStream_t s);
+
+// Gate over several layers on one highway.
+struct GateArgs {
+    float *h;                           // [M, hc, D]
+    const uint16_t *kv[kMaxLayers];     // [M, (hc+1) D]
+    const float *qk[kMaxLayers];        // [hc, D]
+    int32_t L, M, hc, D;
+    float eps, inv_sqrt_dim;
+};
+cudaError_t launch_gate(const GateArgs &a, cudaStream_t s);
+
+}  // namespace engram

@@ -1,0 +1,125 @@
+// gate.cu -- the engram gate (stage 4) for one or more layers on one highway.
+//
+// `gate_and_add` (metrale_model_arch/deepseek_v41_ref/engram.rs) on the FP32
+// highway of spark_model/layers/engram_v41.rs (module doc, item 4), per token
+// t and stream c, with key = kv[t, c D : (c+1) D], value = kv[t, hc D : (hc+1) D]:
+//   hh = sum h^2, kk = sum key^2, dot = sum (h (q k)) key
+//   s  = dot * (1/sqrt(hh/D + eps) * 1/sqrt(kk/D + eps)) * D^-1/2
+//   g  = copysign(sqrt(max(|s|, 1e-6)), s)
+//   h += sigmoid(g) * value.
+//
+// One CTA per (token, stream) row of D values.  The row stays in registers
+// across the layers: layer l+1's norms and dot are taken on the highway that
+// layer l just updated, so the highway is read and written once for all
+// layers.  Reductions: per-thread f32 sums, a warp butterfly, then the
+// per-warp partials summed in warp order -- a fixed order, reproducible.
+#include "common.cuh"
+
+namespace engram {
+
+constexpr int kGateThreads = 256;
+
+__device__ __forceinline__ void block_sum3(float &a, float &b, float &c, float *red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, off);
+        b += __shfl_xor_sync(0xFFFFFFFFu, b, off);
+        c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();                                  // red[] free from the last use
+    if (lane == 0) {
+        red[3 * warp + 0] = a;
+        red[3 * warp + 1] = b;
+        red[3 * warp + 2] = c;
+    }
+    __syncthreads();
+    a = b = c = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kGateThreads / 32; ++w) {
+        a += red[3 * w + 0];
+        b += red[3 * w + 1];
+        c += red[3 * w + 2];
+    }
+}
+
+// NV = float4 chunks per thread (D <= kGateThreads * 4 * NV).
+template <int NV>
+__global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constant__ GateArgs a) {
+    __shared__ float red[3 * kGateThreads / 32];
+    const int row = blockIdx.x;                       // (t, c)
+    const int t = row / a.hc, c = row % a.hc;
+    const int D = a.D, D4 = D >> 2;
+    const int N = D * (a.hc + 1);
+    float4 *hrow = reinterpret_cast<float4 *>(a.h + (size_t)row * D);
+    float4 h[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int i = threadIdx.x + v * kGateThreads;
+        h[v] = i < D4 ? hrow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int l = 0; l < a.L; ++l) {
+        const uint16_t *kvt = a.kv[l] + (size_t)t * N;
+        const uint2 *key = reinterpret_cast<const uint2 *>(kvt + (size_t)c * D);
+        const uint2 *val = reinterpret_cast<const uint2 *>(kvt + (size_t)a.hc * D);
+        const float4 *qk = reinterpret_cast<const float4 *>(a.qk[l] + (size_t)c * D);
+        uint2 kb[NV], vb[NV];
+        float4 q[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int i = threadIdx.x + v * kGateThreads;
+            if (i < D4) {
+                kb[v] = __ldg(key + i);
+                vb[v] = __ldg(val + i);
+                q[v] = __ldg(qk + i);
+            } else {
+                kb[v] = vb[v] = make_uint2(0, 0);
+                q[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float hh = 0.f, kk = 0.f, dot = 0.f;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const float k0 = bf16_lo(kb[v].x), k1 = bf16_hi(kb[v].x);
+            const float k2 = bf16_lo(kb[v].y), k3 = bf16_hi(kb[v].y);
+            hh = fmaf(h[v].x, h[v].x, hh); hh = fmaf(h[v].y, h[v].y, hh);
+            hh = fmaf(h[v].z, h[v].z, hh); hh = fmaf(h[v].w, h[v].w, hh);
+            kk = fmaf(k0, k0, kk); kk = fmaf(k1, k1, kk);
+            kk = fmaf(k2, k2, kk); kk = fmaf(k3, k3, kk);
+            dot = fmaf(h[v].x * q[v].x, k0, dot); dot = fmaf(h[v].y * q[v].y, k1, dot);
+            dot = fmaf(h[v].z * q[v].z, k2, dot); dot = fmaf(h[v].w * q[v].w, k3, dot);
+        }
+        block_sum3(hh, kk, dot, red);
+        const float rstd = (1.0f / sqrtf(hh / (float)D + a.eps)) * (1.0f / sqrtf(kk / (float)D + a.eps));
+        const float s = dot * rstd * a.inv_sqrt_dim;
+        const float g = copysignf(sqrtf(fmaxf(fabsf(s), 1e-6f)), s);
+        const float gate = 1.0f / (1.0f + expf(-g));
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            h[v].x = __fadd_rn(h[v].x, __fmul_rn(gate, bf16_lo(vb[v].x)));
+            h[v].y = __fadd_rn(h[v].y, __fmul_rn(gate, bf16_hi(vb[v].x)));
+            h[v].z = __fadd_rn(h[v].z, __fmul_rn(gate, bf16_lo(vb[v].y)));
+            h[v].w = __fadd_rn(h[v].w, __fmul_rn(gate, bf16_hi(vb[v].y)));
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int i = threadIdx.x + v * kGateThreads;
+        if (i < D4) hrow[i] = h[v];
+    }
+}
+
+cudaError_t launch_gate(const GateArgs &a, cudaStream_t s) {
+    if (a.M == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)a.M * a.hc;
+    const int per = kGateThreads * 4;
+    if (a.D <= per) gate_kernel<1><<<grid, kGateThreads, 0, s>>>(a);
+    else if (a.D <= 2 * per) gate_kernel<2><<<grid, kGateThreads, 0, s>>>(a);
+    else if (a.D <= 4 * per) gate_kernel<4><<<grid, kGateThreads, 0, s>>>(a);
+    else if (a.D <= 8 * per) gate_kernel<8><<<grid, kGateThreads, 0, s>>>(a);
+    else if (a.D <= 16 * per) gate_kernel<16><<<grid, kGateThreads, 0, s>>>(a);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace engram

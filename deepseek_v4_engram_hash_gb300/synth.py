@@ -249,7 +249,7 @@ def _synth_lib():
             raise RuntimeError("libengram_synth.so is not built; run __graft_entry__.build()")
         L = ctypes.CDLL(path)
         u64, i64, P, f32 = ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
-        L.synth_fp8_table.argtypes = [u64, u64, i64, ctypes.c_int, ctypes.c_int, P, P, P]
+        L.synth_fp8_table.argtypes = [u64, u64, i64, ctypes.c_int, ctypes.c_int, f32, P, P, P]
         L.synth_q2k_table.argtypes = [u64, i64, f32, f32, P, P]
         L.synth_bf16_normal.argtypes = [u64, i64, f32, P, P]
         L.synth_f32_normal.argtypes = [u64, i64, i64, f32, P, P]
@@ -273,7 +273,8 @@ def fill_table_fp8_cuda(cfg, layer: int, codes, scales):
     """codes: uint8 CUDA tensor [R, hd]; scales: float32 CUDA tensor [R, hd/blk]."""
     _check(_synth_lib().synth_fp8_table(
         stream_key(cfg.seed, f"table.{layer}"), stream_key(cfg.seed, f"scales.{layer}"),
-        codes.shape[0], cfg.head_dim, cfg.scale_block, ctypes.c_void_p(codes.data_ptr()),
+        codes.shape[0], cfg.head_dim, cfg.scale_block, float(normal_scale(1.0)),
+        ctypes.c_void_p(codes.data_ptr()),
         ctypes.c_void_p(scales.data_ptr()), _stream_of(codes)), "synth_fp8_table")
 
 

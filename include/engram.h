@@ -1,0 +1,192 @@
+/*
+ * engram.h -- C ABI of libengram, the GB300 (sm_103a) engram forward.
+ *
+ * The DeepSeek-V4.1 engram, per token and per engram layer (module docs of
+ * "spark_model/layers/engram_v41.rs" and "Module engram_v41"):
+ *   1. hash the n-gram window of compressed token ids into
+ *      C = (max_ngram - 1) * n_heads row ids;
+ *   2. gather and dequantise those C rows of the layer's table (fp8 e4m3 with
+ *      power-of-two scales, or 84-byte Q2_K blocks) into x [C * head_dim];
+ *   3. project kv = bf16(x . wkv^T), wkv [dim * (hc + 1), C * head_dim]:
+ *      one key of dim per hyper-connection stream, then one shared value;
+ *   4. gate: per stream c, s = <rmsnorm(h_c) (q k)_c, rmsnorm(key_c)> / sqrt(dim),
+ *      g = sign(s) sqrt(max(|s|, 1e-6)), h_c += sigmoid(g) * value, in place
+ *      on the FP32 highway h [tokens, hc, dim].
+ *
+ * Conventions for every entry point:
+ *   - Pointers named d_* are DEVICE pointers, h_* are HOST pointers.  The
+ *     caller owns every buffer it passes; the library keeps no pointer to it
+ *     after the call returns, except the opaque handles it creates itself.
+ *   - `stream` is a cudaStream_t passed as uintptr_t (0 = legacy default).
+ *     Every compute call only enqueues work on that stream: no host
+ *     synchronisation, no allocation, no host<->device copy (except
+ *     engram_forward_host, which enqueues its own copies).
+ *   - Return value: ENGRAM_OK (0) or a negative ENGRAM_E_* code.  Arguments
+ *     are validated on the host before anything is enqueued; a call that
+ *     returns an error has enqueued nothing.
+ *   - Conditions only the device can see (a token id outside token_map, a
+ *     row id outside a table) set a sticky per-device error word; the kernel
+ *     substitutes a safe value (the token is treated as unmapped, the row as
+ *     zeros) and never traps.  engram_check() synchronises the stream and
+ *     returns and clears that word.
+ */
+#ifndef ENGRAM_H
+#define ENGRAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ENGRAM_OK 0
+#define ENGRAM_E_INVALID -1     /* geometry or argument out of range */
+#define ENGRAM_E_NULL -2        /* a required pointer is null */
+#define ENGRAM_E_ALIGN -3       /* a pointer misses its required alignment */
+#define ENGRAM_E_CAPACITY -4    /* start_pos + T exceeds the hasher's max_seq */
+#define ENGRAM_E_WORKSPACE -5   /* workspace smaller than engram_workspace_bytes() */
+#define ENGRAM_E_HC -6          /* hc outside 1..4 */
+#define ENGRAM_E_TOKEN -7       /* device: an input token id outside token_map */
+#define ENGRAM_E_ROW -8         /* device: a row id outside its table */
+#define ENGRAM_E_CUDA -9        /* a CUDA runtime call failed */
+#define ENGRAM_E_TIMEOUT -10    /* device: a bounded wait gave up */
+#define ENGRAM_E_UNSUPPORTED -11 /* shape outside what the kernels handle */
+
+#define ENGRAM_FMT_FP8 0        /* e4m3 codes [rows, head_dim] + f32 scales [rows, head_dim / scale_block] */
+#define ENGRAM_FMT_Q2K 1        /* 84-byte Q2_K super-blocks [rows, 84]; head_dim must be 256 */
+
+/* Geometry.  C = (max_ngram - 1) * n_heads, K = C * head_dim, N = dim * (hc + 1).
+ * Limits: 1 <= n_layers <= 4; 2 <= max_ngram <= 16; n_heads >= 1;
+ * head_dim % 16 == 0, 16 <= head_dim <= 1024; scale_block % 16 == 0 and
+ * divides head_dim; dim % 8 == 0, dim <= 16384; 1 <= hc <= 4
+ * (EngramV41::new refuses other hc); vocab >= 1. */
+typedef struct {
+    int32_t n_layers, max_ngram, n_heads, head_dim, dim, hc, scale_block;
+    int64_t vocab;
+} engram_geom;
+
+typedef struct engram_tables engram_tables;   /* device copies of the hash tables */
+typedef struct engram_hasher engram_hasher;   /* per-batch look-back cache */
+
+/* Hash tables: spark_model/layers/engram_v41.rs, `EngramHashTables::from_flat`.
+ * Host arrays, copied to the current device:
+ *   h_token_map   [vocab]                    compressed id per token, -1 = unmapped
+ *   pad_token_id  pad_id = h_token_map[pad_token_id]
+ *   h_multipliers [n_layers * max_ngram]     multipliers[layer][lookback]
+ *   h_primes      [n_layers * C]             primes[layer][(ngram - 2) * n_heads + head]
+ *   h_offsets     [n_layers * C]             offsets, same layout
+ * Errors: ENGRAM_E_INVALID for bad geometry, pad_token_id outside token_map,
+ * a multiplier/prime/offset above INT64_MAX or a prime of 0; ENGRAM_E_HC;
+ * ENGRAM_E_CUDA if device allocation fails (set-up, not the hot path). */
+int engram_tables_create(const engram_geom *geom, const int64_t *h_token_map,
+                         int64_t pad_token_id, const uint64_t *h_multipliers,
+                         const uint64_t *h_primes, const uint64_t *h_offsets,
+                         engram_tables **out);
+void engram_tables_destroy(engram_tables *t);
+
+/* Look-back cache [batch, max_seq] of compressed ids, zero-filled like
+ * `EngramHasher::new` / `NgramHashState::new`, so decode steps see the
+ * prefill's ids.  The hasher borrows `t`, which must outlive it. */
+int engram_hasher_create(const engram_tables *t, int32_t batch, int64_t max_seq,
+                         engram_hasher **out);
+/* `EngramHasher::reset`: the cache returns to zeros (enqueued on `stream`). */
+int engram_hasher_reset(engram_hasher *hs, uintptr_t stream);
+void engram_hasher_destroy(engram_hasher *hs);
+
+/* Stage 1, `EngramHasher::hash` / `NgramHashState::forward`:
+ *   d_ids     [batch, T] int32 token ids at positions start_pos .. start_pos+T-1
+ *   d_row_ids [batch, T, n_layers, C] int64 out
+ * Writes the new positions into the cache.  The i64 arithmetic (wrapping
+ * multiply, XOR roll, Euclidean remainder, + offset) is bit-exact.
+ * Errors: ENGRAM_E_CAPACITY if start_pos + T > max_seq; device: ENGRAM_E_TOKEN. */
+int engram_hash(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t start_pos,
+                int64_t *d_row_ids, uintptr_t stream);
+
+/* Stage 2, fp8 rows (engram.rs CPU reference, `regen_table` + `embed_rows`):
+ *   row(id)[d] = bf16_rne(e4m3(d_table[id, d]) * d_scales[id, d / scale_block])
+ * for id = d_row_ids[t * id_stride + c], written to d_rows[(t * C + c), :].
+ *   d_table [R, head_dim] u8 (16-byte aligned), d_scales [R, head_dim/scale_block] f32,
+ *   d_rows [n_tok * C, head_dim] bf16 (16-byte aligned).  Bit-exact. */
+int engram_rows_fp8(const uint8_t *d_table, const float *d_scales, int64_t R, int32_t head_dim,
+                    int32_t scale_block, const int64_t *d_row_ids, int64_t n_tok,
+                    int64_t id_stride, int32_t C, uint16_t *d_rows, uintptr_t stream);
+
+/* Stage 2, Q2_K rows (spark_model/layers/engram_v41.rs, `rows_from_q2k`;
+ * head_dim 256): d_blocks [R, 84] u8 (4-byte aligned), ggml Q2_K layout,
+ * decoded y = d * (sc & 15) * q - dmin * (sc >> 4), then bf16 RNE.  Bit-exact. */
+int engram_rows_q2k(const uint8_t *d_blocks, int64_t R, const int64_t *d_row_ids, int64_t n_tok,
+                    int64_t id_stride, int32_t C, uint16_t *d_rows, uintptr_t stream);
+
+/* Stage 3 (engram.rs CPU reference, `linear_bf16`): d_kv[t, o] =
+ * bf16_rne(sum_i d_x[t, i] * d_wkv[o, i]) with f32 accumulation.
+ *   d_x [T, K] bf16, d_wkv [N, K] bf16, d_kv [T, N] bf16; all 16-byte aligned.
+ * K % 64 == 0, N % 16 == 0.  T <= 8 runs the bandwidth-bound GEMV, larger T
+ * the tcgen05 tensor-core GEMM. */
+int engram_project(const uint16_t *d_x, const uint16_t *d_wkv, int32_t T, int32_t K, int32_t N,
+                   uint16_t *d_kv, uintptr_t stream);
+
+/* Stage 4 (engram.rs CPU reference, `gate_and_add`, on the FP32 highway):
+ *   d_h [T, hc, dim] f32 in/out (16-byte aligned); d_kv [T, (hc+1) dim] bf16;
+ *   d_qk [hc, dim] f32 = q_weight * k_weight (exact for bf16 weights,
+ *   `EngramV41::upload_qk`). */
+int engram_gate(float *d_h, const uint16_t *d_kv, const float *d_qk, int32_t T, int32_t hc,
+                int32_t dim, float eps, uintptr_t stream);
+
+/* One engram layer for engram_forward. */
+typedef struct {
+    const void *table;      /* FP8: e4m3 [rows, head_dim]; Q2K: blocks [rows, 84] */
+    const float *scales;    /* FP8: [rows, head_dim / scale_block]; Q2K: unused */
+    int64_t rows;           /* table rows (sum of the layer's primes) */
+    int32_t fmt;            /* ENGRAM_FMT_FP8 or ENGRAM_FMT_Q2K */
+    const uint16_t *wkv;    /* [dim * (hc + 1), C * head_dim] bf16 */
+    const float *qk;        /* [hc, dim] f32 */
+} engram_layer;
+
+/* The whole forward for n_layers engram layers (in `layers` order) on one
+ * highway: one hash launch for every layer (as `V41Runtime.step_hashes`
+ * reuses it), then rows -> projection per layer, then the gates.
+ *   d_ids [batch, T] int32 at positions start_pos..; d_h [batch * T, hc, dim]
+ *   f32 in/out; d_ws device workspace of at least
+ *   engram_workspace_bytes(geom, batch * T) bytes, 256-byte aligned.
+ * After the call the workspace holds (offsets from engram_workspace_layout):
+ *   row ids [batch*T, n_layers, C] int64, then per layer kv [batch*T, N] bf16. */
+int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids,
+                   int32_t T, int64_t start_pos, float *d_h, float eps, void *d_ws,
+                   size_t ws_bytes, uintptr_t stream);
+
+/* engram_forward from host buffers: enqueues the copy of h_ids [batch, T]
+ * and h_h [batch*T, hc, dim] (pinned host memory recommended) into the
+ * device staging buffers d_ids / d_h, the forward, and the copy of d_h back
+ * into h_h.  The caller synchronises `stream` before reading h_h. */
+int engram_forward_host(engram_hasher *hs, const engram_layer *layers, const int32_t *h_ids,
+                        int32_t *d_ids, int32_t T, int64_t start_pos, float *h_h, float *d_h,
+                        float eps, void *d_ws, size_t ws_bytes, uintptr_t stream);
+
+/* Workspace bytes engram_forward needs for up to max_tokens = batch * T. */
+size_t engram_workspace_bytes(const engram_geom *geom, int64_t max_tokens);
+
+/* Byte offsets inside the workspace for `tokens` tokens: off[0] = row ids,
+ * off[1 + l] = kv of layer l, off[1 + n_layers + l] = gathered rows x of
+ * layer l (present only when tokens > 8), off[1 + 2 n_layers] = total bytes.
+ * off must hold 2 + 2 * n_layers entries. */
+int engram_workspace_layout(const engram_geom *geom, int64_t tokens, size_t *off);
+
+/* Optional stage timing: when set, engram_forward records on its stream
+ * events[0] before the hash, [1] after it, [2] after the row gather (== [1]
+ * where the gather is fused into the projection), [3] after the projection
+ * and [4] after the gate.  events holds 5 cudaEvent_t as uintptr_t; the
+ * library keeps the pointer (the array must stay alive) until it is set to
+ * NULL.  Process-wide; not thread-safe. */
+int engram_set_profile_events(const uintptr_t *events, int32_t n);
+
+/* Synchronises `stream`, then returns and clears the current device's
+ * sticky error word (ENGRAM_OK if none). */
+int engram_check(uintptr_t stream);
+
+const char *engram_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ENGRAM_H */
