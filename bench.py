@@ -1,0 +1,376 @@
+"""Benchmark of the engram forward on one GB300 (one JSON line on stdout).
+
+Default workload: the DeepSeek-V4.1-Flash-shaped single-token decode step
+(T = 1, both engram layers {1, 14}, hash included), after a 2048-token
+prefilled look-back; each timed step is one decode position.  A second
+measurement runs the T = 4096 prefill of the same geometry.
+
+  python bench.py [--steps K] [--warmup W] [--impl ours|reference] [--no-prefill]
+
+Under torchrun (WORLD_SIZE > 1) each rank runs its own replica on its own
+sequence (no data-path collective): value = all ranks' tokens / max rank time.
+--impl reference times the CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "engram tokens/s at T=1 and T=4096 (1 GB300); % of HBM / bf16 TC roofline"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _src_hash(*names) -> str:
+    h = hashlib.sha1()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "deepseek_v4_engram_hash_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:12]
+
+
+# DRAM bytes (read + write) per launch from one ncu capture, keyed by the
+# source hash of the kernel they were taken on; a changed kernel reports null.
+NCU_TRAFFIC = {}
+
+
+class Clocks:
+    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.rows, self.proc = gpu, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work
+# ---------------------------------------------------------------------------
+
+def row_bytes(cfg) -> int:
+    if cfg.fmt == "q2k":
+        return 84
+    return cfg.head_dim + (cfg.head_dim // cfg.scale_block) * 4
+
+
+def gemv_bytes(cfg, M) -> int:
+    """Fused gather + GEMV launch, all layers: wkv once, the rows, kv written."""
+    L = cfg.n_layers
+    return L * (cfg.N * cfg.K * 2 + M * cfg.cols * row_bytes(cfg) + M * cfg.N * 2)
+
+
+def step_bytes(cfg, M) -> int:
+    """Whole step (the roofline of the method): wkv once, rows, highway read +
+    write, q*k, ids and token_map entries; intermediates excluded."""
+    L = cfg.n_layers
+    return (L * (cfg.N * cfg.K * 2 + M * cfg.cols * row_bytes(cfg) + cfg.hc * cfg.dim * 4)
+            + M * cfg.hc * cfg.dim * 8 + M * 12)
+
+
+def gemm_flops(cfg, M) -> float:
+    return 2.0 * M * cfg.N * cfg.K * cfg.n_layers
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_decode(args, rank, world):
+    import torch
+    from deepseek_v4_engram_hash_gb300 import _lib as E
+    from deepseek_v4_engram_hash_gb300 import configs, runner, synth
+
+    cfg = configs.V41_DECODE.with_(seed=rank)
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=1)
+    n = args.warmup + args.steps
+    pre = eng.ids_for("prefix", cfg.prefix)
+    out = torch.empty((1, cfg.prefix, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
+    E.engram_hash(eng.hasher, torch.from_numpy(pre).cuda(), cfg.prefix, 0, out)
+    ids_all = torch.from_numpy(eng.ids_for("decode", n).reshape(n, 1, 1)).cuda()
+    d_h = torch.from_numpy(synth.highway(cfg, [cfg.prefix])).cuda()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    E.prepare_events([e for row in ev for e in row])
+    pos = cfg.prefix
+    for i in range(args.warmup):
+        eng.forward(ids_all[i], pos, d_h)
+        pos += 1
+    assert E.engram_check() == 0
+    _barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(torch.cuda.current_device()) as clk:
+        t0.record()
+        for i in range(args.steps):
+            E.engram_set_profile_events(ev[i])
+            eng.forward(ids_all[args.warmup + i], pos, d_h)
+            pos += 1
+        t1.record()
+        torch.cuda.synchronize()
+    E.engram_set_profile_events(None)
+    ms = t0.elapsed_time(t1) / args.steps
+    assert E.engram_check() == 0
+    stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in ev])  # ms
+    gemv_ms = float(stage[:, 2].mean())
+
+    # end to end through the host-buffer entry point: ids and highway copied in, highway out
+    h_ids = torch.from_numpy(eng.ids_for("e2e", n).reshape(n, 1, 1)).pin_memory()
+    h_h = torch.from_numpy(synth.highway(cfg, [0])).pin_memory()
+    d_ids = torch.empty((1, 1), dtype=torch.int32, device="cuda")
+    for i in range(args.warmup):
+        E.engram_forward_host(eng.hasher, eng.layers, h_ids[i], d_ids, 1, pos, h_h, d_h, cfg.eps, eng.ws,
+                              eng.ws_bytes)
+        pos += 1
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        E.engram_forward_host(eng.hasher, eng.layers, h_ids[args.warmup + i], d_ids, 1, pos, h_h, d_h,
+                              cfg.eps, eng.ws, eng.ws_bytes)
+        pos += 1
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    return dict(cfg=cfg, eng=eng, ms=ms, gemv_ms=gemv_ms, stage_ms=stage.mean(0).tolist(), clocks=clk.summary(),
+                e2e_ms=e2e_ms, h2d=4 + cfg.hc * cfg.dim * 4, d2h=cfg.hc * cfg.dim * 4)
+
+
+def run_prefill(args):
+    import torch
+    from deepseek_v4_engram_hash_gb300 import _lib as E
+    from deepseek_v4_engram_hash_gb300 import configs, runner, synth
+
+    cfg = configs.V41_PREFILL
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=cfg.T)
+    T = cfg.T
+    d_h = torch.empty((T, cfg.hc, cfg.dim), dtype=torch.float32, device="cuda")
+    synth.fill_highway_cuda(cfg, d_h)
+    ids = torch.from_numpy(eng.ids_for("prefill", T)).cuda()
+    steps, warm = args.prefill_steps, 3
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    E.prepare_events([e for row in ev for e in row])
+    for _ in range(warm):
+        eng.forward(ids, 0, d_h)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        E.engram_set_profile_events(ev[i])
+        eng.forward(ids, 0, d_h)
+    t1.record()
+    torch.cuda.synchronize()
+    E.engram_set_profile_events(None)
+    assert E.engram_check() == 0
+    stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in ev])
+    ms = t0.elapsed_time(t1) / steps
+    return dict(cfg=cfg, ms=ms, stage_ms=stage.mean(0).tolist())
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_decode_rate(budget_s: float, wkv_host=None):
+    """Oracle decode steps on the host cores for about budget_s seconds.
+    Returns (tokens/s, threads, steps)."""
+    import oracle
+    from deepseek_v4_engram_hash_gb300 import configs, synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle_glue as G
+
+    cfg = configs.V41_DECODE
+    if wkv_host is None:       # regenerate wkv on the host (input preparation, untimed)
+        wkv_host = [synth.wkv_rows(cfg, l, np.arange(cfg.N)) for l in range(cfg.n_layers)]
+    qk = [synth.qk_weights(cfg, l) for l in range(cfg.n_layers)]
+    st = G.hash_state(cfg, 1)
+    st.forward(synth.token_ids(cfg, "prefix.0", cfg.prefix)[None], 0)
+    h = synth.highway(cfg, [cfg.prefix])
+    ids = synth.token_ids(cfg, "decode.0", 4096)
+    pos, n, t_used = cfg.prefix, 0, 0.0
+    while t_used < budget_s and n < 4096:
+        rid = st.forward(ids[n:n + 1][None], pos)[0]          # hash [1, L, C]
+        rows = [G.rows(cfg, l, rid[:, l, :]) for l in range(cfg.n_layers)]   # includes table regen
+        t = time.perf_counter()
+        for l in range(cfg.n_layers):
+            kv = oracle.linear_bf16(rows[l].reshape(1, cfg.K), wkv_host[l])
+            h = oracle.gate(h, kv, qk[l][0], qk[l][1], cfg.hc, cfg.dim, cfg.eps)
+        t_used += time.perf_counter() - t
+        pos += 1
+        n += 1
+    return n / t_used, oracle.num_threads(), n
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    rate, threads, n = oracle_decode_rate(max(10.0, 0.5 * args.steps * 0.1))
+    line = {"metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 / rate, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "v41_decode_T1", "tokens_per_step": 1},
+            "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n} decode steps of the plain C oracle (projection + gate of both "
+                                       f"layers; hash and row gather untimed)"},
+            "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--prefill-steps", type=int, default=5)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import __graft_entry__
+    __graft_entry__.build()
+
+    hbm, bf16_burst, bf16_sust, peak_src = _peaks()
+    d = run_decode(args, rank, world)
+    cfg, M = d["cfg"], 1
+    ms = _max_over_ranks(d["ms"], world)
+    e2e_ms = _max_over_ranks(d["e2e_ms"], world)
+    gemv_gbs = gemv_bytes(cfg, M) / (d["gemv_ms"] * 1e-3) / 1e9
+    step_gbs = step_bytes(cfg, M) / (ms * 1e-3) / 1e9
+    key = _src_hash("gemv.cu")
+    traffic = NCU_TRAFFIC.get(("gemv", key))
+
+    pre = None
+    if not args.no_prefill and rank == 0:
+        p = run_prefill(args)
+        pc = p["cfg"]
+        gemm_ms = p["stage_ms"][2]
+        pre = {"workload": pc.name, "tokens_per_step": pc.T, "ms_per_step": p["ms"],
+               "value": pc.T / (p["ms"] * 1e-3), "unit": "tokens/s",
+               "stage_ms": dict(zip(["hash", "gather", "gemm", "gate"], p["stage_ms"])),
+               "roofline": {"bound": "tensor", "achieved": gemm_flops(pc, pc.T) / (gemm_ms * 1e-3) / 1e12,
+                            "peak": bf16_sust, "unit": "TFLOP/s",
+                            "frac": gemm_flops(pc, pc.T) / (gemm_ms * 1e-3) / 1e12 / bf16_sust,
+                            "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)"}}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        wkv_host = [d["eng"].layer_data[l]["wkv"].view(torch.int16).cpu().numpy().view(np.uint16)
+                    for l in range(cfg.n_layers)]
+        rate, threads, n = oracle_decode_rate(12.0, wkv_host)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} V4.1 decode steps (T=1) of the plain C oracle, projection + gate of both "
+                         f"layers timed; hash and row regeneration untimed"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": world * M / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "v41_decode_T1: V4.1-Flash engram decode step, T=1 per sequence, "
+                                   "layers {1,14}, 2048-token look-back, fp8 tables, dim 4096, hc 4",
+                       "tokens_per_step": M * world, "l2": "inputs larger than L2 (wkv 503 MB read per step)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+            "roofline": {"bound": "hbm", "achieved": gemv_gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gemv_gbs / hbm, "traffic": traffic,
+                         "kernel": "gemv_kernel<1> (fused row gather + wkv GEMV, both layers)",
+                         "algorithmic_bytes": gemv_bytes(cfg, M), "peak_source": f"{peak_src} hbm_gbs"},
+            "step_roofline": {"achieved": step_gbs, "frac": step_gbs / hbm, "algorithmic_bytes": step_bytes(cfg, M)},
+            "stage_ms": dict(zip(["hash", "gather", "gemv", "gate"], d["stage_ms"])),
+            "gpu_launches": 3 * args.steps,
+            "clocks": d["clocks"],
+            "e2e": {"value": world * M / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": d["h2d"], "d2h_bytes_per_step": d["d2h"]},
+            "cpu_baseline": cpu,
+            "prefill": pre,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

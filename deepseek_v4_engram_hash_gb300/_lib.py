@@ -227,18 +227,25 @@ def engram_workspace_layout(geom: engram_geom, tokens: int) -> list:
     return list(off)
 
 
+def prepare_events(events) -> None:
+    """Create the cudaEvent_t behind torch events (record each once, then sync)."""
+    for e in events:
+        e.record()
+    torch.cuda.synchronize()
+
+
 def engram_set_profile_events(events) -> None:
-    """events: list of 5 torch.cuda.Event (recorded by engram_forward), or None."""
+    """events: 5 torch.cuda.Event already created (prepare_events), or None."""
     global _prof_keep
     if events is None:
         _prof_keep = None
         _ok(lib().engram_set_profile_events(None, 0), "engram_set_profile_events")
         return
-    for e in events:
-        e.record()                         # materialise the underlying cudaEvent_t
-    torch.cuda.synchronize()
-    _prof_keep = (ctypes.c_uint64 * len(events))(*[e.cuda_event for e in events])
-    _ok(lib().engram_set_profile_events(ctypes.cast(_prof_keep, ctypes.c_void_p), len(events)),
+    handles = [e.cuda_event for e in events]
+    if not all(handles):
+        raise ValueError("profile events must be created first (prepare_events)")
+    _prof_keep = (ctypes.c_uint64 * len(handles))(*handles)
+    _ok(lib().engram_set_profile_events(ctypes.cast(_prof_keep, ctypes.c_void_p), len(handles)),
         "engram_set_profile_events")
 
 

@@ -1,0 +1,152 @@
+"""End-to-end parity of engram_forward on the five workloads.
+
+For every call: the row ids in the workspace equal the oracle's hash exactly;
+the kv of each layer in the workspace is within 2e-2 of the oracle projection
+of the oracle's own rows (all outputs on the tiny workload, a seeded sample of
+tokens x outputs on the V4.1-shaped ones); the highway is within 1e-3 of the
+oracle gates applied layer after layer to the GPU's kv (stage-wise).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle_glue as G
+from deepseek_v4_engram_hash_gb300 import configs, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def E():
+    import __graft_entry__
+    __graft_entry__.build()
+    from deepseek_v4_engram_hash_gb300 import _lib
+    return _lib
+
+
+def _u16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _check_call(eng, ref, ids, start_pos, d_h, h0_rows, tok_sample, out_sample, first_token):
+    """Run one forward and check it.  h0_rows: f32 [len(tok_sample), hc, D] of
+    the highway rows tok_sample before the call (regenerated on the CPU)."""
+    cfg = eng.cfg
+    B, T = ids.shape
+    M = B * T
+    eng.forward(ids, start_pos, d_h)
+    from deepseek_v4_engram_hash_gb300 import _lib as E
+    assert E.engram_check() == 0
+    want_ids = ref.forward(ids, start_pos).reshape(M, cfg.n_layers, cfg.cols)
+    got_ids = eng.row_ids(M).cpu().numpy()
+    assert np.array_equal(got_ids, want_ids), "row ids"
+    h = h0_rows.copy()
+    for l in range(cfg.n_layers):
+        kv_gpu = _u16(eng.kv(M, l))[tok_sample]                     # [S, N]
+        x = G.x_of(cfg, l, want_ids[tok_sample])
+        want_kv = G.kv(cfg, l, x, out_sample)
+        err = G.kv_rel_err(kv_gpu[:, out_sample], want_kv)
+        assert err <= G.KV_TOL, f"layer {l} kv rel err {err}"
+        h = G.gate(cfg, l, h, kv_gpu)                               # stage-wise
+    got_h = d_h.view(M, cfg.hc, cfg.dim)[torch.as_tensor(tok_sample, device=d_h.device)].cpu().numpy()
+    dh = np.abs(got_h - h).max()
+    assert dh <= G.H_TOL, f"highway |dh| {dh}"
+    return dh
+
+
+def _h_device(cfg, first_token, M, numpy_ok):
+    if numpy_ok:
+        return torch.from_numpy(synth.highway(cfg, np.arange(first_token, first_token + M))).cuda()
+    d_h = torch.empty((M, cfg.hc, cfg.dim), dtype=torch.float32, device="cuda")
+    synth.fill_highway_cuda(cfg, d_h, first_token)
+    return d_h
+
+
+def test_forward_tiny_full(E):
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = configs.TINY
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=cfg.T)
+    ref = G.hash_state(cfg, 1)
+    pos, first = 0, 0
+    for T in (cfg.T, 1, 1, 1, 5):                       # prefill (tensor path), decode (GEMV path)
+        ids = eng.ids_for(f"tiny{pos}", T)
+        d_h = _h_device(cfg, first, T, True)
+        h0 = d_h.cpu().numpy()
+        _check_call(eng, ref, ids, pos, d_h, h0, np.arange(T), np.arange(cfg.N), first)
+        pos += T
+        first += T
+
+
+def _sample(rng, n, k):
+    return np.sort(rng.choice(n, size=min(n, k), replace=False))
+
+
+@pytest.mark.parametrize("name", ["v41_decode_T1", "v41_prefill_T4096", "v41_q2k_T512"])
+def test_forward_v41(E, name):
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = configs.CONFIGS[name]
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=max(cfg.T, 1))
+    ref = G.hash_state(cfg, 1)
+    rng = np.random.default_rng(11)
+    pos = 0
+    if cfg.prefix:
+        from deepseek_v4_engram_hash_gb300 import _lib as EL
+        pre = eng.ids_for("prefix", cfg.prefix)
+        out = torch.empty((1, cfg.prefix, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
+        EL.engram_hash(eng.hasher, torch.from_numpy(pre).cuda(), cfg.prefix, 0, out)
+        assert np.array_equal(out.cpu().numpy(), ref.forward(pre, 0))
+        pos = cfg.prefix
+    calls = 3 if cfg.T == 1 else 1
+    outs = np.concatenate([np.arange(0, cfg.N, 97), [cfg.dim - 1, cfg.dim, cfg.hc * cfg.dim,
+                                                       cfg.N - 1]])
+    outs = np.unique(outs)
+    for i in range(calls):
+        T = cfg.T
+        ids = eng.ids_for(f"call{i}", T)
+        d_h = _h_device(cfg, pos, T, T <= 64)
+        toks = _sample(rng, T, 24) if T > 24 else np.arange(T)
+        h0 = synth.highway(cfg, pos + toks)
+        _check_call(eng, ref, ids, pos, d_h, h0, toks, outs, pos)
+        pos += T
+
+
+def test_forward_stress_batch8_prefill_then_decode(E):
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = configs.STRESS
+    B = cfg.batch
+    eng = runner.EngramSetup(cfg, batch=B, max_tokens=B * cfg.T)
+    ref = G.hash_state(cfg, B)
+    rng = np.random.default_rng(12)
+    outs = np.unique(np.concatenate([np.arange(5, cfg.N, 211), [cfg.N - 1]]))
+    ids = eng.ids_for("prefill", cfg.T)
+    M = B * cfg.T
+    d_h = _h_device(cfg, 0, M, False)
+    toks = _sample(rng, M, 16)
+    _check_call(eng, ref, ids, 0, d_h, synth.highway(cfg, toks), toks, outs, 0)
+    pos, first = cfg.T, M
+    for step in range(3):                               # single-token decode of all 8 sequences
+        ids = eng.ids_for(f"dec{step}", 1)
+        d_h = _h_device(cfg, first, B, True)
+        _check_call(eng, ref, ids, pos, d_h, d_h.cpu().numpy(), np.arange(B), outs, first)
+        pos += 1
+        first += B
+
+
+def test_forward_fused_gemv_matches_staged_calls(E):
+    """At one token the forward's fused gather + GEMV gives the same kv bits
+    as engram_rows_fp8 followed by engram_project."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = configs.V41_DECODE
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=1)
+    ids = eng.ids_for("fused", 1)
+    d_h = _h_device(cfg, 0, 1, True)
+    eng.forward(ids, 7, d_h)
+    row_ids = eng.row_ids(1).clone()
+    for l in range(cfg.n_layers):
+        d = eng.layer_data[l]
+        x = torch.empty((cfg.cols, cfg.head_dim), dtype=torch.bfloat16, device="cuda")
+        E.engram_rows_fp8(d["table"], d["scales"], d["rows"], cfg.head_dim, cfg.scale_block,
+                          row_ids[:, l, :].contiguous(), 1, cfg.cols, cfg.cols, x)
+        kv = torch.empty((1, cfg.N), dtype=torch.bfloat16, device="cuda")
+        E.engram_project(x, d["wkv"], 1, cfg.K, cfg.N, kv)
+        assert torch.equal(kv.view(torch.int16), eng.kv(1, l).view(torch.int16))
