@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
                                 P, sz, st], ctypes.c_int),
             "engram_forward_host": ([P, ctypes.POINTER(engram_layer), P, P, i32, i64, P, P,
                                      ctypes.c_float, P, sz, st], ctypes.c_int),
+            "engram_forward_noalloc": ([P, ctypes.POINTER(engram_layer), P, i32, i64, P, ctypes.c_float,
+                                        st], ctypes.c_int),
             "engram_workspace_bytes": ([ctypes.POINTER(engram_geom), i64], sz),
             "engram_workspace_layout": ([ctypes.POINTER(engram_geom), i64, ctypes.POINTER(sz)],
                                         ctypes.c_int),
@@ -215,6 +217,13 @@ def engram_forward_host(hs: Hasher, layers, h_ids, d_ids, T, start_pos, h_h, d_h
     _ok(lib().engram_forward_host(hs.handle, arr, _ptr(h_ids), _ptr(d_ids), int(T), int(start_pos),
                                   _ptr(h_h), _ptr(d_h), float(eps), _ptr(d_ws), int(ws_bytes),
                                   _stream(stream)), "engram_forward_host")
+
+
+def engram_forward_noalloc(hs: Hasher, layers, d_ids, T, start_pos, d_h, eps, stream=None):
+    """engram_forward with the library's fixed device scratch (no allocation)."""
+    arr = layers if isinstance(layers, ctypes.Array) else layers_array(layers)
+    _ok(lib().engram_forward_noalloc(hs.handle, arr, _ptr(d_ids), int(T), int(start_pos), _ptr(d_h),
+                                     float(eps), _stream(stream)), "engram_forward_noalloc")
 
 
 def engram_workspace_bytes(geom: engram_geom, max_tokens: int) -> int:

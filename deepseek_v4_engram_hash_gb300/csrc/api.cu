@@ -25,6 +25,16 @@ struct engram_hasher {
     int device;
 };
 
+namespace engram {
+// Geometry and batch of a hasher, for entry points defined in other files.
+bool hasher_geometry(const engram_hasher *hs, engram_geom *g, int *batch) {
+    if (!hs || !hs->t) return false;
+    *g = hs->t->g;
+    *batch = hs->batch;
+    return true;
+}
+}  // namespace engram
+
 // The sticky error word, one per device (this module's copy on each GPU).
 static __device__ int g_err_word;
 
@@ -104,6 +114,7 @@ const char *engram_strerror(int code) {
         case ENGRAM_E_CUDA: return "a CUDA runtime call failed";
         case ENGRAM_E_TIMEOUT: return "a bounded device wait gave up";
         case ENGRAM_E_UNSUPPORTED: return "shape outside what the kernels handle";
+        case ENGRAM_E_NOALLOC_LIMIT: return "request larger than the fixed scratch of engram_forward_noalloc";
         default: return "unknown engram error";
     }
 }

@@ -52,6 +52,7 @@ extern "C" {
 #define ENGRAM_E_CUDA -9        /* a CUDA runtime call failed */
 #define ENGRAM_E_TIMEOUT -10    /* device: a bounded wait gave up */
 #define ENGRAM_E_UNSUPPORTED -11 /* shape outside what the kernels handle */
+#define ENGRAM_E_NOALLOC_LIMIT -12 /* request larger than engram_forward_noalloc's fixed scratch */
 
 #define ENGRAM_FMT_FP8 0        /* e4m3 codes [rows, head_dim] + f32 scales [rows, head_dim / scale_block] */
 #define ENGRAM_FMT_Q2K 1        /* 84-byte Q2_K super-blocks [rows, 84]; head_dim must be 256 */
@@ -162,6 +163,28 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
 int engram_forward_host(engram_hasher *hs, const engram_layer *layers, const int32_t *h_ids,
                         int32_t *d_ids, int32_t T, int64_t start_pos, float *h_h, float *d_h,
                         float eps, void *d_ws, size_t ws_bytes, uintptr_t stream);
+
+/* engram_forward for callers that cannot allocate device memory.  (The pages
+ * have no counterpart: this entry point belongs to this library's ABI.)
+ * Code that runs where cudaMalloc is unavailable or unwelcome -- inside a host
+ * that owns every allocation itself, a real-time loop that must not enter the
+ * allocator, or a plugin with no allocator handle -- still needs the forward's
+ * scratch (row ids and per-layer kv, plus the gathered rows beyond 8 tokens).
+ * This entry point takes it from a fixed 4 MiB array that the library places
+ * in device memory (a file-scope __device__ array, held on every GPU that
+ * loads the library until the process exits), so the call allocates nothing.
+ *   Arguments and results are those of engram_forward without d_ws/ws_bytes.
+ *   A request whose workspace (engram_workspace_bytes for batch * T tokens)
+ *   exceeds 4 MiB is refused with ENGRAM_E_NOALLOC_LIMIT before anything is
+ *   enqueued; at the V4.1-Flash shape that is about 39 tokens a call.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call on a device shares the one array, which keeps the previous
+ *   call's contents (nothing in it needs to start at zero: each call writes
+ *   what it reads).  Calls whose work overlaps on the GPU -- on different
+ *   streams, or from different threads -- race on it: serialise them. */
+int engram_forward_noalloc(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids,
+                           int32_t T, int64_t start_pos, float *d_h, float eps, uintptr_t stream);
 
 /* Workspace bytes engram_forward needs for up to max_tokens = batch * T. */
 size_t engram_workspace_bytes(const engram_geom *geom, int64_t max_tokens);
