@@ -454,10 +454,22 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
             if (e != cudaSuccess) return ENGRAM_E_CUDA;
         }
         record(2, s);
+        const uint16_t *xs[kMaxLayers], *ws_[kMaxLayers];
+        uint16_t *kvs[kMaxLayers];
         for (int l = 0; l < L; ++l) {
-            e = launch_gemm(reinterpret_cast<uint16_t *>(ws + off[1 + L + l]), layers[l].wkv,
-                            reinterpret_cast<uint16_t *>(ws + off[1 + l]), (int)M, N, K, err, s);
+            xs[l] = reinterpret_cast<uint16_t *>(ws + off[1 + L + l]);
+            ws_[l] = layers[l].wkv;
+            kvs[l] = reinterpret_cast<uint16_t *>(ws + off[1 + l]);
+        }
+        if (gemm_tc_supported((int)M, N, K)) {
+            // every layer's tiles in one persistent tensor-core launch
+            e = launch_gemm_tc(L, xs, ws_, kvs, (int)M, N, K, err, s);
             if (e != cudaSuccess) return ENGRAM_E_CUDA;
+        } else {
+            for (int l = 0; l < L; ++l) {
+                e = launch_gemm_simt(xs[l], ws_[l], kvs[l], (int)M, N, K, s);
+                if (e != cudaSuccess) return ENGRAM_E_CUDA;
+            }
         }
         record(3, s);
     }

@@ -120,6 +120,9 @@ size_t gemv_smem_bytes(int T, int K);
 // GEMM: kv [M, N] = bf16(x [M, K] . wkv [N, K]^T).
 cudaError_t launch_gemm(const uint16_t *x, const uint16_t *wkv, uint16_t *kv, int M, int N, int K,
                         int *err, cudaStream_t s);
+bool gemm_tc_supported(int M, int N, int K);
+cudaError_t launch_gemm_tc(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
+                           int M, int N, int K, int *err, cudaStream_t s);
 cudaError_t launch_gemm_simt(const uint16_t *x, const uint16_t *wkv, uint16_t *kv, int M, int N,
                              int K, cudaStream_t s);
 

@@ -259,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         int i = 0;
         for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x, ++i) {
             const int acc = i & 1;
-            if (!mbar_wait(tfull(acc), (i >> 1) & 1, abort_flag, p.err)) break;
+            const bool ok = mbar_wait(tfull(acc), (i >> 1) & 1, abort_flag, p.err);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;          // reconverge before .sync.aligned loads
             tc_fence_after();
             const int l = tile / tiles_per_layer, r = tile % tiles_per_layer;
             const int m = (r % p.m_tiles) * BM + row, n0 = (r / p.m_tiles) * BN;
@@ -350,15 +351,16 @@ cudaError_t launch_gemm_tc(int L, const uint16_t *const *x, const uint16_t *cons
     p.m_tiles = (M + BM - 1) / BM;
     p.n_tiles = (N + BN - 1) / BN;
     p.err = err;
-    static bool attr = false;
-    if (!attr) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    static bool attr[64] = {};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr[dev]) {
         cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr = true;
+        attr[dev] = true;
     }
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int tiles = p.m_tiles * p.n_tiles * L;
     const int grid = tiles < sms ? tiles : sms;
