@@ -294,6 +294,8 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=5)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
+                    help="run one workload only (for profiling); prints its own JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -312,6 +314,11 @@ def main():
     __graft_entry__.build()
 
     hbm, bf16_burst, bf16_sust, peak_src = _peaks()
+    if args.only == "prefill":
+        p = run_prefill(args)
+        print(json.dumps({"workload": p["cfg"].name, "ms_per_step": p["ms"], "stage_ms": p["stage_ms"],
+                          "tokens_per_s": p["cfg"].T / (p["ms"] * 1e-3)}), flush=True)
+        return
     d = run_decode(args, rank, world)
     cfg, M = d["cfg"], 1
     ms = _max_over_ranks(d["ms"], world)
@@ -322,7 +329,7 @@ def main():
     traffic = NCU_TRAFFIC.get(("gemv", key))
 
     pre = None
-    if not args.no_prefill and rank == 0:
+    if not args.no_prefill and rank == 0 and args.only is None:
         p = run_prefill(args)
         pc = p["cfg"]
         gemm_ms = p["stage_ms"][2]
@@ -336,7 +343,7 @@ def main():
                             "kernel": "gemm_tc_kernel (tcgen05, both layers in one launch)"}}
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and args.only is None:
         wkv_host = [d["eng"].layer_data[l]["wkv"].view(torch.int16).cpu().numpy().view(np.uint16)
                     for l in range(cfg.n_layers)]
         rate, threads, n = oracle_decode_rate(12.0, wkv_host)
