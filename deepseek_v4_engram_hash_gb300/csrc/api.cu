@@ -401,9 +401,16 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
     uint8_t *ws = static_cast<uint8_t *>(d_ws);
     int64_t *ids = reinterpret_cast<int64_t *>(ws + off[0]);
 
+    // Small steps hash inside the projection kernel (each CTA hashes the ids
+    // of its own layer); larger ones run the hash kernel first.
+    const bool small = gemv_fits((int)M, K);
+    const bool fuse_hash = small && M * C <= kFusedHashMaxIds;
     record(0, s);
-    cudaError_t e = launch_hash(hash_args(hs, d_ids, T, start_pos, ids), s);
-    if (e != cudaSuccess) return ENGRAM_E_CUDA;
+    cudaError_t e = cudaSuccess;
+    if (!fuse_hash) {
+        e = launch_hash(hash_args(hs, d_ids, T, start_pos, ids), s);
+        if (e != cudaSuccess) return ENGRAM_E_CUDA;
+    }
     record(1, s);
 
     GateArgs ga{};
@@ -419,9 +426,10 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
         ga.qk[l] = layers[l].qk;
     }
 
-    if (gemv_fits((int)M, K)) {
-        // Small step: one launch gathers every layer's rows into shared memory
-        // and streams every layer's wkv.
+    if (small) {
+        // Small step: one launch hashes, gathers every layer's rows into shared
+        // memory and streams every layer's wkv; the gate follows it as a
+        // programmatic dependent launch.
         GemvArgs a{};
         for (int l = 0; l < L; ++l) {
             a.layer[l].wkv = layers[l].wkv;
@@ -441,7 +449,11 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
         a.C = C;
         a.id_stride = (int64_t)L * C;
         a.gather = 1;
+        a.fuse_hash = fuse_hash ? 1 : 0;
+        a.hash = hash_args(hs, d_ids, T, start_pos, ids);
+        a.pdl = 1;
         a.err = err;
+        ga.pdl = 1;
         record(2, s);
         if (launch_gemv(a, s) != cudaSuccess) return ENGRAM_E_CUDA;
         record(3, s);

@@ -81,6 +81,58 @@ struct HashArgs {
 };
 cudaError_t launch_hash(const HashArgs &a, cudaStream_t s);
 
+// Compressed id of input token s of sequence b (the token_map lookup); an id
+// outside token_map raises ENGRAM_E_TOKEN and reads as unmapped (-1).
+__device__ __forceinline__ int64_t hash_compress(const HashArgs &a, int b, int64_t s) {
+    const int32_t id = a.ids[(int64_t)b * a.T + s];
+    if (id < 0 || (int64_t)id >= a.vocab) {
+        set_err(a.err, ENGRAM_E_TOKEN);
+        return -1;
+    }
+    return a.token_map[id];
+}
+
+// Row id of (sequence b, position start_pos + s, layer li, column col):
+// `EngramHasher::hash` (spark_model/layers/engram_v41.rs) and
+// `NgramHashState::forward` (metrale_model_arch/deepseek_v41_ref/engram.rs).
+// The window holds the compressed ids at shifts 0..n (n = col / H + 1);
+// once a shift reaches before position 0 or an unmapped (-1) id, it and every
+// larger shift take pad_id.  rolling = tok0 * m0, then rolling ^= tok_k * m_k,
+// and the id is rem_euclid(rolling, prime) + offset, all i64 with wrap.  Ids
+// of this call come from the input through token_map, older positions from
+// the cache, so no thread depends on another thread's cache write.
+__device__ __forceinline__ int64_t hash_one(const HashArgs &a, int b, int s, int li, int col) {
+    const int C = (a.ng - 1) * a.H;
+    const int64_t pos = a.start_pos + s;
+    const int n_top = col / a.H + 1;
+    int64_t tok[kMaxNgram];
+    bool blocked = false;
+    for (int shift = 0; shift <= n_top; ++shift) {
+        int64_t src;
+        if (pos < shift) {
+            src = 0;                                 // blocked below; value unused
+        } else if (pos - shift >= a.start_pos) {
+            src = hash_compress(a, b, pos - shift - a.start_pos);
+        } else {
+            src = a.cache[(int64_t)b * a.max_seq + (pos - shift)];
+        }
+        blocked = blocked || pos < shift || src == -1;
+        tok[shift] = blocked ? a.pad_id : src;
+    }
+    const int64_t *m = a.mult + (int64_t)li * a.ng;
+    uint64_t rolling = (uint64_t)tok[0] * (uint64_t)m[0];
+    for (int n = 1; n <= n_top; ++n) rolling ^= (uint64_t)tok[n] * (uint64_t)m[n];
+    const int64_t p = a.primes[(int64_t)li * C + col];
+    int64_t r = (int64_t)rolling % p;
+    if (r < 0) r += p;
+    return (int64_t)((uint64_t)r + (uint64_t)a.offsets[(int64_t)li * C + col]);
+}
+
+// Programmatic dependent launch: wait for the grids this one depends on, and
+// let the next grid in the stream start its independent prologue.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 struct RowsArgs {
     const uint8_t *table;   // fp8 codes [R, hd] or q2k blocks [R, 84]
     const float *scales;    // fp8 only
@@ -112,8 +164,12 @@ struct GemvArgs {
     int32_t hd, blk, C;
     int64_t id_stride;
     int32_t gather;
+    int32_t fuse_hash;      // compute the row ids in-kernel (hash below), write them to ids_out
+    HashArgs hash;          // hash.out = row ids [T, L, C] in the workspace
+    int32_t pdl;            // launched as a programmatic dependent
     int *err;
 };
+constexpr int kFusedHashMaxIds = 2048;  // T * C row ids a CTA may hash for its layer
 cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t s);
 size_t gemv_smem_bytes(int T, int K);
 
@@ -133,6 +189,7 @@ struct GateArgs {
     const float *qk[kMaxLayers];        // [hc, D]
     int32_t L, M, hc, D;
     float eps, inv_sqrt_dim;
+    int32_t pdl;            // launched as a programmatic dependent of the projection
 };
 cudaError_t launch_gate(const GateArgs &a, cudaStream_t s);
 

@@ -43,51 +43,81 @@ __device__ __forceinline__ void block_sum3(float &a, float &b, float &c, float *
     }
 }
 
-// NV = float4 chunks per thread (D <= kGateThreads * 4 * NV).
+// The per-layer operands of one thread: NV chunks of 4 key and value bf16
+// and 4 q*k f32 values.
+template <int NV>
+struct GateChunk {
+    uint2 kb[NV], vb[NV];
+    float4 q[NV];
+};
+
+template <int NV>
+__device__ __forceinline__ void load_qk(const GateArgs &a, int l, int c, GateChunk<NV> &g) {
+    const int D4 = a.D >> 2;
+    const float4 *qk = reinterpret_cast<const float4 *>(a.qk[l] + (size_t)c * a.D);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int i = threadIdx.x + v * kGateThreads;
+        g.q[v] = i < D4 ? __ldg(qk + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+template <int NV>
+__device__ __forceinline__ void load_kv(const GateArgs &a, int l, int t, int c, GateChunk<NV> &g) {
+    const int D4 = a.D >> 2;
+    const size_t N = (size_t)a.D * (a.hc + 1);
+    const uint16_t *kvt = a.kv[l] + (size_t)t * N;
+    const uint2 *key = reinterpret_cast<const uint2 *>(kvt + (size_t)c * a.D);
+    const uint2 *val = reinterpret_cast<const uint2 *>(kvt + (size_t)a.hc * a.D);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int i = threadIdx.x + v * kGateThreads;
+        g.kb[v] = i < D4 ? key[i] : make_uint2(0, 0);
+        g.vb[v] = i < D4 ? val[i] : make_uint2(0, 0);
+    }
+}
+
+// NV = float4 chunks per thread (D <= kGateThreads * 4 * NV).  Up to NV = 4
+// the next layer's operands are loaded while this layer reduces.
 template <int NV>
 __global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constant__ GateArgs a) {
+    constexpr bool kPipe = NV <= 4;
     __shared__ float red[3 * kGateThreads / 32];
     const int row = blockIdx.x;                       // (t, c)
     const int t = row / a.hc, c = row % a.hc;
     const int D = a.D, D4 = D >> 2;
-    const int N = D * (a.hc + 1);
     float4 *hrow = reinterpret_cast<float4 *>(a.h + (size_t)row * D);
+    // The highway and the first q*k do not depend on the projection: load
+    // them before waiting for it.
     float4 h[NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int i = threadIdx.x + v * kGateThreads;
         h[v] = i < D4 ? hrow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    GateChunk<NV> cur, nxt;
+    load_qk(a, 0, c, cur);
+    if (a.pdl) {
+        griddep_wait();
+        griddep_launch();
+    }
+    load_kv(a, 0, t, c, cur);
     for (int l = 0; l < a.L; ++l) {
-        const uint16_t *kvt = a.kv[l] + (size_t)t * N;
-        const uint2 *key = reinterpret_cast<const uint2 *>(kvt + (size_t)c * D);
-        const uint2 *val = reinterpret_cast<const uint2 *>(kvt + (size_t)a.hc * D);
-        const float4 *qk = reinterpret_cast<const float4 *>(a.qk[l] + (size_t)c * D);
-        uint2 kb[NV], vb[NV];
-        float4 q[NV];
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int i = threadIdx.x + v * kGateThreads;
-            if (i < D4) {
-                kb[v] = __ldg(key + i);
-                vb[v] = __ldg(val + i);
-                q[v] = __ldg(qk + i);
-            } else {
-                kb[v] = vb[v] = make_uint2(0, 0);
-                q[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+        if (kPipe && l + 1 < a.L) {
+            load_qk(a, l + 1, c, nxt);
+            load_kv(a, l + 1, t, c, nxt);
         }
         float hh = 0.f, kk = 0.f, dot = 0.f;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const float k0 = bf16_lo(kb[v].x), k1 = bf16_hi(kb[v].x);
-            const float k2 = bf16_lo(kb[v].y), k3 = bf16_hi(kb[v].y);
+            const float k0 = bf16_lo(cur.kb[v].x), k1 = bf16_hi(cur.kb[v].x);
+            const float k2 = bf16_lo(cur.kb[v].y), k3 = bf16_hi(cur.kb[v].y);
             hh = fmaf(h[v].x, h[v].x, hh); hh = fmaf(h[v].y, h[v].y, hh);
             hh = fmaf(h[v].z, h[v].z, hh); hh = fmaf(h[v].w, h[v].w, hh);
             kk = fmaf(k0, k0, kk); kk = fmaf(k1, k1, kk);
             kk = fmaf(k2, k2, kk); kk = fmaf(k3, k3, kk);
-            dot = fmaf(h[v].x * q[v].x, k0, dot); dot = fmaf(h[v].y * q[v].y, k1, dot);
-            dot = fmaf(h[v].z * q[v].z, k2, dot); dot = fmaf(h[v].w * q[v].w, k3, dot);
+            dot = fmaf(h[v].x * cur.q[v].x, k0, dot); dot = fmaf(h[v].y * cur.q[v].y, k1, dot);
+            dot = fmaf(h[v].z * cur.q[v].z, k2, dot); dot = fmaf(h[v].w * cur.q[v].w, k3, dot);
         }
         block_sum3(hh, kk, dot, red);
         const float rstd = (1.0f / sqrtf(hh / (float)D + a.eps)) * (1.0f / sqrtf(kk / (float)D + a.eps));
@@ -96,10 +126,18 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constan
         const float gate = 1.0f / (1.0f + expf(-g));
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            h[v].x = __fadd_rn(h[v].x, __fmul_rn(gate, bf16_lo(vb[v].x)));
-            h[v].y = __fadd_rn(h[v].y, __fmul_rn(gate, bf16_hi(vb[v].x)));
-            h[v].z = __fadd_rn(h[v].z, __fmul_rn(gate, bf16_lo(vb[v].y)));
-            h[v].w = __fadd_rn(h[v].w, __fmul_rn(gate, bf16_hi(vb[v].y)));
+            h[v].x = __fadd_rn(h[v].x, __fmul_rn(gate, bf16_lo(cur.vb[v].x)));
+            h[v].y = __fadd_rn(h[v].y, __fmul_rn(gate, bf16_hi(cur.vb[v].x)));
+            h[v].z = __fadd_rn(h[v].z, __fmul_rn(gate, bf16_lo(cur.vb[v].y)));
+            h[v].w = __fadd_rn(h[v].w, __fmul_rn(gate, bf16_hi(cur.vb[v].y)));
+        }
+        if (l + 1 < a.L) {
+            if (kPipe) {
+                cur = nxt;
+            } else {
+                load_qk(a, l + 1, c, cur);
+                load_kv(a, l + 1, t, c, cur);
+            }
         }
     }
 #pragma unroll
@@ -109,17 +147,29 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constan
     }
 }
 
+template <int NV>
+static cudaError_t launch_nv(const GateArgs &a, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.M * a.hc);
+    cfg.blockDim = dim3(kGateThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gate_kernel<NV>, a);
+}
+
 cudaError_t launch_gate(const GateArgs &a, cudaStream_t s) {
     if (a.M == 0) return cudaSuccess;
-    const unsigned grid = (unsigned)a.M * a.hc;
     const int per = kGateThreads * 4;
-    if (a.D <= per) gate_kernel<1><<<grid, kGateThreads, 0, s>>>(a);
-    else if (a.D <= 2 * per) gate_kernel<2><<<grid, kGateThreads, 0, s>>>(a);
-    else if (a.D <= 4 * per) gate_kernel<4><<<grid, kGateThreads, 0, s>>>(a);
-    else if (a.D <= 8 * per) gate_kernel<8><<<grid, kGateThreads, 0, s>>>(a);
-    else if (a.D <= 16 * per) gate_kernel<16><<<grid, kGateThreads, 0, s>>>(a);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    if (a.D <= per) return launch_nv<1>(a, s);
+    if (a.D <= 2 * per) return launch_nv<2>(a, s);
+    if (a.D <= 4 * per) return launch_nv<4>(a, s);
+    if (a.D <= 8 * per) return launch_nv<8>(a, s);
+    if (a.D <= 16 * per) return launch_nv<16>(a, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace engram

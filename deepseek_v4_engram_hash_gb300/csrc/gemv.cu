@@ -70,10 +70,11 @@ __device__ __forceinline__ void q2k_row_to_smem(const uint8_t *blk, bool ok, int
     reinterpret_cast<uint4 *>(dst)[lane] = o;
 }
 
-template <int T>
+template <int T, bool HASH>
 __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_constant__ GemvArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);
+    int64_t *s_ids = reinterpret_cast<int64_t *>(smem_raw + (size_t)T * a.K * 2);
     const int ctas_per_layer = gridDim.x / a.L;
     const int li = blockIdx.x / ctas_per_layer;
     const int cta = blockIdx.x % ctas_per_layer;
@@ -81,6 +82,48 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
     const int K = a.K, N = a.N;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = kGemvThreads / 32;
+    const int rows_per_cta = (N + ctas_per_layer - 1) / ctas_per_layer;
+    const int r0 = cta * rows_per_cta;
+    const int r1 = min(N, r0 + rows_per_cta);
+    const int chunks = K >> 3;
+
+    // ---- the first batch of this warp's wkv stream needs nothing computed:
+    //      start it before waiting on the previous grid ------------------------
+    int o = r0 + warp;
+    uint4 wv[kGemvUnroll];
+    bool prefetched = o < r1;
+    if (prefetched) {
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)o * K);
+#pragma unroll
+        for (int u = 0; u < kGemvUnroll; ++u) {
+            const int j = u * 32 + lane;
+            wv[u] = j < chunks ? ld_stream(wrow + j) : make_uint4(0, 0, 0, 0);
+        }
+    }
+    if (a.pdl) {
+        griddep_wait();          // ids, cache, workspace: ready once the previous grid is done
+        griddep_launch();        // the gate may now launch and prefetch the highway
+    }
+
+    // ---- row ids: hashed here (one thread per id), or read ------------------
+    const int n_ids = T * a.C;
+    const int64_t *ids = ly.ids;
+    int64_t id_stride = a.id_stride;
+    if (HASH) {
+        const HashArgs &h = a.hash;
+        for (int j = tid; j < n_ids; j += kGemvThreads) {
+            const int m = j / a.C, col = j % a.C;
+            const int b = m / h.T, s = m % h.T;
+            const int64_t id = hash_one(h, b, s, li, col);
+            s_ids[j] = id;
+            if (cta == 0) h.out[((int64_t)m * a.L + li) * a.C + col] = id;
+            if (cta == 0 && li == 0 && col == 0)
+                h.cache[(int64_t)b * h.max_seq + h.start_pos + s] = hash_compress(h, b, s);
+        }
+        __syncthreads();
+        ids = s_ids;
+        id_stride = a.C;
+    }
 
     // ---- stage x [T, K] bf16 in shared memory --------------------------------
     if (!a.gather) {
@@ -89,10 +132,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
         for (int i = tid; i < T * K / 8; i += kGemvThreads) dst[i] = __ldg(src + i);
     } else if (ly.fmt == ENGRAM_FMT_FP8) {
         const int lpr = a.hd >> 4, nblk = a.hd / a.blk;
-        for (int g = tid; g < T * a.C * lpr; g += kGemvThreads) {
+        for (int g = tid; g < n_ids * lpr; g += kGemvThreads) {
             const int row = g / lpr, part = g % lpr;
             const int t = row / a.C, c = row % a.C;
-            const int64_t id = ly.ids[(int64_t)t * a.id_stride + c];
+            const int64_t id = ids[(int64_t)t * id_stride + c];
             uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
             if (id >= 0 && id < ly.rows) {
                 const uint4 v = __ldg(reinterpret_cast<const uint4 *>(ly.table + id * a.hd) + part);
@@ -109,9 +152,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
             dst[1] = o1;
         }
     } else {
-        for (int row = warp; row < T * a.C; row += nwarps) {
+        for (int row = warp; row < n_ids; row += nwarps) {
             const int t = row / a.C, c = row % a.C;
-            const int64_t id = ly.ids[(int64_t)t * a.id_stride + c];
+            const int64_t id = ids[(int64_t)t * id_stride + c];
             const bool ok = id >= 0 && id < ly.rows;
             if (!ok && lane == 0) set_err(a.err, ENGRAM_E_ROW);
             q2k_row_to_smem(ly.table + (ok ? id : 0) * 84, ok, lane, xs + (size_t)t * K + (size_t)c * 256);
@@ -120,23 +163,21 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
     __syncthreads();
 
     // ---- stream this CTA's wkv rows -------------------------------------------
-    const int rows_per_cta = (N + ctas_per_layer - 1) / ctas_per_layer;
-    const int r0 = cta * rows_per_cta;
-    const int r1 = min(N, r0 + rows_per_cta);
-    const int chunks = K >> 3;
     const uint4 *xs4 = reinterpret_cast<const uint4 *>(xs);
-    for (int o = r0 + warp; o < r1; o += nwarps) {
+    for (; o < r1; o += nwarps) {
         const uint4 *wrow = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)o * K);
         float acc[T];
 #pragma unroll
         for (int t = 0; t < T; ++t) acc[t] = 0.0f;
         for (int base = 0; base < chunks; base += 32 * kGemvUnroll) {
-            uint4 wv[kGemvUnroll];
+            if (!prefetched) {
 #pragma unroll
-            for (int u = 0; u < kGemvUnroll; ++u) {
-                const int j = base + u * 32 + lane;
-                wv[u] = j < chunks ? ld_stream(wrow + j) : make_uint4(0, 0, 0, 0);
+                for (int u = 0; u < kGemvUnroll; ++u) {
+                    const int j = base + u * 32 + lane;
+                    wv[u] = j < chunks ? ld_stream(wrow + j) : make_uint4(0, 0, 0, 0);
+                }
             }
+            prefetched = false;
 #pragma unroll
             for (int u = 0; u < kGemvUnroll; ++u) {
                 const int j = base + u * 32 + lane;
@@ -162,27 +203,41 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
     }
 }
 
-size_t gemv_smem_bytes(int T, int K) { return (size_t)T * K * 2; }
+size_t gemv_smem_bytes(int T, int K) { return (size_t)T * K * 2 + (size_t)kFusedHashMaxIds * 8; }
 
-template <int T>
-static cudaError_t launch_t(const GemvArgs &a, cudaStream_t s) {
+template <int T, bool HASH>
+static cudaError_t launch_th(const GemvArgs &a, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const size_t smem = gemv_smem_bytes(T, a.K);
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = (size_t)T * a.K * 2 + (HASH ? (size_t)T * a.C * 8 : 0);
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<T, HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<T>, kGemvThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<T, HASH>, kGemvThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     int ctas_per_layer = (sms * per_sm) / a.L;
     const int max_useful = (a.N + 15) / 16;          // at least 16 rows a CTA
     if (ctas_per_layer > max_useful) ctas_per_layer = max_useful;
     if (ctas_per_layer < 1) ctas_per_layer = 1;
-    gemv_kernel<T><<<ctas_per_layer * a.L, kGemvThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas_per_layer * a.L);
+    cfg.blockDim = dim3(kGemvThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<T, HASH>, a);
+}
+
+template <int T>
+static cudaError_t launch_t(const GemvArgs &a, cudaStream_t s) {
+    return a.fuse_hash ? launch_th<T, true>(a, s) : launch_th<T, false>(a, s);
 }
 
 cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t s) {

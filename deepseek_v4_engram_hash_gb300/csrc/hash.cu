@@ -17,15 +17,6 @@
 
 namespace engram {
 
-__device__ __forceinline__ int64_t compress(const HashArgs &a, int b, int64_t s) {
-    const int32_t id = a.ids[(int64_t)b * a.T + s];
-    if (id < 0 || (int64_t)id >= a.vocab) {
-        set_err(a.err, ENGRAM_E_TOKEN);
-        return -1;                                  // treated as unmapped
-    }
-    return a.token_map[id];
-}
-
 __global__ void __launch_bounds__(256) hash_kernel(const HashArgs a) {
     const int C = (a.ng - 1) * a.H;
     const int64_t total = (int64_t)a.B * a.T * a.L * C;
@@ -36,32 +27,8 @@ __global__ void __launch_bounds__(256) hash_kernel(const HashArgs a) {
         const int64_t bs = g / ((int64_t)C * a.L);
         const int s = (int)(bs % a.T);
         const int b = (int)(bs / a.T);
-        const int64_t pos = a.start_pos + s;
-        const int n_top = col / a.H + 1;            // this column's n-gram reaches shift n_top
-
-        int64_t tok[kMaxNgram];
-        bool blocked = false;
-        for (int shift = 0; shift <= n_top; ++shift) {
-            int64_t src;
-            if (pos < shift) {
-                src = 0;                            // blocked below; value unused
-            } else if (pos - shift >= a.start_pos) {
-                src = compress(a, b, pos - shift - a.start_pos);
-            } else {
-                src = a.cache[(int64_t)b * a.max_seq + (pos - shift)];
-            }
-            blocked = blocked || pos < shift || src == -1;
-            tok[shift] = blocked ? a.pad_id : src;
-        }
-        const int64_t *m = a.mult + (int64_t)li * a.ng;
-        uint64_t rolling = (uint64_t)tok[0] * (uint64_t)m[0];
-        for (int n = 1; n <= n_top; ++n) rolling ^= (uint64_t)tok[n] * (uint64_t)m[n];
-        const int64_t p = a.primes[(int64_t)li * C + col];
-        int64_t r = (int64_t)rolling % p;
-        if (r < 0) r += p;
-        a.out[g] = (int64_t)((uint64_t)r + (uint64_t)a.offsets[(int64_t)li * C + col]);
-
-        if (li == 0 && col == 0) a.cache[(int64_t)b * a.max_seq + pos] = compress(a, b, s);
+        a.out[g] = hash_one(a, b, s, li, col);
+        if (li == 0 && col == 0) a.cache[(int64_t)b * a.max_seq + a.start_pos + s] = hash_compress(a, b, s);
     }
 }
 
