@@ -131,7 +131,7 @@ def run_decode(args, rank, world):
     from deepseek_v4_engram_hash_gb300 import _lib as E
     from deepseek_v4_engram_hash_gb300 import configs, runner, synth
 
-    cfg = configs.V41_DECODE.with_(seed=rank)
+    cfg = configs.V41_DECODE.with_(seed=rank_seed(rank))
     cfg = cfg.with_(decode_steps=4 * args.steps + 4 * args.warmup)
     eng = runner.EngramSetup(cfg, batch=1, max_tokens=1)
     n = args.warmup + 2 * args.steps
@@ -233,13 +233,26 @@ def _barrier(world):
 
 
 def _max_over_ranks(v, world):
+    """The largest per-rank value (step time) over all ranks; CPU tensors
+    under gloo, device tensors under NCCL."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank_step: int, max_ms_per_step: float, world: int) -> float:
+    """Tokens/s of the whole job: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank_step / (max_ms_per_step * 1e-3)
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank runs its own replica on its own synthetic sequence."""
+    return rank
 
 
 # ---------------------------------------------------------------------------
@@ -362,7 +375,7 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": world * M / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "metric": METRIC, "value": whole_job_rate(M, ms, world), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "v41_decode_T1: V4.1-Flash engram decode step, T=1 per sequence, "
@@ -379,7 +392,7 @@ def main():
                           "the hash and the gather run inside the gemv launch",
             "gpu_launches": 2 * args.steps,
             "clocks": d["clocks"],
-            "e2e": {"value": world * M / (e2e_ms * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": whole_job_rate(M, e2e_ms, world), "unit": "tokens/s",
                     "h2d_bytes_per_step": d["h2d"], "d2h_bytes_per_step": d["d2h"]},
             "cpu_baseline": cpu,
             "prefill": pre,
