@@ -226,6 +226,68 @@ def run_prefill(args):
     return dict(cfg=cfg, ms=ms, stage_ms=stage.mean(0).tolist())
 
 
+def run_other(cfg, prefill_steps, decode_steps, warm=3):
+    """Prefill (batch x T tokens in one call) and, if asked, single-token decode
+    steps of every sequence, for the Q2_K and large-table workloads."""
+    import torch
+    from deepseek_v4_engram_hash_gb300 import _lib as E
+    from deepseek_v4_engram_hash_gb300 import runner, synth
+
+    B, T = cfg.batch, cfg.T
+    M = B * T
+    eng = runner.EngramSetup(cfg, batch=B, max_tokens=M)
+    d_h = torch.empty((M, cfg.hc, cfg.dim), dtype=torch.float32, device="cuda")
+    synth.fill_highway_cuda(cfg, d_h)
+    ids = torch.from_numpy(eng.ids_for("prefill", T)).cuda()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(prefill_steps)]
+    E.prepare_events([e for row in ev for e in row])
+    for _ in range(warm):
+        eng.forward(ids, 0, d_h)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(prefill_steps):
+        eng.forward(ids, 0, d_h)
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / prefill_steps
+    for i in range(prefill_steps):
+        E.engram_set_profile_events(ev[i])
+        eng.forward(ids, 0, d_h)
+    torch.cuda.synchronize()
+    E.engram_set_profile_events(None)
+    stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in ev]).mean(0)
+    rows_rw = M * cfg.n_layers * cfg.cols * (row_bytes(cfg) + cfg.head_dim * 2)
+    out = {"prefill": {"tokens_per_step": M, "ms_per_step": ms, "tokens_per_s": M / (ms * 1e-3),
+                       "stage_ms": dict(zip(["hash", "gather", "gemm", "gate"], stage.tolist())),
+                       "gemm_tflops": gemm_flops(cfg, M) / (stage[2] * 1e-3) / 1e12,
+                       "gather_gbs": rows_rw / (stage[1] * 1e-3) / 1e9}}
+    if decode_steps:
+        n = warm + decode_steps
+        dids = torch.from_numpy(eng.ids_for("decode", n).T.copy().reshape(n, B, 1)).cuda()
+        dh = torch.empty((B, cfg.hc, cfg.dim), dtype=torch.float32, device="cuda")
+        synth.fill_highway_cuda(cfg, dh, M)
+        pos = T
+        for i in range(warm):
+            eng.forward(dids[i], pos, dh)
+            pos += 1
+        torch.cuda.synchronize()
+        t0.record()
+        for i in range(decode_steps):
+            eng.forward(dids[warm + i], pos, dh)
+            pos += 1
+        t1.record()
+        torch.cuda.synchronize()
+        dms = t0.elapsed_time(t1) / decode_steps
+        sb = step_bytes(cfg, B)
+        out["decode"] = {"tokens_per_step": B, "ms_per_step": dms, "tokens_per_s": B / (dms * 1e-3),
+                         "step_gbs": sb / (dms * 1e-3) / 1e9, "step_algorithmic_bytes": sb}
+    assert E.engram_check() == 0
+    del eng
+    torch.cuda.empty_cache()
+    return out
+
+
 def _barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -316,6 +378,7 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=5)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-others", action="store_true", help="skip the Q2_K and large-table lines")
     ap.add_argument("--only", choices=["decode", "prefill"], default=None,
                     help="run one workload only (for profiling); prints its own JSON line")
     args = ap.parse_args()
@@ -364,6 +427,16 @@ def main():
                             "peak_source": f"{peak_src} bf16 burst (GEMM timed in short back-to-back steps)",
                             "kernel": "gemm_tc_kernel (tcgen05, both layers in one launch)"}}
 
+    others = None
+    if rank == 0 and args.only is None and not args.no_others:
+        from deepseek_v4_engram_hash_gb300 import configs
+        others = {}
+        for name, c, ps, ds in (("v41_q2k_T512", configs.V41_Q2K, 10, 0),
+                                ("large_table_stress", configs.STRESS, 3, 200)):
+            r = run_other(c, ps, ds)
+            r["workload"] = name
+            others[name] = r
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and args.only is None:
         wkv_host = [d["eng"].layer_data[l]["wkv"].view(torch.int16).cpu().numpy().view(np.uint16)
@@ -396,6 +469,7 @@ def main():
                     "h2d_bytes_per_step": d["h2d"], "d2h_bytes_per_step": d["d2h"]},
             "cpu_baseline": cpu,
             "prefill": pre,
+            "other_workloads": others,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -241,9 +241,11 @@ HashArgs hash_args(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t s
 }
 
 int check_hash(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t start_pos, const void *out) {
-    if (!hs || !d_ids || !out) return ENGRAM_E_NULL;
+    if (!hs) return ENGRAM_E_NULL;
     if (T < 0 || start_pos < 0) return ENGRAM_E_INVALID;
     if (start_pos + T > hs->max_seq) return ENGRAM_E_CAPACITY;
+    if (T == 0) return ENGRAM_OK;                 // nothing to read or write
+    if (!d_ids || !out) return ENGRAM_E_NULL;
     if (!aligned(d_ids, 4) || !aligned(out, 8)) return ENGRAM_E_ALIGN;
     return ENGRAM_OK;
 }
@@ -263,7 +265,7 @@ extern "C" {
 int engram_hash(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t start_pos,
                 int64_t *d_row_ids, uintptr_t stream) {
     int rc = check_hash(hs, d_ids, T, start_pos, d_row_ids);
-    if (rc) return rc;
+    if (rc || T == 0) return rc;
     if (!err_ptr()) return ENGRAM_E_CUDA;
     return cuda_rc(launch_hash(hash_args(hs, d_ids, T, start_pos, d_row_ids), S(stream)));
 }
@@ -367,9 +369,10 @@ size_t engram_workspace_bytes(const engram_geom *geom, int64_t max_tokens) {
 
 int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
                    int64_t start_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes, uintptr_t stream) {
-    if (!hs || !layers || !d_ids || !d_h || !d_ws) return ENGRAM_E_NULL;
+    if (!hs || !layers) return ENGRAM_E_NULL;
     int rc = check_hash(hs, d_ids, T, start_pos, d_ws);
-    if (rc) return rc;
+    if (rc || T == 0) return rc;                  // T == 0: a valid no-op
+    if (!d_h) return ENGRAM_E_NULL;
     const engram_geom &g = hs->t->g;
     if (!(eps >= 0.0f)) return ENGRAM_E_INVALID;
     if (!aligned(d_h, 16) || !aligned(d_ws, 256)) return ENGRAM_E_ALIGN;

@@ -13,8 +13,9 @@
 //               K 16) from one thread, committing each stage back to the
 //               producer and each finished tile to the epilogue;
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, bf16 round, store.
-// The epilogue of tile i overlaps the main loop of tile i + 1.  Tiles walk M
-// fastest, so CTAs running together share one wkv column block through L2.
+// The epilogue of tile i overlaps the main loop of tile i + 1.  Tiles are
+// grouped (16 row tiles x all column tiles) so CTAs running together share
+// x row blocks and wkv column blocks through L2.
 //
 // Every mbarrier wait is bounded (2 s on %globaltimer); on expiry the kernel
 // sets ENGRAM_E_TIMEOUT, lets every role drain, frees its tensor memory and
@@ -152,6 +153,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Tile order within a layer: groups of up to kGroupM row tiles; inside a
+// group, row tiles fastest, then column tiles.  The CTAs running at one time
+// then share a few x row blocks and a few wkv column blocks, both L2-resident,
+// even when x itself is larger than L2.
+constexpr int kGroupM = 16;
+__device__ __forceinline__ void tile_coords(int r, int m_tiles, int n_tiles, int &mt, int &nt) {
+    const int per_group = kGroupM * n_tiles;
+    const int g = r / per_group, idx = r % per_group;
+    const int gsz = min(kGroupM, m_tiles - g * kGroupM);
+    mt = g * kGroupM + idx % gsz;
+    nt = idx / gsz;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -203,7 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             int it = 0;
             for (int tile = blockIdx.x; tile < n_tiles_total && !*abort_flag; tile += gridDim.x) {
                 const int l = tile / tiles_per_layer, r = tile % tiles_per_layer;
-                const int m0 = (r % p.m_tiles) * BM, n0 = (r / p.m_tiles) * BN;
+                int mt, nt;
+                tile_coords(r, p.m_tiles, p.n_tiles, mt, nt);
+                const int m0 = mt * BM, n0 = nt * BN;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(empty(s), ((it / STAGES) & 1) ^ 1, abort_flag, p.err)) break;
@@ -263,7 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             if (!__all_sync(0xFFFFFFFFu, ok)) break;          // reconverge before .sync.aligned loads
             tc_fence_after();
             const int l = tile / tiles_per_layer, r = tile % tiles_per_layer;
-            const int m = (r % p.m_tiles) * BM + row, n0 = (r / p.m_tiles) * BN;
+            int mt, nt;
+            tile_coords(r, p.m_tiles, p.n_tiles, mt, nt);
+            const int m = mt * BM + row, n0 = nt * BN;
             uint16_t *out = p.kv[l] + (size_t)m * p.N;
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {

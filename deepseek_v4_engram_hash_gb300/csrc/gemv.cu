@@ -70,6 +70,69 @@ __device__ __forceinline__ void q2k_row_to_smem(const uint8_t *blk, bool ok, int
     reinterpret_cast<uint4 *>(dst)[lane] = o;
 }
 
+// Stage x [T rows, K] bf16 into shared memory at `xs` with row stride `xstride`
+// elements: from a plain x, or by gathering and dequantising the layer's
+// table rows ids[t * id_stride + c].
+__device__ __forceinline__ void stage_x(const GemvArgs &a, const GemvLayer &ly, int T, const int64_t *ids,
+                                        int64_t id_stride, uint16_t *xs, int xstride) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+    const int K = a.K, n_ids = T * a.C;
+    if (!a.gather) {
+        const int cpr = K >> 3;                      // 16-byte chunks a row
+        for (int i = tid; i < T * cpr; i += nthreads) {
+            const int t = i / cpr, j = i % cpr;
+            reinterpret_cast<uint4 *>(xs + (size_t)t * xstride)[j] =
+                __ldg(reinterpret_cast<const uint4 *>(ly.x + (size_t)t * K) + j);
+        }
+    } else if (ly.fmt == ENGRAM_FMT_FP8) {
+        const int lpr = a.hd >> 4, nblk = a.hd / a.blk;
+        for (int g = tid; g < n_ids * lpr; g += nthreads) {
+            const int row = g / lpr, part = g % lpr;
+            const int t = row / a.C, c = row % a.C;
+            const int64_t id = ids[(int64_t)t * id_stride + c];
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+            if (id >= 0 && id < ly.rows) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(ly.table + id * a.hd) + part);
+                const float sc = __ldg(ly.scales + id * nblk + (part * 16) / a.blk);
+                e4m3x4_scaled_to_bf16(v.x, sc, o0.x, o0.y);
+                e4m3x4_scaled_to_bf16(v.y, sc, o0.z, o0.w);
+                e4m3x4_scaled_to_bf16(v.z, sc, o1.x, o1.y);
+                e4m3x4_scaled_to_bf16(v.w, sc, o1.z, o1.w);
+            } else {
+                set_err(a.err, ENGRAM_E_ROW);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)t * xstride + (size_t)c * a.hd) + 2 * part;
+            dst[0] = o0;
+            dst[1] = o1;
+        }
+    } else {
+        for (int row = warp; row < n_ids; row += nwarps) {
+            const int t = row / a.C, c = row % a.C;
+            const int64_t id = ids[(int64_t)t * id_stride + c];
+            const bool ok = id >= 0 && id < ly.rows;
+            if (!ok && lane == 0) set_err(a.err, ENGRAM_E_ROW);
+            q2k_row_to_smem(ly.table + (ok ? id : 0) * 84, ok, lane, xs + (size_t)t * xstride + (size_t)c * 256);
+        }
+    }
+}
+
+// Row ids of this CTA's layer for the T tokens of the call, hashed here (one
+// thread per id) into s_ids; the CTAs with index 0 in each layer also write
+// them to the workspace, and the very first CTA writes the cache.
+__device__ __forceinline__ void hash_ids(const GemvArgs &a, int T, int li, int cta, int64_t *s_ids) {
+    const HashArgs &h = a.hash;
+    for (int j = threadIdx.x; j < T * a.C; j += blockDim.x) {
+        const int m = j / a.C, col = j % a.C;
+        const int b = m / h.T, s = m % h.T;
+        const int64_t id = hash_one(h, b, s, li, col);
+        s_ids[j] = id;
+        if (cta == 0) h.out[((int64_t)m * a.L + li) * a.C + col] = id;
+        if (cta == 0 && li == 0 && col == 0)
+            h.cache[(int64_t)b * h.max_seq + h.start_pos + s] = hash_compress(h, b, s);
+    }
+}
+
 template <int T, bool HASH>
 __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_constant__ GemvArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -105,61 +168,16 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
         griddep_launch();        // the gate may now launch and prefetch the highway
     }
 
-    // ---- row ids: hashed here (one thread per id), or read ------------------
-    const int n_ids = T * a.C;
+    // ---- row ids: hashed here (one thread per id), or read; then x -----------
     const int64_t *ids = ly.ids;
     int64_t id_stride = a.id_stride;
     if (HASH) {
-        const HashArgs &h = a.hash;
-        for (int j = tid; j < n_ids; j += kGemvThreads) {
-            const int m = j / a.C, col = j % a.C;
-            const int b = m / h.T, s = m % h.T;
-            const int64_t id = hash_one(h, b, s, li, col);
-            s_ids[j] = id;
-            if (cta == 0) h.out[((int64_t)m * a.L + li) * a.C + col] = id;
-            if (cta == 0 && li == 0 && col == 0)
-                h.cache[(int64_t)b * h.max_seq + h.start_pos + s] = hash_compress(h, b, s);
-        }
+        hash_ids(a, T, li, cta, s_ids);
         __syncthreads();
         ids = s_ids;
         id_stride = a.C;
     }
-
-    // ---- stage x [T, K] bf16 in shared memory --------------------------------
-    if (!a.gather) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(ly.x);
-        uint4 *dst = reinterpret_cast<uint4 *>(xs);
-        for (int i = tid; i < T * K / 8; i += kGemvThreads) dst[i] = __ldg(src + i);
-    } else if (ly.fmt == ENGRAM_FMT_FP8) {
-        const int lpr = a.hd >> 4, nblk = a.hd / a.blk;
-        for (int g = tid; g < n_ids * lpr; g += kGemvThreads) {
-            const int row = g / lpr, part = g % lpr;
-            const int t = row / a.C, c = row % a.C;
-            const int64_t id = ids[(int64_t)t * id_stride + c];
-            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-            if (id >= 0 && id < ly.rows) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(ly.table + id * a.hd) + part);
-                const float sc = __ldg(ly.scales + id * nblk + (part * 16) / a.blk);
-                e4m3x4_scaled_to_bf16(v.x, sc, o0.x, o0.y);
-                e4m3x4_scaled_to_bf16(v.y, sc, o0.z, o0.w);
-                e4m3x4_scaled_to_bf16(v.z, sc, o1.x, o1.y);
-                e4m3x4_scaled_to_bf16(v.w, sc, o1.z, o1.w);
-            } else {
-                set_err(a.err, ENGRAM_E_ROW);
-            }
-            uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)t * K + (size_t)c * a.hd) + 2 * part;
-            dst[0] = o0;
-            dst[1] = o1;
-        }
-    } else {
-        for (int row = warp; row < n_ids; row += nwarps) {
-            const int t = row / a.C, c = row % a.C;
-            const int64_t id = ids[(int64_t)t * id_stride + c];
-            const bool ok = id >= 0 && id < ly.rows;
-            if (!ok && lane == 0) set_err(a.err, ENGRAM_E_ROW);
-            q2k_row_to_smem(ly.table + (ok ? id : 0) * 84, ok, lane, xs + (size_t)t * K + (size_t)c * 256);
-        }
-    }
+    stage_x(a, ly, T, ids, id_stride, xs, K);
     __syncthreads();
 
     // ---- stream this CTA's wkv rows -------------------------------------------
@@ -203,7 +221,154 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
     }
 }
 
-size_t gemv_smem_bytes(int T, int K) { return (size_t)T * K * 2 + (size_t)kFusedHashMaxIds * 8; }
+// ---------------------------------------------------------------------------
+// 2..8 tokens: the same stream of wkv through mma.sync m16n8k16 (bf16 in, f32
+// accumulate).  With several tokens a CUDA-core dot product needs one
+// shared-memory read of x per token for every 16 bytes of wkv, more
+// shared-memory traffic than the SM can serve at HBM rate; one mma covers 16
+// wkv rows x 16 k x 8 tokens from registers, so the kernel stays HBM-bound.
+//
+// Each warp owns 16-row tasks.  The dot product runs over k, so any
+// permutation of k applied to both operands gives the same sum; we let lane
+// (g = lane/4, q = lane%4) hold physical k 8q .. 8q+7 of each 32-wide k
+// block: one 16-byte load of wkv rows g and g+8 (straight from HBM) and one
+// 16-byte load of token g's x (from shared memory, rows padded by 16 bytes so
+// the 32 lanes spread over all banks) feed two mma instructions.
+// ---------------------------------------------------------------------------
+constexpr int kMmaT = 8;
+constexpr int kMmaThreads = 512;
+constexpr int kMmaWarps = kMmaThreads / 32;
+constexpr int kMmaKbMax = 12;        // 32-wide k blocks a warp holds in flight per row group
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One CTA per SM and layer slice; the CTA walks its contiguous wkv rows 16 at a
+// time, and all 16 warps share each 16-row group: warp w takes k blocks
+// w*kpw .. (w+1)*kpw-1 with every load of them in flight at once, the 16
+// partial 16 x 8 tiles are summed in warp order through shared memory, and the
+// next group's loads are issued before that reduction.
+template <bool HASH>
+__global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_constant__ GemvArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int K = a.K, N = a.N, T = a.T;
+    const int xstride = K + 8;
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);
+    float *red = reinterpret_cast<float *>(smem_raw + (size_t)kMmaT * xstride * 2);    // [16][32][4]
+    int64_t *s_ids = reinterpret_cast<int64_t *>(red + kMmaWarps * 32 * 4);
+    const int ctas_per_layer = gridDim.x / a.L;
+    const int li = blockIdx.x / ctas_per_layer;
+    const int cta = blockIdx.x % ctas_per_layer;
+    const GemvLayer &ly = a.layer[li];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, q = lane & 3;
+    const int kblocks = K >> 5;
+    const int kpw = (kblocks + kMmaWarps - 1) / kMmaWarps;   // <= kMmaKbMax (host-checked)
+    const int kb_lo = warp * kpw;
+    const int groups_total = (N + 15) / 16;
+    const int gpc = (groups_total + ctas_per_layer - 1) / ctas_per_layer;
+    const int grp0 = cta * gpc, grp1 = min(groups_total, grp0 + gpc);
+
+    uint4 wa[kMmaKbMax], wb[kMmaKbMax];
+    auto load_group = [&](int grp) {
+        const int r0 = grp * 16;
+        const uint4 *pa = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)min(r0 + g, N - 1) * K) + q;
+        const uint4 *pb = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)min(r0 + g + 8, N - 1) * K) + q;
+#pragma unroll
+        for (int u = 0; u < kMmaKbMax; ++u) {
+            const int kb = kb_lo + u;
+            const bool ok = u < kpw && kb < kblocks;
+            wa[u] = ok ? ld_stream(pa + 4 * kb) : make_uint4(0, 0, 0, 0);
+            wb[u] = ok ? ld_stream(pb + 4 * kb) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    if (grp0 < grp1) load_group(grp0);          // needs nothing computed: before the wait
+    if (a.pdl) {
+        griddep_wait();
+        griddep_launch();
+    }
+    const int64_t *ids = ly.ids;
+    int64_t id_stride = a.id_stride;
+    if (HASH) {
+        hash_ids(a, T, li, cta, s_ids);
+        __syncthreads();
+        ids = s_ids;
+        id_stride = a.C;
+    }
+    stage_x(a, ly, T, ids, id_stride, xs, xstride);
+    for (int i = threadIdx.x; i < (kMmaT - T) * (xstride >> 3); i += kMmaThreads)   // zero the padding tokens
+        reinterpret_cast<uint4 *>(xs + (size_t)T * xstride)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+
+    const uint16_t *xg = xs + (size_t)g * xstride + 8 * q;
+    for (int grp = grp0; grp < grp1; ++grp) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < kMmaKbMax; ++u) {
+            const int kb = kb_lo + u;
+            if (u < kpw && kb < kblocks) {
+                const uint4 xb = *reinterpret_cast<const uint4 *>(xg + 32 * kb);
+                mma_16816(c, wa[u].x, wb[u].x, wa[u].y, wb[u].y, xb.x, xb.y);
+                mma_16816(c, wa[u].z, wb[u].z, wa[u].w, wb[u].w, xb.z, xb.w);
+            }
+        }
+        if (grp + 1 < grp1) load_group(grp + 1);
+        float4 *rw = reinterpret_cast<float4 *>(red) + warp * 32 + lane;
+        *rw = make_float4(c[0], c[1], c[2], c[3]);
+        __syncthreads();
+        if (threadIdx.x < 128) {
+            // output (lane l, component j): c0 (row g, token 2q), c1 (row g, 2q+1), c2/c3 row g + 8
+            const int l = threadIdx.x >> 2, j = threadIdx.x & 3;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kMmaWarps; ++w) v += red[(w * 32 + l) * 4 + j];
+            const int gg = l >> 2, qq = l & 3;
+            const int r = grp * 16 + gg + ((j & 2) ? 8 : 0), t = 2 * qq + (j & 1);
+            if (r < N && t < T) ly.kv[(size_t)t * N + r] = (uint16_t)f32_to_bf16_bits(v);
+        }
+        __syncthreads();
+    }
+}
+
+template <bool HASH>
+static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (((a.K >> 5) + kMmaWarps - 1) / kMmaWarps > kMmaKbMax) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)kMmaT * (a.K + 8) * 2 + kMmaWarps * 32 * 16 +
+                        (HASH ? (size_t)a.T * a.C * 8 : 0);
+    cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    int ctas_per_layer = sms / a.L;
+    const int groups = (a.N + 15) / 16;
+    if (ctas_per_layer > groups) ctas_per_layer = groups;
+    if (ctas_per_layer < 1) ctas_per_layer = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas_per_layer * a.L);
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<HASH>, a);
+}
+
+size_t gemv_smem_bytes(int T, int K) {
+    if (T > 1 && ((K >> 5) + kMmaWarps - 1) / kMmaWarps > kMmaKbMax) return SIZE_MAX;   // GEMM path
+    return (T <= 1 ? (size_t)K * 2 : (size_t)kMmaT * (K + 8) * 2 + kMmaWarps * 32 * 16) +
+           (size_t)kFusedHashMaxIds * 8;
+}
 
 template <int T, bool HASH>
 static cudaError_t launch_th(const GemvArgs &a, cudaStream_t s) {
@@ -241,18 +406,11 @@ static cudaError_t launch_t(const GemvArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t s) {
-    switch (a.T) {
-        case 0: return cudaSuccess;
-        case 1: return launch_t<1>(a, s);
-        case 2: return launch_t<2>(a, s);
-        case 3: return launch_t<3>(a, s);
-        case 4: return launch_t<4>(a, s);
-        case 5: return launch_t<5>(a, s);
-        case 6: return launch_t<6>(a, s);
-        case 7: return launch_t<7>(a, s);
-        case 8: return launch_t<8>(a, s);
-        default: return cudaErrorInvalidValue;
-    }
+    if (a.T == 0) return cudaSuccess;
+    if (a.T == 1) return launch_t<1>(a, s);
+    if (a.T <= kMmaT && a.K % 32 == 0 && ((a.K >> 5) + kMmaWarps - 1) / kMmaWarps <= kMmaKbMax)
+        return a.fuse_hash ? launch_mma<true>(a, s) : launch_mma<false>(a, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace engram

@@ -24,6 +24,8 @@
  *   - Return value: ENGRAM_OK (0) or a negative ENGRAM_E_* code.  Arguments
  *     are validated on the host before anything is enqueued; a call that
  *     returns an error has enqueued nothing.
+ *   - T = 0 is a valid no-op for every call that takes a token count; its
+ *     buffers may then be null.
  *   - Conditions only the device can see (a token id outside token_map, a
  *     row id outside a table) set a sticky per-device error word; the kernel
  *     substitutes a safe value (the token is treated as unmapped, the row as

@@ -150,3 +150,55 @@ def test_forward_fused_gemv_matches_staged_calls(E):
         kv = torch.empty((1, cfg.N), dtype=torch.bfloat16, device="cuda")
         E.engram_project(x, d["wkv"], 1, cfg.K, cfg.N, kv)
         assert torch.equal(kv.view(torch.int16), eng.kv(1, l).view(torch.int16))
+
+
+ODD_FP8 = configs.TINY.with_(
+    name="odd_fp8", vocab=5000, n_compressed=3000, unmapped_5pct=True, pad_token_id=7,
+    pad_compressed=-1, layer_ids=(2, 9, 30), max_ngram=5, n_heads=3, prime_target=1000,
+    head_dim=128, scale_block=64, dim=256, hc=3, batch=2, T=37, ids="uniform", seed=5)
+
+ODD_Q2K = configs.TINY.with_(
+    name="odd_q2k", vocab=700, n_compressed=400, unmapped_5pct=True, pad_token_id=3,
+    pad_compressed=None, layer_ids=(1, 4), max_ngram=2, n_heads=5, prime_target=300,
+    head_dim=256, scale_block=32, dim=64, hc=1, fmt="q2k", batch=3, T=9, ids="uniform", seed=6)
+
+
+@pytest.mark.parametrize("cfg", [ODD_FP8, ODD_Q2K], ids=lambda c: c.name)
+def test_forward_odd_geometry_all_paths(E, cfg):
+    """Three layers / pad id -1 / 5-grams / 64-wide scale blocks, and Q2_K at
+    C = 5; the call sequence crosses both projection paths (GEMM above 8
+    tokens, fused GEMV at or below) and checks every output."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    B = cfg.batch
+    eng = runner.EngramSetup(cfg, batch=B, max_tokens=B * cfg.T)
+    ref = G.hash_state(cfg, B)
+    pos, first = 0, 0
+    for T in (cfg.T, 1, 2, 0, 1, 4, 1):
+        M = B * T
+        if B * T > B * cfg.T:
+            continue
+        ids = eng.ids_for(f"odd{pos}", T)
+        d_h = _h_device(cfg, first, max(M, 1), True)[:M]
+        h0 = d_h.cpu().numpy()
+        if M == 0:
+            eng.forward(ids, pos, d_h)
+            assert E.engram_check() == 0
+            continue
+        _check_call(eng, ref, ids, pos, d_h, h0, np.arange(M), np.arange(cfg.N), first)
+        pos += T
+        first += M
+
+
+def test_forward_all_unmapped_tokens_use_pad_windows(E):
+    """Every token maps to -1: every window is all pad, so every id equals
+    rem_euclid(rolling(pad, ..., pad)) + offset, identical at every position."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = configs.TINY
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=12)
+    unmapped = int(np.flatnonzero(eng.hash_np["token_map"] == -1)[0])
+    ids = np.full((1, 12), unmapped, dtype=np.int32)
+    d_h = _h_device(cfg, 0, 12, True)
+    ref = G.hash_state(cfg, 1)
+    _check_call(eng, ref, ids, 0, d_h, d_h.cpu().numpy(), np.arange(12), np.arange(cfg.N), 0)
+    got = eng.row_ids(12).cpu().numpy()
+    assert (got == got[0]).all()
