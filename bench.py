@@ -288,6 +288,43 @@ def run_other(cfg, prefill_steps, decode_steps, warm=3):
     return out
 
 
+def run_decode_only(cfg, steps, warm=10):
+    """Single-token decode steps (batch 1) after the configured look-back."""
+    import torch
+    from deepseek_v4_engram_hash_gb300 import _lib as E
+    from deepseek_v4_engram_hash_gb300 import runner, synth
+
+    cfg = cfg.with_(decode_steps=steps + warm + 8)
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=1)
+    if cfg.prefix:
+        pre = torch.from_numpy(eng.ids_for("prefix", cfg.prefix)).cuda()
+        out = torch.empty((1, cfg.prefix, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
+        E.engram_hash(eng.hasher, pre, cfg.prefix, 0, out)
+    n = warm + steps
+    ids = torch.from_numpy(eng.ids_for("decode", n).reshape(n, 1, 1)).cuda()
+    d_h = torch.from_numpy(synth.highway(cfg, [cfg.prefix])).cuda()
+    pos = cfg.prefix
+    for i in range(warm):
+        eng.forward(ids[i], pos, d_h)
+        pos += 1
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        eng.forward(ids[warm + i], pos, d_h)
+        pos += 1
+    t1.record()
+    torch.cuda.synchronize()
+    assert E.engram_check() == 0
+    ms = t0.elapsed_time(t1) / steps
+    wbytes = cfg.n_layers * cfg.N * (cfg.K // 256) * 84 if cfg.wkv_fmt == "q2k" else cfg.n_layers * cfg.N * cfg.K * 2
+    sb = step_bytes(cfg, 1) - cfg.n_layers * cfg.N * cfg.K * 2 + wbytes
+    del eng
+    torch.cuda.empty_cache()
+    return {"tokens_per_step": 1, "ms_per_step": ms, "tokens_per_s": 1.0 / (ms * 1e-3),
+            "step_algorithmic_bytes": sb, "step_gbs": sb / (ms * 1e-3) / 1e9}
+
+
 def _barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -379,7 +416,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true", help="skip the Q2_K and large-table lines")
-    ap.add_argument("--only", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill", "wkvq2k"], default=None,
                     help="run one workload only (for profiling); prints its own JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -399,6 +436,11 @@ def main():
     __graft_entry__.build()
 
     hbm, bf16_burst, bf16_sust, peak_src = _peaks()
+    if args.only == "wkvq2k":
+        from deepseek_v4_engram_hash_gb300 import configs
+        r = run_decode_only(configs.V41_DECODE_WKVQ2K, args.steps)
+        print(json.dumps(r), flush=True)
+        return
     if args.only == "prefill":
         p = run_prefill(args)
         print(json.dumps({"workload": p["cfg"].name, "ms_per_step": p["ms"], "stage_ms": p["stage_ms"],
@@ -436,6 +478,10 @@ def main():
             r = run_other(c, ps, ds)
             r["workload"] = name
             others[name] = r
+        r = run_decode_only(configs.V41_DECODE_WKVQ2K, 2000)
+        r["workload"] = configs.V41_DECODE_WKVQ2K.name
+        r["note"] = "projection read from Q2_K-quantised wkv (82.6 MB a step instead of 503.3 MB)"
+        others[configs.V41_DECODE_WKVQ2K.name] = r
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and args.only is None:

@@ -36,7 +36,7 @@ class engram_geom(ctypes.Structure):
 class engram_layer(ctypes.Structure):
     _fields_ = [("table", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("fmt", ctypes.c_int32),
-                ("wkv", ctypes.c_void_p), ("qk", ctypes.c_void_p)]
+                ("wkv", ctypes.c_void_p), ("qk", ctypes.c_void_p), ("wkv_q2k", ctypes.c_void_p)]
 
 
 _lib = None
@@ -63,6 +63,7 @@ def lib() -> ctypes.CDLL:
             "engram_rows_q2k": ([P, i64, P, i64, i64, i32, P, st], ctypes.c_int),
             "engram_project": ([P, P, i32, i32, i32, P, st], ctypes.c_int),
             "engram_gate": ([P, P, P, i32, i32, i32, ctypes.c_float, st], ctypes.c_int),
+            "engram_project_q2k": ([P, P, i32, i32, P, st], ctypes.c_int),
             "engram_forward": ([P, ctypes.POINTER(engram_layer), P, i32, i64, P, ctypes.c_float,
                                 P, sz, st], ctypes.c_int),
             "engram_forward_host": ([P, ctypes.POINTER(engram_layer), P, P, i32, i64, P, P,
@@ -191,6 +192,11 @@ def engram_project(d_x, d_wkv, T, K, N, d_kv, stream=None):
                              _stream(stream)), "engram_project")
 
 
+def engram_project_q2k(d_x, d_wkv_q2k, K, N, d_kv, stream=None):
+    _ok(lib().engram_project_q2k(_ptr(d_x), _ptr(d_wkv_q2k), int(K), int(N), _ptr(d_kv), _stream(stream)),
+        "engram_project_q2k")
+
+
 def engram_gate(d_h, d_kv, d_qk, T, hc, dim, eps, stream=None):
     _ok(lib().engram_gate(_ptr(d_h), _ptr(d_kv), _ptr(d_qk), int(T), int(hc), int(dim), float(eps),
                           _stream(stream)), "engram_gate")
@@ -201,7 +207,8 @@ def layers_array(layers) -> ctypes.Array:
     arr = (engram_layer * len(layers))()
     for i, ly in enumerate(layers):
         arr[i] = engram_layer(_ptr(ly["table"]).value, _ptr(ly.get("scales")).value, int(ly["rows"]),
-                              int(ly["fmt"]), _ptr(ly["wkv"]).value, _ptr(ly["qk"]).value)
+                              int(ly["fmt"]), _ptr(ly.get("wkv")).value, _ptr(ly["qk"]).value,
+                              _ptr(ly.get("wkv_q2k")).value)
     return arr
 
 

@@ -36,6 +36,7 @@ class EngramConfig:
     seed: int = 0
     eps: float = 1e-6
     decode_steps: int = 0        # single-token steps after the prefill
+    wkv_fmt: str = "bf16"        # "q2k": wkv also held as Q2_K blocks (its bf16 form is their dequantisation)
 
     @property
     def n_layers(self) -> int:
@@ -81,4 +82,7 @@ V41_Q2K = V41_DECODE.with_(name="v41_q2k_T512", prime_target=1 << 18, fmt="q2k",
 STRESS = V41_DECODE.with_(name="large_table_stress", prime_target=1 << 20, batch=8,
                           prefix=0, T=1536, ids="uniform", decode_steps=512)
 
-CONFIGS = {c.name: c for c in (TINY, V41_DECODE, V41_PREFILL, V41_Q2K, STRESS)}
+# The single-token step projecting from Q2_K-quantised wkv (6x fewer weight bytes).
+V41_DECODE_WKVQ2K = V41_DECODE.with_(name="v41_decode_T1_wkv_q2k", wkv_fmt="q2k")
+
+CONFIGS = {c.name: c for c in (TINY, V41_DECODE, V41_PREFILL, V41_Q2K, STRESS, V41_DECODE_WKVQ2K)}

@@ -319,6 +319,27 @@ int engram_project(const uint16_t *d_x, const uint16_t *d_wkv, int32_t T, int32_
     return cuda_rc(launch_gemm(d_x, d_wkv, d_kv, T, N, K, err, S(stream)));
 }
 
+int engram_project_q2k(const uint16_t *d_x, const uint8_t *d_wkv_q2k, int32_t K, int32_t N, uint16_t *d_kv,
+                       uintptr_t stream) {
+    if (!d_x || !d_wkv_q2k || !d_kv) return ENGRAM_E_NULL;
+    if (K < 256 || K % 256 || N < 1 || K > (1 << 20)) return ENGRAM_E_INVALID;
+    if (!aligned(d_x, 16) || !aligned(d_wkv_q2k, 4) || !aligned(d_kv, 2)) return ENGRAM_E_ALIGN;
+    if ((size_t)K * 2 > 200 * 1024) return ENGRAM_E_UNSUPPORTED;
+    int *err = err_ptr();
+    if (!err) return ENGRAM_E_CUDA;
+    GemvArgs a{};
+    a.layer[0].wkv_q2k = d_wkv_q2k;
+    a.layer[0].kv = d_kv;
+    a.layer[0].x = d_x;
+    a.L = 1;
+    a.T = 1;
+    a.K = K;
+    a.N = N;
+    a.gather = 0;
+    a.err = err;
+    return cuda_rc(launch_gemv_q2k(a, S(stream)));
+}
+
 int engram_gate(float *d_h, const uint16_t *d_kv, const float *d_qk, int32_t T, int32_t hc, int32_t dim,
                 float eps, uintptr_t stream) {
     if (!d_h || !d_kv || !d_qk) return ENGRAM_E_NULL;
@@ -377,9 +398,14 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
     if (!(eps >= 0.0f)) return ENGRAM_E_INVALID;
     if (!aligned(d_h, 16) || !aligned(d_ws, 256)) return ENGRAM_E_ALIGN;
     const int L = g.n_layers, C = cols(g), hd = g.head_dim, K = C * hd, N = g.dim * (g.hc + 1);
+    const int64_t M = (int64_t)hs->batch * T;
+    bool all_q2k = K % 256 == 0;
+    for (int l = 0; l < L; ++l) all_q2k = all_q2k && layers[l].wkv_q2k != nullptr;
+    const bool use_q2k = all_q2k && M == 1;
     for (int l = 0; l < L; ++l) {
         const engram_layer &ly = layers[l];
-        if (!ly.table || !ly.wkv || !ly.qk) return ENGRAM_E_NULL;
+        if (!ly.table || !ly.qk || (!ly.wkv && !use_q2k)) return ENGRAM_E_NULL;
+        if (ly.wkv_q2k && !aligned(ly.wkv_q2k, 4)) return ENGRAM_E_ALIGN;
         if (ly.rows < 1) return ENGRAM_E_INVALID;
         if (ly.fmt == ENGRAM_FMT_FP8) {
             if (!ly.scales) return ENGRAM_E_NULL;
@@ -392,7 +418,6 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
         }
         if (!aligned(ly.wkv, 16) || !aligned(ly.qk, 16)) return ENGRAM_E_ALIGN;
     }
-    const int64_t M = (int64_t)hs->batch * T;
     if (M > (int64_t)1 << 24) return ENGRAM_E_UNSUPPORTED;
     if (ws_bytes < engram_workspace_bytes(&g, M)) return ENGRAM_E_WORKSPACE;
     if (M == 0) return ENGRAM_OK;
@@ -436,6 +461,7 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
         GemvArgs a{};
         for (int l = 0; l < L; ++l) {
             a.layer[l].wkv = layers[l].wkv;
+            a.layer[l].wkv_q2k = layers[l].wkv_q2k;
             a.layer[l].kv = reinterpret_cast<uint16_t *>(ws + off[1 + l]);
             a.layer[l].table = static_cast<const uint8_t *>(layers[l].table);
             a.layer[l].scales = layers[l].scales;
@@ -458,7 +484,7 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
         a.err = err;
         ga.pdl = 1;
         record(2, s);
-        if (launch_gemv(a, s) != cudaSuccess) return ENGRAM_E_CUDA;
+        if ((use_q2k ? launch_gemv_q2k(a, s) : launch_gemv(a, s)) != cudaSuccess) return ENGRAM_E_CUDA;
         record(3, s);
     } else {
         for (int l = 0; l < L; ++l) {

@@ -63,6 +63,33 @@ __device__ __forceinline__ float q2k_value(float d, float dmin, uint32_t sc, uin
                      __fmul_rn(dmin, (float)(sc >> 4)));
 }
 
+// One lane's share of a Q2_K block decode: the warp holds the block's 21
+// little-endian words in lanes 0..20 (`word`); lane l returns the bf16 values
+// 8l .. 8l+7 packed in a uint4.  For v = 8l + e: half = l/16, j = (l%16)/4,
+// the quant bytes are qs[32 half + 8 (l%4) + e] (block words 4 + 8 half +
+// 2 (l%4) and the next), the sub-block is 8 half + 2j + (l%4)/2, and the
+// quant is (byte >> 2j) & 3.  All 32 lanes must call it (shuffles).
+__device__ __forceinline__ uint4 q2k_lane_decode(uint32_t word, int lane) {
+    const int half = lane >> 4, j = (lane & 15) >> 2, m = lane & 3;
+    const int qw = 4 + 8 * half + 2 * m;
+    const uint32_t q0 = __shfl_sync(0xFFFFFFFFu, word, qw);
+    const uint32_t q1 = __shfl_sync(0xFFFFFFFFu, word, qw + 1);
+    const int sb = 8 * half + 2 * j + (m >> 1);
+    const uint32_t scw = __shfl_sync(0xFFFFFFFFu, word, sb >> 2);
+    const uint32_t dw = __shfl_sync(0xFFFFFFFFu, word, 20);
+    const uint32_t sc = (scw >> (8 * (sb & 3))) & 0xFFu;
+    const float d = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const uint32_t byte = ((e < 4 ? q0 : q1) >> (8 * (e & 3))) & 0xFFu;
+        y[e] = q2k_value(d, dmin, sc, (byte >> (2 * j)) & 3u);
+    }
+    return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                      pack_bf16x2(y[6], y[7]));
+}
+
 // ---------------------------------------------------------------------------
 // Launchers (host side, defined in the kernel translation units)
 // ---------------------------------------------------------------------------
@@ -150,6 +177,7 @@ cudaError_t launch_rows_q2k(const RowsArgs &a, cudaStream_t s);
 // Small-T GEMV, optionally with the row gather fused into the x staging.
 struct GemvLayer {
     const uint16_t *wkv;    // [N, K]
+    const uint8_t *wkv_q2k; // [N, K / 256] Q2_K blocks (the q2k launch reads these instead)
     uint16_t *kv;           // [T, N]
     const uint16_t *x;      // plain x [T, K] (gather == 0)
     const uint8_t *table;   // gather source (gather == 1)
@@ -171,6 +199,7 @@ struct GemvArgs {
 };
 constexpr int kFusedHashMaxIds = 2048;  // T * C row ids a CTA may hash for its layer
 cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t s);
+cudaError_t launch_gemv_q2k(const GemvArgs &a, cudaStream_t s);   // one token, Q2_K wkv
 size_t gemv_smem_bytes(int T, int K);
 
 // GEMM: kv [M, N] = bf16(x [M, K] . wkv [N, K]^T).

@@ -43,29 +43,12 @@ __device__ __forceinline__ float dot8(const uint4 &w, const uint4 &x, float acc)
     return acc;
 }
 
-// Q2_K decode of one 256-wide row by one warp (see rows.cu for the layout).
+// Q2_K decode of one 256-wide row by one warp into shared memory.
 __device__ __forceinline__ void q2k_row_to_smem(const uint8_t *blk, bool ok, int lane,
                                                 uint16_t *dst) {
-    const int half = lane >> 4, j = (lane & 15) >> 2, m = lane & 3;
     uint32_t word = 0;
     if (ok && lane < 21) word = __ldg(reinterpret_cast<const uint32_t *>(blk) + lane);
-    const int qw = 4 + 8 * half + 2 * m;
-    const uint32_t q0 = __shfl_sync(0xFFFFFFFFu, word, qw);
-    const uint32_t q1 = __shfl_sync(0xFFFFFFFFu, word, qw + 1);
-    const int sb = 8 * half + 2 * j + (m >> 1);
-    const uint32_t scw = __shfl_sync(0xFFFFFFFFu, word, sb >> 2);
-    const uint32_t dw = __shfl_sync(0xFFFFFFFFu, word, 20);
-    const uint32_t sc = (scw >> (8 * (sb & 3))) & 0xFFu;
-    const float d = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFFu)));
-    const float dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
-    float y[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const uint32_t byte = ((e < 4 ? q0 : q1) >> (8 * (e & 3))) & 0xFFu;
-        y[e] = q2k_value(d, dmin, sc, (byte >> (2 * j)) & 3u);
-    }
-    uint4 o = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                         pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+    uint4 o = q2k_lane_decode(word, lane);
     if (!ok) o = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4 *>(dst)[lane] = o;
 }
@@ -362,6 +345,173 @@ static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<HASH>, a);
+}
+
+// ---------------------------------------------------------------------------
+// One token against Q2_K-quantised wkv ([N, K/256] blocks of 84 bytes, a row's
+// blocks contiguous): `wkv_q2k` on spark_model/layers/engram_v41.rs, read by
+// the single-token projection in place of the bf16 expansion, 6x fewer bytes.
+// Lane l decodes weights 8l .. 8l+7 of every block -- exactly the k values it
+// owns in gemv_kernel<1> (chunk 32 b + l) -- to bf16 and runs the same FMA
+// sequence and the same butterfly, so kv is bit-identical to the bf16 GEMV on
+// the dequantised weights.
+// ---------------------------------------------------------------------------
+constexpr int kQ2kUnroll = 16;
+
+// Small non-negative integer -> f32 without the quarter-rate conversion unit:
+// 2^23 + n has n in its low mantissa bits, so subtracting 2^23 is exact.
+__device__ __forceinline__ float small_u2f(uint32_t n) {
+    return __uint_as_float(0x4B000000u | n) - 8388608.0f;
+}
+
+// Lane l's eight weights 8l .. 8l+7 of one Q2_K block, each rounded to bf16
+// and widened back to f32 (the values the bf16 GEMV multiplies).  Same layout
+// as q2k_lane_decode; y = fma(d*sc, q, -dmin*m) equals d*sc*q - dmin*m rounded
+// once because d*sc*q is exact in f32.
+__device__ __forceinline__ void q2k_lane_weights(uint32_t word, int lane, float (&w)[8]) {
+    const int half = lane >> 4, j = (lane & 15) >> 2, m = lane & 3;
+    const int qw = 4 + 8 * half + 2 * m;
+    const uint32_t q0 = __shfl_sync(0xFFFFFFFFu, word, qw);
+    const uint32_t q1 = __shfl_sync(0xFFFFFFFFu, word, qw + 1);
+    const int sb = 8 * half + 2 * j + (m >> 1);
+    const uint32_t scw = __shfl_sync(0xFFFFFFFFu, word, sb >> 2);
+    const uint32_t dw = __shfl_sync(0xFFFFFFFFu, word, 20);
+    const uint32_t sc = (scw >> (8 * (sb & 3))) & 0xFFu;
+    const float d = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
+    const float dl = __fmul_rn(d, small_u2f(sc & 15u));
+    const float nml = -__fmul_rn(dmin, small_u2f(sc >> 4));
+    const uint32_t t0 = (q0 >> (2 * j)) & 0x03030303u, t1 = (q1 >> (2 * j)) & 0x03030303u;
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        const uint32_t t = e < 4 ? t0 : t1;
+        // byte e of t into the low byte of 0x4B000000: the f32 2^23 + q, minus 2^23
+        const float f0 = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7540u | (e & 3))) - 8388608.0f;
+        const float f1 = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7540u | ((e + 1) & 3))) - 8388608.0f;
+        const float y0 = __fmaf_rn(dl, f0, nml);
+        const float y1 = __fmaf_rn(dl, f1, nml);
+        const uint32_t p = pack_bf16x2(y0, y1);
+        w[e] = bf16_lo(p);
+        w[e + 1] = bf16_hi(p);
+    }
+}
+
+template <bool HASH>
+__global__ void __launch_bounds__(kGemvThreads, 2) gemv_q2k_kernel(const __grid_constant__ GemvArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    float *xf = reinterpret_cast<float *>(smem_raw);                       // x widened to f32 [K]
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw + (size_t)a.K * 4);
+    int64_t *s_ids = reinterpret_cast<int64_t *>(smem_raw + (size_t)a.K * 6);
+    const int ctas_per_layer = gridDim.x / a.L;
+    const int li = blockIdx.x / ctas_per_layer;
+    const int cta = blockIdx.x % ctas_per_layer;
+    const GemvLayer &ly = a.layer[li];
+    const int K = a.K, N = a.N, nblk = K >> 8;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = kGemvThreads / 32;
+    const int rows_per_cta = (N + ctas_per_layer - 1) / ctas_per_layer;
+    const int r0 = cta * rows_per_cta;
+    const int r1 = min(N, r0 + rows_per_cta);
+
+    auto row_words = [&](int o) {
+        return reinterpret_cast<const uint32_t *>(ly.wkv_q2k + (size_t)o * nblk * 84) + lane;
+    };
+    int o = r0 + warp;
+    uint32_t wq[kQ2kUnroll];
+    bool prefetched = o < r1;
+    if (prefetched) {
+        const uint32_t *w = row_words(o);
+#pragma unroll
+        for (int u = 0; u < kQ2kUnroll; ++u) wq[u] = (u < nblk && lane < 21) ? __ldg(w + 21 * u) : 0u;
+    }
+    if (a.pdl) {
+        griddep_wait();
+        griddep_launch();
+    }
+    const int64_t *ids = ly.ids;
+    int64_t id_stride = a.id_stride;
+    if (HASH) {
+        hash_ids(a, 1, li, cta, s_ids);
+        __syncthreads();
+        ids = s_ids;
+        id_stride = a.C;
+    }
+    stage_x(a, ly, 1, ids, id_stride, xs, K);
+    __syncthreads();
+    for (int i = tid; i < K / 2; i += kGemvThreads) {
+        const uint32_t v = reinterpret_cast<const uint32_t *>(xs)[i];
+        reinterpret_cast<float2 *>(xf)[i] = make_float2(bf16_lo(v), bf16_hi(v));
+    }
+    __syncthreads();
+
+    const float4 *xf4 = reinterpret_cast<const float4 *>(xf);
+    for (; o < r1; o += nwarps) {
+        const uint32_t *w = row_words(o);
+        float acc = 0.0f;
+        for (int b0 = 0; b0 < nblk; b0 += kQ2kUnroll) {
+            if (!prefetched) {
+#pragma unroll
+                for (int u = 0; u < kQ2kUnroll; ++u)
+                    wq[u] = (b0 + u < nblk && lane < 21) ? __ldg(w + 21 * (b0 + u)) : 0u;
+            }
+            prefetched = false;
+#pragma unroll
+            for (int u = 0; u < kQ2kUnroll; ++u) {
+                if (b0 + u < nblk) {                       // warp-uniform
+                    float wv[8];
+                    q2k_lane_weights(wq[u], lane, wv);
+                    const int c = (b0 + u) * 32 + lane;    // the lane's 8 k values: chunk 32 b + l
+                    const float4 xa = xf4[2 * c], xb = xf4[2 * c + 1];
+                    acc = fmaf(wv[0], xa.x, acc);
+                    acc = fmaf(wv[1], xa.y, acc);
+                    acc = fmaf(wv[2], xa.z, acc);
+                    acc = fmaf(wv[3], xa.w, acc);
+                    acc = fmaf(wv[4], xb.x, acc);
+                    acc = fmaf(wv[5], xb.y, acc);
+                    acc = fmaf(wv[6], xb.z, acc);
+                    acc = fmaf(wv[7], xb.w, acc);
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+        if (lane == 0) ly.kv[o] = (uint16_t)f32_to_bf16_bits(acc);
+    }
+}
+
+template <bool HASH>
+static cudaError_t launch_q2k_h(const GemvArgs &a, cudaStream_t s) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t smem = (size_t)a.K * 6 + (HASH ? (size_t)a.C * 8 : 0);
+    cudaError_t e = cudaFuncSetAttribute(gemv_q2k_kernel<HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_q2k_kernel<HASH>, kGemvThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    int ctas_per_layer = (sms * per_sm) / a.L;
+    const int max_useful = (a.N + 15) / 16;
+    if (ctas_per_layer > max_useful) ctas_per_layer = max_useful;
+    if (ctas_per_layer < 1) ctas_per_layer = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas_per_layer * a.L);
+    cfg.blockDim = dim3(kGemvThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemv_q2k_kernel<HASH>, a);
+}
+
+cudaError_t launch_gemv_q2k(const GemvArgs &a, cudaStream_t s) {
+    if (a.T != 1 || a.K % 256) return cudaErrorInvalidValue;
+    return a.fuse_hash ? launch_q2k_h<true>(a, s) : launch_q2k_h<false>(a, s);
 }
 
 size_t gemv_smem_bytes(int T, int K) {

@@ -42,32 +42,7 @@ __global__ void __launch_bounds__(256) rows_fp8_kernel(const RowsArgs a) {
 
 // Q2_K: one warp per row.  Lanes 0..20 load the block's 21 little-endian
 // words (the block is 4-byte aligned: 84 = 4 * 21); lane l then decodes values
-// 8l .. 8l+7, which share half = l/16, j = (l%16)/4 and the quant bytes
-// qs[32 half + 8 (l%4) + e], e = 0..7, and one sub-block scale byte.
-__device__ __forceinline__ void q2k_decode_lane(uint32_t word, int lane, uint4 &out) {
-    const int half = lane >> 4, j = (lane & 15) >> 2, m = lane & 3;
-    const int qw = 4 + 8 * half + 2 * m;             // word index of qs[32 half + 8 m]
-    const uint32_t q0 = __shfl_sync(0xFFFFFFFFu, word, qw);
-    const uint32_t q1 = __shfl_sync(0xFFFFFFFFu, word, qw + 1);
-    const int sb = 8 * half + 2 * j + (m >> 1);
-    const uint32_t scw = __shfl_sync(0xFFFFFFFFu, word, sb >> 2);
-    const uint32_t dw = __shfl_sync(0xFFFFFFFFu, word, 20);
-    const uint32_t sc = (scw >> (8 * (sb & 3))) & 0xFFu;
-    const float d = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFFu)));
-    const float dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
-    const int sh = 2 * j;
-    float y[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const uint32_t byte = ((e < 4 ? q0 : q1) >> (8 * (e & 3))) & 0xFFu;
-        y[e] = q2k_value(d, dmin, sc, (byte >> sh) & 3u);
-    }
-    out.x = pack_bf16x2(y[0], y[1]);
-    out.y = pack_bf16x2(y[2], y[3]);
-    out.z = pack_bf16x2(y[4], y[5]);
-    out.w = pack_bf16x2(y[6], y[7]);
-}
-
+// 8l .. 8l+7 (q2k_lane_decode).
 __global__ void __launch_bounds__(256) rows_q2k_kernel(const RowsArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t n_rows = a.n_tok * a.C;
@@ -80,8 +55,7 @@ __global__ void __launch_bounds__(256) rows_q2k_kernel(const RowsArgs a) {
         const bool ok = id >= 0 && id < a.R;
         uint32_t word = 0;
         if (ok && lane < 21) word = __ldg(reinterpret_cast<const uint32_t *>(a.table + id * 84) + lane);
-        uint4 o;
-        q2k_decode_lane(word, lane, o);
+        uint4 o = q2k_lane_decode(word, lane);
         if (!ok) {
             o = make_uint4(0, 0, 0, 0);
             if (lane == 0) set_err(a.err, ENGRAM_E_ROW);

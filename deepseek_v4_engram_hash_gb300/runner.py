@@ -43,7 +43,15 @@ class EngramSetup:
                     synth.fill_table_q2k_cuda(cfg, l, d["table"])
                     d["fmt"] = E.ENGRAM_FMT_Q2K
                 d["wkv"] = torch.empty((cfg.N, cfg.K), dtype=torch.bfloat16, device=self.device)
-                synth.fill_wkv_cuda(cfg, l, d["wkv"])
+                if cfg.wkv_fmt == "q2k":
+                    # Q2_K blocks, and their bf16 dequantisation (by libengram) for multi-token calls
+                    nb = cfg.N * (cfg.K // 256)
+                    d["wkv_q2k"] = torch.empty((nb, 84), dtype=torch.uint8, device=self.device)
+                    synth.fill_table_q2k_cuda(cfg, l, d["wkv_q2k"], tag="wkvq2k")
+                    ids = torch.arange(nb, dtype=torch.int64, device=self.device)
+                    E.engram_rows_q2k(d["wkv_q2k"], nb, ids, nb, 1, 1, d["wkv"])
+                else:
+                    synth.fill_wkv_cuda(cfg, l, d["wkv"])
                 q, k = synth.qk_weights(cfg, l)
                 d["q"], d["k"] = q, k
                 d["qk"] = torch.from_numpy(q * k).to(self.device)   # exact: bf16 x bf16 fits f32

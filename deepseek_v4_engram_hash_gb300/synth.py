@@ -185,12 +185,13 @@ Q2K_D_LO = np.float32(1e-3)
 Q2K_D_STEP = np.float32(9e-3 / (1 << 24))
 
 
-def table_q2k_rows(cfg, layer: int, rows) -> np.ndarray:
+def table_q2k_rows(cfg, layer: int, rows, tag: str = "q2k") -> np.ndarray:
     """Rows of layer `layer`'s Q2_K table: [n, 84] u8.  Bytes 0..79 (sub-block
     scale/min nibbles and 2-bit quants) uniform; d and dmin uniform in
-    (1e-3, 1e-2), stored as binary16."""
+    (1e-3, 1e-2), stored as binary16.  tag "wkvq2k" gives Q2_K wkv blocks
+    ([N * K / 256] of them, a row's blocks contiguous)."""
     rows = np.atleast_1d(np.asarray(rows, dtype=np.uint64)).ravel()
-    key = stream_key(cfg.seed, f"q2k.{layer}")
+    key = stream_key(cfg.seed, f"{tag}.{layer}")
     idx = rows[:, None] * np.uint64(12) + np.arange(12, dtype=np.uint64)[None, :]
     z = splitmix64(key, idx).reshape(rows.size, 12)
     out = np.zeros((rows.size, 84), dtype=np.uint8)
@@ -278,10 +279,10 @@ def fill_table_fp8_cuda(cfg, layer: int, codes, scales):
         ctypes.c_void_p(scales.data_ptr()), _stream_of(codes)), "synth_fp8_table")
 
 
-def fill_table_q2k_cuda(cfg, layer: int, blocks):
+def fill_table_q2k_cuda(cfg, layer: int, blocks, tag: str = "q2k"):
     """blocks: uint8 CUDA tensor [R, 84]."""
     _check(_synth_lib().synth_q2k_table(
-        stream_key(cfg.seed, f"q2k.{layer}"), blocks.shape[0], float(Q2K_D_STEP), float(Q2K_D_LO),
+        stream_key(cfg.seed, f"{tag}.{layer}"), blocks.shape[0], float(Q2K_D_STEP), float(Q2K_D_LO),
         ctypes.c_void_p(blocks.data_ptr()), _stream_of(blocks)), "synth_q2k_table")
 
 

@@ -136,14 +136,27 @@ int engram_project(const uint16_t *d_x, const uint16_t *d_wkv, int32_t T, int32_
 int engram_gate(float *d_h, const uint16_t *d_kv, const float *d_qk, int32_t T, int32_t hc,
                 int32_t dim, float eps, uintptr_t stream);
 
+/* Stage 3 at one token from Q2_K-quantised wkv (spark_model/layers/engram_v41.rs,
+ * `EngramLayerWeights.wkv_q2k`: the weight as the GGUF ships it, read by the
+ * single-token projection in place of the bf16 expansion, 6x fewer bytes):
+ *   d_wkv_q2k [N, K / 256] 84-byte ggml Q2_K blocks (a row's blocks contiguous,
+ *   4-byte aligned); d_x [1, K] bf16; d_kv [1, N] bf16.  K % 256 == 0.
+ * kv is bit-identical to engram_project(d_x, W) where W is the bf16
+ * dequantisation of the blocks (engram_rows_q2k). */
+int engram_project_q2k(const uint16_t *d_x, const uint8_t *d_wkv_q2k, int32_t K, int32_t N,
+                       uint16_t *d_kv, uintptr_t stream);
+
 /* One engram layer for engram_forward. */
 typedef struct {
     const void *table;      /* FP8: e4m3 [rows, head_dim]; Q2K: blocks [rows, 84] */
     const float *scales;    /* FP8: [rows, head_dim / scale_block]; Q2K: unused */
     int64_t rows;           /* table rows (sum of the layer's primes) */
     int32_t fmt;            /* ENGRAM_FMT_FP8 or ENGRAM_FMT_Q2K */
-    const uint16_t *wkv;    /* [dim * (hc + 1), C * head_dim] bf16 */
+    const uint16_t *wkv;    /* [dim * (hc + 1), C * head_dim] bf16; may be NULL when wkv_q2k
+                               is set and every call has batch * T == 1 */
     const float *qk;        /* [hc, dim] f32 */
+    const uint8_t *wkv_q2k; /* optional [dim * (hc + 1), C * head_dim / 256] Q2_K blocks: when
+                               every layer has it, single-token calls project from it */
 } engram_layer;
 
 /* The whole forward for n_layers engram layers (in `layers` order) on one

@@ -36,12 +36,23 @@ def x_of(cfg, layer, row_ids) -> np.ndarray:
     return r.reshape(M, cfg.cols * cfg.head_dim)
 
 
+def wkv(cfg, layer, out_rows) -> np.ndarray:
+    """wkv rows [len(out_rows), K] as bf16 bits; with Q2_K wkv, the oracle's
+    decode of the row's K / 256 blocks."""
+    out_rows = np.asarray(out_rows, dtype=np.int64).ravel()
+    if getattr(cfg, "wkv_fmt", "bf16") == "q2k":
+        nb = cfg.K // 256
+        blk_ids = (out_rows[:, None] * nb + np.arange(nb)[None, :]).ravel()
+        blocks = synth.table_q2k_rows(cfg, layer, blk_ids, tag="wkvq2k")
+        return oracle.rows_q2k(blocks, np.arange(blk_ids.size)).reshape(out_rows.size, cfg.K)
+    return synth.wkv_rows(cfg, layer, out_rows)
+
+
 def kv(cfg, layer, x_bits, out_rows=None) -> np.ndarray:
     """kv [M, len(out_rows)] bf16 bits; out_rows defaults to all N outputs."""
     if out_rows is None:
         out_rows = np.arange(cfg.N)
-    w = synth.wkv_rows(cfg, layer, out_rows)
-    return oracle.linear_bf16(x_bits, w)
+    return oracle.linear_bf16(x_bits, wkv(cfg, layer, out_rows))
 
 
 def gate(cfg, layer, h, kv_bits):
