@@ -101,7 +101,7 @@ class Clocks:
 def row_bytes(cfg) -> int:
     if cfg.fmt == "q2k":
         return 84
-    return cfg.head_dim + (cfg.head_dim // cfg.scale_block) * 4
+    return cfg.head_dim + (cfg.head_dim // cfg.scale_block) * (1 if cfg.fmt == "fp8_e8m0" else 4)
 
 
 def gemv_bytes(cfg, M) -> int:
@@ -478,6 +478,10 @@ def main():
             r = run_other(c, ps, ds)
             r["workload"] = name
             others[name] = r
+        r = run_decode_only(configs.V41_DECODE_E8M0, 2000)
+        r["workload"] = configs.V41_DECODE_E8M0.name
+        r["note"] = "one-byte e8m0 table scales (264 B a row instead of 288 B)"
+        others[configs.V41_DECODE_E8M0.name] = r
         r = run_decode_only(configs.V41_DECODE_WKVQ2K, 2000)
         r["workload"] = configs.V41_DECODE_WKVQ2K.name
         r["note"] = "projection read from Q2_K-quantised wkv (82.6 MB a step instead of 503.3 MB)"

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libengram.so")
 
 ENGRAM_FMT_FP8 = 0
 ENGRAM_FMT_Q2K = 1
+ENGRAM_FMT_FP8_E8M0 = 2
 
 
 class EngramError(RuntimeError):
@@ -61,6 +62,7 @@ def lib() -> ctypes.CDLL:
             "engram_hash": ([P, P, i32, i64, P, st], ctypes.c_int),
             "engram_rows_fp8": ([P, P, i64, i32, i32, P, i64, i64, i32, P, st], ctypes.c_int),
             "engram_rows_q2k": ([P, i64, P, i64, i64, i32, P, st], ctypes.c_int),
+            "engram_rows_fp8_e8m0": ([P, P, i64, i32, i32, P, i64, i64, i32, P, st], ctypes.c_int),
             "engram_project": ([P, P, i32, i32, i32, P, st], ctypes.c_int),
             "engram_gate": ([P, P, P, i32, i32, i32, ctypes.c_float, st], ctypes.c_int),
             "engram_project_q2k": ([P, P, i32, i32, P, st], ctypes.c_int),
@@ -180,6 +182,13 @@ def engram_rows_fp8(d_table, d_scales, R, head_dim, scale_block, d_row_ids, n_to
     _ok(lib().engram_rows_fp8(_ptr(d_table), _ptr(d_scales), int(R), int(head_dim), int(scale_block),
                               _ptr(d_row_ids), int(n_tok), int(id_stride), int(C), _ptr(d_rows),
                               _stream(stream)), "engram_rows_fp8")
+
+
+def engram_rows_fp8_e8m0(d_table, d_scales_u8, R, head_dim, scale_block, d_row_ids, n_tok, id_stride, C,
+                         d_rows, stream=None):
+    _ok(lib().engram_rows_fp8_e8m0(_ptr(d_table), _ptr(d_scales_u8), int(R), int(head_dim), int(scale_block),
+                                   _ptr(d_row_ids), int(n_tok), int(id_stride), int(C), _ptr(d_rows),
+                                   _stream(stream)), "engram_rows_fp8_e8m0")
 
 
 def engram_rows_q2k(d_blocks, R, d_row_ids, n_tok, id_stride, C, d_rows, stream=None):

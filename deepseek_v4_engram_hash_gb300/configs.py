@@ -27,7 +27,7 @@ class EngramConfig:
     scale_block: int
     dim: int
     hc: int
-    fmt: str                     # "fp8" (e4m3 + pow2 scales) or "q2k"
+    fmt: str                     # "fp8" (e4m3 + pow2 f32 scales), "fp8_e8m0" (one-byte scales) or "q2k"
     batch: int                   # independent sequences
     prefix: int                  # positions hashed before the measured call
     T: int                       # tokens per sequence per call
@@ -85,4 +85,8 @@ STRESS = V41_DECODE.with_(name="large_table_stress", prime_target=1 << 20, batch
 # The single-token step projecting from Q2_K-quantised wkv (6x fewer weight bytes).
 V41_DECODE_WKVQ2K = V41_DECODE.with_(name="v41_decode_T1_wkv_q2k", wkv_fmt="q2k")
 
-CONFIGS = {c.name: c for c in (TINY, V41_DECODE, V41_PREFILL, V41_Q2K, STRESS, V41_DECODE_WKVQ2K)}
+# The decode step with one-byte e8m0 scales (264 instead of 288 bytes a row).
+V41_DECODE_E8M0 = V41_DECODE.with_(name="v41_decode_T1_e8m0", fmt="fp8_e8m0")
+
+CONFIGS = {c.name: c for c in (TINY, V41_DECODE, V41_PREFILL, V41_Q2K, STRESS, V41_DECODE_WKVQ2K,
+                               V41_DECODE_E8M0)}

@@ -280,7 +280,24 @@ int engram_rows_fp8(const uint8_t *d_table, const float *d_scales, int64_t R, in
         head_dim % scale_block)
         return ENGRAM_E_INVALID;
     if (!aligned(d_table, 16) || !aligned(d_scales, 4)) return ENGRAM_E_ALIGN;
-    RowsArgs a{d_table, d_scales, R, head_dim, scale_block, d_row_ids, n_tok, id_stride, C, d_rows, err_ptr()};
+    RowsArgs a{d_table, d_scales, R, head_dim, scale_block, d_row_ids, n_tok, id_stride, C, d_rows, err_ptr(),
+               ENGRAM_FMT_FP8};
+    if (!a.err) return ENGRAM_E_CUDA;
+    return cuda_rc(launch_rows_fp8(a, S(stream)));
+}
+
+int engram_rows_fp8_e8m0(const uint8_t *d_table, const uint8_t *d_scales, int64_t R, int32_t head_dim,
+                         int32_t scale_block, const int64_t *d_row_ids, int64_t n_tok, int64_t id_stride,
+                         int32_t C, uint16_t *d_rows, uintptr_t stream) {
+    int rc = check_rows(d_table, d_row_ids, R, n_tok, id_stride, C, d_rows);
+    if (rc) return rc;
+    if (!d_scales) return ENGRAM_E_NULL;
+    if (head_dim < 16 || head_dim > 1024 || head_dim % 16 || scale_block < 16 || scale_block % 16 ||
+        head_dim % scale_block)
+        return ENGRAM_E_INVALID;
+    if (!aligned(d_table, 16)) return ENGRAM_E_ALIGN;
+    RowsArgs a{d_table, d_scales, R, head_dim, scale_block, d_row_ids, n_tok, id_stride, C, d_rows, err_ptr(),
+               ENGRAM_FMT_FP8_E8M0};
     if (!a.err) return ENGRAM_E_CUDA;
     return cuda_rc(launch_rows_fp8(a, S(stream)));
 }
@@ -290,7 +307,7 @@ int engram_rows_q2k(const uint8_t *d_blocks, int64_t R, const int64_t *d_row_ids
     int rc = check_rows(d_blocks, d_row_ids, R, n_tok, id_stride, C, d_rows);
     if (rc) return rc;
     if (!aligned(d_blocks, 4)) return ENGRAM_E_ALIGN;
-    RowsArgs a{d_blocks, nullptr, R, 256, 256, d_row_ids, n_tok, id_stride, C, d_rows, err_ptr()};
+    RowsArgs a{d_blocks, nullptr, R, 256, 256, d_row_ids, n_tok, id_stride, C, d_rows, err_ptr(), ENGRAM_FMT_Q2K};
     if (!a.err) return ENGRAM_E_CUDA;
     return cuda_rc(launch_rows_q2k(a, S(stream)));
 }
@@ -407,9 +424,10 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
         if (!ly.table || !ly.qk || (!ly.wkv && !use_q2k)) return ENGRAM_E_NULL;
         if (ly.wkv_q2k && !aligned(ly.wkv_q2k, 4)) return ENGRAM_E_ALIGN;
         if (ly.rows < 1) return ENGRAM_E_INVALID;
-        if (ly.fmt == ENGRAM_FMT_FP8) {
+        if (ly.fmt == ENGRAM_FMT_FP8 || ly.fmt == ENGRAM_FMT_FP8_E8M0) {
             if (!ly.scales) return ENGRAM_E_NULL;
-            if (!aligned(ly.table, 16) || !aligned(ly.scales, 4)) return ENGRAM_E_ALIGN;
+            if (!aligned(ly.table, 16) || (ly.fmt == ENGRAM_FMT_FP8 && !aligned(ly.scales, 4)))
+                return ENGRAM_E_ALIGN;
         } else if (ly.fmt == ENGRAM_FMT_Q2K) {
             if (hd != 256) return ENGRAM_E_INVALID;      // one Q2_K block per 256-wide row
             if (!aligned(ly.table, 4)) return ENGRAM_E_ALIGN;
@@ -490,8 +508,8 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
         for (int l = 0; l < L; ++l) {
             RowsArgs ra{static_cast<const uint8_t *>(layers[l].table), layers[l].scales, layers[l].rows,
                         hd, g.scale_block, ids + (int64_t)l * C, M, (int64_t)L * C, C,
-                        reinterpret_cast<uint16_t *>(ws + off[1 + L + l]), err};
-            e = layers[l].fmt == ENGRAM_FMT_FP8 ? launch_rows_fp8(ra, s) : launch_rows_q2k(ra, s);
+                        reinterpret_cast<uint16_t *>(ws + off[1 + L + l]), err, layers[l].fmt};
+            e = layers[l].fmt == ENGRAM_FMT_Q2K ? launch_rows_q2k(ra, s) : launch_rows_fp8(ra, s);
             if (e != cudaSuccess) return ENGRAM_E_CUDA;
         }
         record(2, s);

@@ -56,6 +56,18 @@ __device__ __forceinline__ void e4m3x4_scaled_to_bf16(uint32_t codes, float scal
     out23 = pack_bf16x2(__fmul_rn(b.x, scale), __fmul_rn(b.y, scale));
 }
 
+// e8m0 byte -> f32 scale 2^(code - 127): the byte is the biased exponent
+// (code 0 is the subnormal 2^-127, code 255 NaN).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t code) {
+    return __uint_as_float(code == 0u ? 0x00400000u : (code == 255u ? 0x7FC00000u : code << 23));
+}
+
+// The scale of fp8 row `id`, block `b`: f32 (fmt FP8) or an e8m0 byte (FP8_E8M0).
+__device__ __forceinline__ float fp8_row_scale(const void *scales, int fmt, int64_t idx) {
+    return fmt == ENGRAM_FMT_FP8_E8M0 ? e8m0_to_f32(__ldg(static_cast<const uint8_t *>(scales) + idx))
+                                      : __ldg(static_cast<const float *>(scales) + idx);
+}
+
 // One Q2_K value: d * (sc & 15) * q - dmin * (sc >> 4); every product is exact
 // in f32, so only the subtraction rounds.
 __device__ __forceinline__ float q2k_value(float d, float dmin, uint32_t sc, uint32_t q) {
@@ -162,7 +174,7 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 
 struct RowsArgs {
     const uint8_t *table;   // fp8 codes [R, hd] or q2k blocks [R, 84]
-    const float *scales;    // fp8 only
+    const void *scales;     // fp8: f32 or e8m0 bytes (fmt)
     int64_t R;
     int32_t hd, blk;
     const int64_t *ids;     // ids[t * id_stride + c]
@@ -170,6 +182,7 @@ struct RowsArgs {
     int32_t C;
     uint16_t *out;          // [n_tok * C, hd] bf16
     int *err;
+    int32_t fmt;            // ENGRAM_FMT_FP8 or ENGRAM_FMT_FP8_E8M0 (fp8 rows)
 };
 cudaError_t launch_rows_fp8(const RowsArgs &a, cudaStream_t s);
 cudaError_t launch_rows_q2k(const RowsArgs &a, cudaStream_t s);
@@ -181,7 +194,7 @@ struct GemvLayer {
     uint16_t *kv;           // [T, N]
     const uint16_t *x;      // plain x [T, K] (gather == 0)
     const uint8_t *table;   // gather source (gather == 1)
-    const float *scales;
+    const void *scales;     // f32 or e8m0 bytes, by fmt
     int64_t rows;
     const int64_t *ids;     // ids[t * id_stride + c] of this layer
     int32_t fmt;

@@ -68,7 +68,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const GemvLayer &ly, 
             reinterpret_cast<uint4 *>(xs + (size_t)t * xstride)[j] =
                 __ldg(reinterpret_cast<const uint4 *>(ly.x + (size_t)t * K) + j);
         }
-    } else if (ly.fmt == ENGRAM_FMT_FP8) {
+    } else if (ly.fmt != ENGRAM_FMT_Q2K) {
         const int lpr = a.hd >> 4, nblk = a.hd / a.blk;
         for (int g = tid; g < n_ids * lpr; g += nthreads) {
             const int row = g / lpr, part = g % lpr;
@@ -77,7 +77,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const GemvLayer &ly, 
             uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
             if (id >= 0 && id < ly.rows) {
                 const uint4 v = __ldg(reinterpret_cast<const uint4 *>(ly.table + id * a.hd) + part);
-                const float sc = __ldg(ly.scales + id * nblk + (part * 16) / a.blk);
+                const float sc = fp8_row_scale(ly.scales, ly.fmt, id * nblk + (part * 16) / a.blk);
                 e4m3x4_scaled_to_bf16(v.x, sc, o0.x, o0.y);
                 e4m3x4_scaled_to_bf16(v.y, sc, o0.z, o0.w);
                 e4m3x4_scaled_to_bf16(v.z, sc, o1.x, o1.y);

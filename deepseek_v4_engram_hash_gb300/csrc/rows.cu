@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(256) rows_fp8_kernel(const RowsArgs a) {
         uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
         if (id >= 0 && id < a.R) {
             const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.table + id * a.hd) + part);
-            const float sc = __ldg(a.scales + id * nblk + (part * 16) / a.blk);
+            const float sc = fp8_row_scale(a.scales, a.fmt, id * nblk + (part * 16) / a.blk);
             e4m3x4_scaled_to_bf16(v.x, sc, o0.x, o0.y);
             e4m3x4_scaled_to_bf16(v.y, sc, o0.z, o0.w);
             e4m3x4_scaled_to_bf16(v.z, sc, o1.x, o1.y);

@@ -58,6 +58,7 @@ extern "C" {
 
 #define ENGRAM_FMT_FP8 0        /* e4m3 codes [rows, head_dim] + f32 scales [rows, head_dim / scale_block] */
 #define ENGRAM_FMT_Q2K 1        /* 84-byte Q2_K super-blocks [rows, 84]; head_dim must be 256 */
+#define ENGRAM_FMT_FP8_E8M0 2   /* e4m3 codes [rows, head_dim] + one-byte e8m0 scales [rows, head_dim / scale_block] */
 
 /* Geometry.  C = (max_ngram - 1) * n_heads, K = C * head_dim, N = dim * (hc + 1).
  * Limits: 1 <= n_layers <= 4; 2 <= max_ngram <= 16; n_heads >= 1;
@@ -115,6 +116,14 @@ int engram_rows_fp8(const uint8_t *d_table, const float *d_scales, int64_t R, in
                     int32_t scale_block, const int64_t *d_row_ids, int64_t n_tok,
                     int64_t id_stride, int32_t C, uint16_t *d_rows, uintptr_t stream);
 
+/* Stage 2, fp8 rows with one-byte scales: as engram_rows_fp8, with d_scales
+ * [R, head_dim / scale_block] e8m0 bytes, scale = 2^(byte - 127) (the byte
+ * `f32_to_e8m0_rne` on the CPU reference page stores; 255 is NaN).  Rows are
+ * bit-identical to engram_rows_fp8 with the equal f32 scales. */
+int engram_rows_fp8_e8m0(const uint8_t *d_table, const uint8_t *d_scales, int64_t R, int32_t head_dim,
+                         int32_t scale_block, const int64_t *d_row_ids, int64_t n_tok, int64_t id_stride,
+                         int32_t C, uint16_t *d_rows, uintptr_t stream);
+
 /* Stage 2, Q2_K rows (spark_model/layers/engram_v41.rs, `rows_from_q2k`;
  * head_dim 256): d_blocks [R, 84] u8 (4-byte aligned), ggml Q2_K layout,
  * decoded y = d * (sc & 15) * q - dmin * (sc >> 4), then bf16 RNE.  Bit-exact. */
@@ -148,10 +157,11 @@ int engram_project_q2k(const uint16_t *d_x, const uint8_t *d_wkv_q2k, int32_t K,
 
 /* One engram layer for engram_forward. */
 typedef struct {
-    const void *table;      /* FP8: e4m3 [rows, head_dim]; Q2K: blocks [rows, 84] */
-    const float *scales;    /* FP8: [rows, head_dim / scale_block]; Q2K: unused */
+    const void *table;      /* FP8, FP8_E8M0: e4m3 [rows, head_dim]; Q2K: blocks [rows, 84] */
+    const void *scales;     /* FP8: f32 [rows, head_dim / scale_block]; FP8_E8M0: e8m0 bytes,
+                               same shape; Q2K: unused */
     int64_t rows;           /* table rows (sum of the layer's primes) */
-    int32_t fmt;            /* ENGRAM_FMT_FP8 or ENGRAM_FMT_Q2K */
+    int32_t fmt;            /* ENGRAM_FMT_FP8, ENGRAM_FMT_Q2K or ENGRAM_FMT_FP8_E8M0 */
     const uint16_t *wkv;    /* [dim * (hc + 1), C * head_dim] bf16; may be NULL when wkv_q2k
                                is set and every call has batch * T == 1 */
     const float *qk;        /* [hc, dim] f32 */

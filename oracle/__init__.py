@@ -69,6 +69,10 @@ def lib() -> ctypes.CDLL:
             L.orc_f32_to_e4m3.restype = ctypes.c_uint8
             L.orc_f32_to_e8m0.argtypes = [ctypes.c_float]
             L.orc_f32_to_e8m0.restype = ctypes.c_float
+            L.orc_e8m0_to_f32.argtypes = [ctypes.c_uint8]
+            L.orc_e8m0_to_f32.restype = ctypes.c_float
+            L.orc_rows_fp8_e8m0.argtypes = [P, P, i64, i32, i32, P, i64, P]
+            L.orc_rows_fp8_e8m0.restype = i32
             L.orc_hash.argtypes = [P, i64, i64, P, P, P, i32, i32, i32, P, i32, i64, P, i32, i64, P]
             L.orc_hash.restype = i32
             L.orc_rows_fp8.argtypes = [P, P, i64, i32, i32, P, i64, P]
@@ -121,6 +125,10 @@ def f32_to_e8m0(x: float) -> float:
     return float(lib().orc_f32_to_e8m0(float(x)))
 
 
+def e8m0_to_f32(code: int) -> float:
+    return float(lib().orc_e8m0_to_f32(int(code)))
+
+
 # ---- stages ----------------------------------------------------------------
 
 class HashState:
@@ -166,6 +174,19 @@ def rows_fp8(table, scales, hd: int, scale_block: int, ids) -> np.ndarray:
     rc = lib().orc_rows_fp8(_p(table), _p(scales), R, hd, scale_block, _p(ids), ids.size, _p(out))
     if rc != OK:
         raise ValueError(f"oracle rows_fp8 error {rc}")
+    return out
+
+
+def rows_fp8_e8m0(table, scales_u8, hd: int, scale_block: int, ids) -> np.ndarray:
+    """table [R, hd] e4m3 codes, scales [R, hd/blk] e8m0 bytes, ids [n] -> [n, hd] bf16 bits."""
+    table = _c(table, np.uint8)
+    scales = _c(scales_u8, np.uint8)
+    ids = _c(ids, np.int64).ravel()
+    R = table.size // hd
+    out = np.zeros((ids.size, hd), dtype=np.uint16)
+    rc = lib().orc_rows_fp8_e8m0(_p(table), _p(scales), R, hd, scale_block, _p(ids), ids.size, _p(out))
+    if rc != OK:
+        raise ValueError(f"oracle rows_fp8_e8m0 error {rc}")
     return out
 
 

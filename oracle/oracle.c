@@ -124,6 +124,14 @@ float orc_f32_to_e8m0(float x) {
     return u2f(e << 23);
 }
 
+/* e8m0 byte -> f32: the byte is a biased exponent, value 2^(code - 127);
+ * code 255 is NaN (the byte f32_to_e8m0_rne's result stores: its exponent
+ * field).  Code 0 is 2^-127, an f32 subnormal. */
+float orc_e8m0_to_f32(uint8_t code) {
+    if (code == 255) return NAN;
+    return ldexpf(1.0f, (int)code - 127);
+}
+
 /* ------------------------------------------------------------------ */
 /* Stage 1: the n-gram hash                                             */
 /* ------------------------------------------------------------------ */
@@ -219,6 +227,27 @@ int orc_rows_fp8(const uint8_t *table, const float *scales, int64_t R, int hd, i
         for (int d = 0; d < hd; ++d) {
             const float v = orc_e4m3_to_f32(table[id * hd + d]);
             const float s = scales[id * nblk + d / blk];
+            out[i * hd + d] = orc_f32_to_bf16(v * s);
+        }
+    }
+    return ORC_OK;
+}
+
+/* The fp8 rows with one-byte e8m0 scales (the 1-byte scale storage of
+ * `f32_to_e8m0_rne` on the CPU reference page):
+ *   row(id)[d] = bf16_rne( e4m3_to_f32(table[id][d]) * e8m0_to_f32(scales[id][d / blk]) )
+ * scales [R, hd / blk] u8. */
+int orc_rows_fp8_e8m0(const uint8_t *table, const uint8_t *scales, int64_t R, int hd, int blk,
+                      const int64_t *ids, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i)
+        if (ids[i] < 0 || ids[i] >= R) return ORC_E_ROW;
+    const int nblk = hd / blk;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t id = ids[i];
+        for (int d = 0; d < hd; ++d) {
+            const float v = orc_e4m3_to_f32(table[id * hd + d]);
+            const float s = orc_e8m0_to_f32(scales[id * nblk + d / blk]);
             out[i * hd + d] = orc_f32_to_bf16(v * s);
         }
     }

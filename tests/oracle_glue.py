@@ -25,6 +25,10 @@ def rows(cfg, layer, ids) -> np.ndarray:
     if cfg.fmt == "fp8":
         codes, scales = synth.table_fp8_rows(cfg, layer, uniq)
         return oracle.rows_fp8(codes, scales, cfg.head_dim, cfg.scale_block, inv)
+    if cfg.fmt == "fp8_e8m0":
+        codes, scales = synth.table_fp8_rows(cfg, layer, uniq)
+        e8 = ((scales.view(np.int32) >> 23) & 0xFF).astype(np.uint8)      # exact powers of two
+        return oracle.rows_fp8_e8m0(codes, e8, cfg.head_dim, cfg.scale_block, inv)
     blocks = synth.table_q2k_rows(cfg, layer, uniq)
     return oracle.rows_q2k(blocks, inv)
 

@@ -131,3 +131,29 @@ def test_q2k_gather_and_bounds(orc):
     import pytest
     with pytest.raises(ValueError):
         orc.rows_q2k(blocks, [3])
+
+
+def test_e8m0_decode_exact_powers(orc):
+    """code c -> 2^(c - 127) exactly (c = 0 is the f32 subnormal 2^-127), 255 -> NaN;
+    and the page's encoder maps every such power back to itself."""
+    for c in range(255):
+        v = orc.e8m0_to_f32(c)
+        assert Fraction(v) == Fraction(2) ** (c - 127), c
+        if c >= 1:
+            assert orc.f32_to_e8m0(v) == v
+    assert np.isnan(orc.e8m0_to_f32(255))
+
+
+def test_fp8_rows_e8m0_scales_exact(orc):
+    """One-byte scales give the float64 product e4m3 x 2^(code-127) exactly."""
+    codes = np.array([b for b in range(256) if b & 0x7F != 0x7F], dtype=np.uint8)
+    hd, blk = 256, 32
+    table = np.zeros((15, hd), dtype=np.uint8)
+    table[:, :codes.size] = codes
+    sc = np.array([[117 + r] * (hd // blk) for r in range(15)], dtype=np.uint8)   # 2^-10 .. 2^4
+    out = orc.rows_fp8_e8m0(table, sc, hd, blk, np.arange(15))
+    vals = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    for r in range(15):
+        want = vals[codes].astype(np.float64) * 2.0 ** (r - 10)
+        got = orc.bf16_bits_to_f32(out[r, :codes.size]).astype(np.float64)
+        assert np.array_equal(got, want) and np.array_equal(np.signbit(got), np.signbit(want))
