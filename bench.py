@@ -226,7 +226,7 @@ def run_prefill(args):
     return dict(cfg=cfg, ms=ms, stage_ms=stage.mean(0).tolist())
 
 
-def run_other(cfg, prefill_steps, decode_steps, warm=3):
+def run_other(cfg, prefill_steps, decode_steps, warm=3, tables_on_host=False):
     """Prefill (batch x T tokens in one call) and, if asked, single-token decode
     steps of every sequence, for the Q2_K and large-table workloads."""
     import torch
@@ -235,7 +235,7 @@ def run_other(cfg, prefill_steps, decode_steps, warm=3):
 
     B, T = cfg.batch, cfg.T
     M = B * T
-    eng = runner.EngramSetup(cfg, batch=B, max_tokens=M)
+    eng = runner.EngramSetup(cfg, batch=B, max_tokens=M, tables_on_host=tables_on_host)
     d_h = torch.empty((M, cfg.hc, cfg.dim), dtype=torch.float32, device="cuda")
     synth.fill_highway_cuda(cfg, d_h)
     ids = torch.from_numpy(eng.ids_for("prefill", T)).cuda()
@@ -288,14 +288,14 @@ def run_other(cfg, prefill_steps, decode_steps, warm=3):
     return out
 
 
-def run_decode_only(cfg, steps, warm=10):
+def run_decode_only(cfg, steps, warm=10, tables_on_host=False):
     """Single-token decode steps (batch 1) after the configured look-back."""
     import torch
     from deepseek_v4_engram_hash_gb300 import _lib as E
     from deepseek_v4_engram_hash_gb300 import runner, synth
 
     cfg = cfg.with_(decode_steps=steps + warm + 8)
-    eng = runner.EngramSetup(cfg, batch=1, max_tokens=1)
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=1, tables_on_host=tables_on_host)
     if cfg.prefix:
         pre = torch.from_numpy(eng.ids_for("prefix", cfg.prefix)).cuda()
         out = torch.empty((1, cfg.prefix, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
@@ -482,6 +482,13 @@ def main():
         r["workload"] = configs.V41_DECODE_E8M0.name
         r["note"] = "one-byte e8m0 table scales (264 B a row instead of 288 B)"
         others[configs.V41_DECODE_E8M0.name] = r
+        r = run_decode_only(configs.V41_DECODE, 2000, tables_on_host=True)
+        r["workload"] = "v41_decode_T1_host_tables"
+        r["note"] = "tables in page-locked host memory, rows read in place over the CPU-GPU link"
+        others["v41_decode_T1_host_tables"] = r
+        r = run_other(configs.V41_PREFILL, 5, 0, tables_on_host=True)
+        r["workload"] = "v41_prefill_T4096_host_tables"
+        others["v41_prefill_T4096_host_tables"] = r
         r = run_decode_only(configs.V41_DECODE_WKVQ2K, 2000)
         r["workload"] = configs.V41_DECODE_WKVQ2K.name
         r["note"] = "projection read from Q2_K-quantised wkv (82.6 MB a step instead of 503.3 MB)"

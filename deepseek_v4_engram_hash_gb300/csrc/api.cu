@@ -91,6 +91,20 @@ int dev_copy(T **dst, const T *src, size_t n) {
     return ENGRAM_OK;
 }
 
+// Tables may live in device memory or in page-locked host memory the device
+// reads in place (mapped, same address); anything else would fault the GPU,
+// so it is refused before any launch.
+bool device_readable(const void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return true;
+    if (at.type == cudaMemoryTypeHost) return at.devicePointer == p;
+    return false;
+}
+
 // The projection of one layer's x [M, K] (or of its fused gather) into kv.
 bool gemv_fits(int M, int K) {
     return M >= 1 && M <= kSmallT && gemv_smem_bytes(M, K) <= 200 * 1024;
@@ -280,6 +294,7 @@ int engram_rows_fp8(const uint8_t *d_table, const float *d_scales, int64_t R, in
         head_dim % scale_block)
         return ENGRAM_E_INVALID;
     if (!aligned(d_table, 16) || !aligned(d_scales, 4)) return ENGRAM_E_ALIGN;
+    if (!device_readable(d_table) || !device_readable(d_scales)) return ENGRAM_E_INVALID;
     RowsArgs a{d_table, d_scales, R, head_dim, scale_block, d_row_ids, n_tok, id_stride, C, d_rows, err_ptr(),
                ENGRAM_FMT_FP8};
     if (!a.err) return ENGRAM_E_CUDA;
@@ -296,6 +311,7 @@ int engram_rows_fp8_e8m0(const uint8_t *d_table, const uint8_t *d_scales, int64_
         head_dim % scale_block)
         return ENGRAM_E_INVALID;
     if (!aligned(d_table, 16)) return ENGRAM_E_ALIGN;
+    if (!device_readable(d_table) || !device_readable(d_scales)) return ENGRAM_E_INVALID;
     RowsArgs a{d_table, d_scales, R, head_dim, scale_block, d_row_ids, n_tok, id_stride, C, d_rows, err_ptr(),
                ENGRAM_FMT_FP8_E8M0};
     if (!a.err) return ENGRAM_E_CUDA;
@@ -307,6 +323,7 @@ int engram_rows_q2k(const uint8_t *d_blocks, int64_t R, const int64_t *d_row_ids
     int rc = check_rows(d_blocks, d_row_ids, R, n_tok, id_stride, C, d_rows);
     if (rc) return rc;
     if (!aligned(d_blocks, 4)) return ENGRAM_E_ALIGN;
+    if (!device_readable(d_blocks)) return ENGRAM_E_INVALID;
     RowsArgs a{d_blocks, nullptr, R, 256, 256, d_row_ids, n_tok, id_stride, C, d_rows, err_ptr(), ENGRAM_FMT_Q2K};
     if (!a.err) return ENGRAM_E_CUDA;
     return cuda_rc(launch_rows_q2k(a, S(stream)));
@@ -435,6 +452,7 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
             return ENGRAM_E_INVALID;
         }
         if (!aligned(ly.wkv, 16) || !aligned(ly.qk, 16)) return ENGRAM_E_ALIGN;
+        if (!device_readable(ly.table) || (ly.scales && !device_readable(ly.scales))) return ENGRAM_E_INVALID;
     }
     if (M > (int64_t)1 << 24) return ENGRAM_E_UNSUPPORTED;
     if (ws_bytes < engram_workspace_bytes(&g, M)) return ENGRAM_E_WORKSPACE;

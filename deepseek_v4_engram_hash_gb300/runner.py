@@ -15,8 +15,12 @@ from . import synth
 
 
 class EngramSetup:
-    def __init__(self, cfg, device="cuda", batch: int | None = None, max_tokens: int | None = None):
+    def __init__(self, cfg, device="cuda", batch: int | None = None, max_tokens: int | None = None,
+                 tables_on_host: bool = False):
+        """tables_on_host: keep the per-layer tables in page-locked host memory,
+        read row by row in place by the kernels (tables larger than HBM)."""
         self.cfg = cfg
+        self.tables_on_host = tables_on_host
         self.device = torch.device(device)
         self.batch = int(batch or cfg.batch)
         t = synth.hash_tables(cfg)
@@ -56,6 +60,11 @@ class EngramSetup:
                     E.engram_rows_q2k(d["wkv_q2k"], nb, ids, nb, 1, 1, d["wkv"])
                 else:
                     synth.fill_wkv_cuda(cfg, l, d["wkv"])
+                if tables_on_host:
+                    for key in ("table", "scales"):
+                        if d.get(key) is not None:
+                            d[key] = d[key].cpu().pin_memory()      # device-visible, read in place
+                    torch.cuda.empty_cache()
                 q, k = synth.qk_weights(cfg, l)
                 d["q"], d["k"] = q, k
                 d["qk"] = torch.from_numpy(q * k).to(self.device)   # exact: bf16 x bf16 fits f32

@@ -24,6 +24,12 @@
  *   - Return value: ENGRAM_OK (0) or a negative ENGRAM_E_* code.  Arguments
  *     are validated on the host before anything is enqueued; a call that
  *     returns an error has enqueued nothing.
+ *   - Tables (fp8 codes and scales, Q2_K blocks) may live in device memory
+ *     or in page-locked host memory that the device reads in place (mapped
+ *     at the same address, e.g. cudaHostAlloc): rows are then read by id over
+ *     the CPU-GPU link, so a table need not fit in HBM (the page-locked,
+ *     device-visible arena of spark_model/layers/deepseek_v41_layer.rs).  Any
+ *     other table pointer is refused with ENGRAM_E_INVALID.
  *   - T = 0 is a valid no-op for every call that takes a token count; its
  *     buffers may then be null.
  *   - Conditions only the device can see (a token id outside token_map, a
