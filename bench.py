@@ -325,6 +325,44 @@ def run_decode_only(cfg, steps, warm=10, tables_on_host=False):
             "step_algorithmic_bytes": sb, "step_gbs": sb / (ms * 1e-3) / 1e9}
 
 
+def run_decode_graph(cfg, steps, warm=10):
+    """Single-token decode steps replayed from one captured graph; the next
+    ids are copied into the graph's id buffer on the device before each replay."""
+    import torch
+    from deepseek_v4_engram_hash_gb300 import _lib as E
+    from deepseek_v4_engram_hash_gb300 import runner, synth
+
+    cfg = cfg.with_(decode_steps=steps + warm + 8)
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=1)
+    pre = torch.from_numpy(eng.ids_for("prefix", cfg.prefix)).cuda()
+    out = torch.empty((1, cfg.prefix, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
+    E.engram_hash(eng.hasher, pre, cfg.prefix, 0, out)
+    n = warm + steps
+    ids = torch.from_numpy(eng.ids_for("decode", n).reshape(n, 1, 1)).cuda()
+    d_ids = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    d_pos = torch.tensor([cfg.prefix], dtype=torch.int64, device="cuda")
+    d_h = torch.from_numpy(synth.highway(cfg, [cfg.prefix])).cuda()
+    graph = E.Graph(eng.hasher, eng.layers, d_ids, 1, d_pos, d_h, cfg.eps, eng.ws, eng.ws_bytes)
+    for i in range(warm):
+        d_ids.copy_(ids[i])
+        graph.launch()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        d_ids.copy_(ids[warm + i])
+        graph.launch()
+    t1.record()
+    torch.cuda.synchronize()
+    assert E.engram_check() == 0
+    ms = t0.elapsed_time(t1) / steps
+    graph.close()
+    del eng
+    torch.cuda.empty_cache()
+    return {"tokens_per_step": 1, "ms_per_step": ms, "tokens_per_s": 1.0 / (ms * 1e-3),
+            "note": "one graph replay a step plus a device copy of the next id"}
+
+
 def _barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -482,6 +520,9 @@ def main():
         r["workload"] = configs.V41_DECODE_E8M0.name
         r["note"] = "one-byte e8m0 table scales (264 B a row instead of 288 B)"
         others[configs.V41_DECODE_E8M0.name] = r
+        r = run_decode_graph(configs.V41_DECODE, 2000)
+        r["workload"] = "v41_decode_T1_graph"
+        others["v41_decode_T1_graph"] = r
         r = run_decode_only(configs.V41_DECODE, 2000, tables_on_host=True)
         r["workload"] = "v41_decode_T1_host_tables"
         r["note"] = "tables in page-locked host memory, rows read in place over the CPU-GPU link"

@@ -72,6 +72,12 @@ def lib() -> ctypes.CDLL:
                                      ctypes.c_float, P, sz, st], ctypes.c_int),
             "engram_forward_noalloc": ([P, ctypes.POINTER(engram_layer), P, i32, i64, P, ctypes.c_float,
                                         st], ctypes.c_int),
+            "engram_forward_dpos": ([P, ctypes.POINTER(engram_layer), P, i32, P, P, ctypes.c_float,
+                                     P, sz, st], ctypes.c_int),
+            "engram_graph_create": ([P, ctypes.POINTER(engram_layer), P, i32, P, P, ctypes.c_float,
+                                     P, sz, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
+            "engram_graph_launch": ([P, st], ctypes.c_int),
+            "engram_graph_destroy": ([P], None),
             "engram_workspace_bytes": ([ctypes.POINTER(engram_geom), i64], sz),
             "engram_workspace_layout": ([ctypes.POINTER(engram_geom), i64, ctypes.POINTER(sz)],
                                         ctypes.c_int),
@@ -240,6 +246,38 @@ def engram_forward_noalloc(hs: Hasher, layers, d_ids, T, start_pos, d_h, eps, st
     arr = layers if isinstance(layers, ctypes.Array) else layers_array(layers)
     _ok(lib().engram_forward_noalloc(hs.handle, arr, _ptr(d_ids), int(T), int(start_pos), _ptr(d_h),
                                      float(eps), _stream(stream)), "engram_forward_noalloc")
+
+
+def engram_forward_dpos(hs: Hasher, layers, d_ids, T, d_start_pos, d_h, eps, d_ws, ws_bytes, stream=None):
+    arr = layers if isinstance(layers, ctypes.Array) else layers_array(layers)
+    _ok(lib().engram_forward_dpos(hs.handle, arr, _ptr(d_ids), int(T), _ptr(d_start_pos), _ptr(d_h),
+                                  float(eps), _ptr(d_ws), int(ws_bytes), _stream(stream)), "engram_forward_dpos")
+
+
+class Graph:
+    """A captured decode step (`engram_graph_create`); replay with launch()."""
+
+    def __init__(self, hs: Hasher, layers, d_ids, T, d_start_pos, d_h, eps, d_ws, ws_bytes):
+        self._keep = (hs, layers if isinstance(layers, ctypes.Array) else layers_array(layers))
+        g = ctypes.c_void_p()
+        _ok(lib().engram_graph_create(hs.handle, self._keep[1], _ptr(d_ids), int(T), _ptr(d_start_pos),
+                                      _ptr(d_h), float(eps), _ptr(d_ws), int(ws_bytes), ctypes.byref(g)),
+            "engram_graph_create")
+        self.handle = g
+
+    def launch(self, stream=None):
+        _ok(lib().engram_graph_launch(self.handle, _stream(stream)), "engram_graph_launch")
+
+    def close(self):
+        if self.handle:
+            lib().engram_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def engram_workspace_bytes(geom: engram_geom, max_tokens: int) -> int:

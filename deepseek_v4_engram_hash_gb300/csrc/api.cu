@@ -231,13 +231,14 @@ int engram_check(uintptr_t stream) {
 namespace {
 
 HashArgs hash_args(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t start_pos,
-                   int64_t *d_row_ids) {
+                   int64_t *d_row_ids, const int64_t *d_pos = nullptr) {
     const engram_tables *t = hs->t;
     HashArgs a;
     a.ids = d_ids;
     a.B = hs->batch;
     a.T = T;
     a.start_pos = start_pos;
+    a.start_pos_dev = d_pos;
     a.token_map = t->token_map;
     a.vocab = t->g.vocab;
     a.pad_id = t->pad_id;
@@ -422,11 +423,19 @@ size_t engram_workspace_bytes(const engram_geom *geom, int64_t max_tokens) {
     return off[1 + 2 * geom->n_layers];
 }
 
-int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
-                   int64_t start_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes, uintptr_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward; d_pos (device memory) replaces start_pos when set, and is then
+// advanced by T at the end of the step.
+int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
+                 int64_t start_pos, int64_t *d_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes,
+                 uintptr_t stream) {
     if (!hs || !layers) return ENGRAM_E_NULL;
-    int rc = check_hash(hs, d_ids, T, start_pos, d_ws);
+    int rc = check_hash(hs, d_ids, T, d_pos ? 0 : start_pos, d_ws);
     if (rc || T == 0) return rc;                  // T == 0: a valid no-op
+    if (d_pos && !aligned(d_pos, 8)) return ENGRAM_E_ALIGN;
     if (!d_h) return ENGRAM_E_NULL;
     const engram_geom &g = hs->t->g;
     if (!(eps >= 0.0f)) return ENGRAM_E_INVALID;
@@ -472,7 +481,7 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
     record(0, s);
     cudaError_t e = cudaSuccess;
     if (!fuse_hash) {
-        e = launch_hash(hash_args(hs, d_ids, T, start_pos, ids), s);
+        e = launch_hash(hash_args(hs, d_ids, T, start_pos, ids, d_pos), s);
         if (e != cudaSuccess) return ENGRAM_E_CUDA;
     }
     record(1, s);
@@ -485,6 +494,8 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
     ga.D = g.dim;
     ga.eps = eps;
     ga.inv_sqrt_dim = powf((float)g.dim, -0.5f);
+    ga.advance_pos = d_pos;
+    ga.advance_by = T;
     for (int l = 0; l < L; ++l) {
         ga.kv[l] = reinterpret_cast<uint16_t *>(ws + off[1 + l]);
         ga.qk[l] = layers[l].qk;
@@ -515,7 +526,7 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
         a.id_stride = (int64_t)L * C;
         a.gather = 1;
         a.fuse_hash = fuse_hash ? 1 : 0;
-        a.hash = hash_args(hs, d_ids, T, start_pos, ids);
+        a.hash = hash_args(hs, d_ids, T, start_pos, ids, d_pos);
         a.pdl = 1;
         a.err = err;
         ga.pdl = 1;
@@ -553,6 +564,77 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
     if (launch_gate(ga, s) != cudaSuccess) return ENGRAM_E_CUDA;
     record(4, s);
     return ENGRAM_OK;
+}
+
+}  // namespace
+
+struct engram_graph {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+extern "C" {
+
+int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
+                   int64_t start_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes, uintptr_t stream) {
+    return forward_impl(hs, layers, d_ids, T, start_pos, nullptr, d_h, eps, d_ws, ws_bytes, stream);
+}
+
+int engram_forward_dpos(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
+                        int64_t *d_start_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes,
+                        uintptr_t stream) {
+    if (!d_start_pos) return ENGRAM_E_NULL;
+    return forward_impl(hs, layers, d_ids, T, 0, d_start_pos, d_h, eps, d_ws, ws_bytes, stream);
+}
+
+int engram_graph_create(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
+                        int64_t *d_start_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes,
+                        engram_graph **out) {
+    if (!out) return ENGRAM_E_NULL;
+    *out = nullptr;
+    if (!hs || !layers || !d_start_pos) return ENGRAM_E_NULL;
+    if (T < 1) return ENGRAM_E_INVALID;
+    if (!err_ptr()) return ENGRAM_E_CUDA;            // looked up before the capture
+    cudaStream_t cs;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return ENGRAM_E_CUDA;
+    const uintptr_t *prof = g_prof_events;
+    g_prof_events = nullptr;                          // no profiling events inside the graph
+    int rc = ENGRAM_OK;
+    cudaGraph_t graph = nullptr;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        rc = ENGRAM_E_CUDA;
+    } else {
+        rc = forward_impl(hs, layers, d_ids, T, 0, d_start_pos, d_h, eps, d_ws, ws_bytes,
+                          reinterpret_cast<uintptr_t>(cs));
+        if (cudaStreamEndCapture(cs, &graph) != cudaSuccess && rc == ENGRAM_OK) rc = ENGRAM_E_CUDA;
+    }
+    g_prof_events = prof;
+    cudaStreamDestroy(cs);
+    if (rc != ENGRAM_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return rc;
+    }
+    engram_graph *g = new engram_graph();
+    g->graph = graph;
+    if (cudaGraphInstantiate(&g->exec, graph, 0) != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        delete g;
+        return ENGRAM_E_CUDA;
+    }
+    *out = g;
+    return ENGRAM_OK;
+}
+
+int engram_graph_launch(engram_graph *g, uintptr_t stream) {
+    if (!g) return ENGRAM_E_NULL;
+    return cuda_rc(cudaGraphLaunch(g->exec, S(stream)));
+}
+
+void engram_graph_destroy(engram_graph *g) {
+    if (!g) return;
+    cudaGraphExecDestroy(g->exec);
+    cudaGraphDestroy(g->graph);
+    delete g;
 }
 
 int engram_forward_host(engram_hasher *hs, const engram_layer *layers, const int32_t *h_ids, int32_t *d_ids,

@@ -109,6 +109,7 @@ struct HashArgs {
     const int32_t *ids;
     int32_t B, T;
     int64_t start_pos;
+    const int64_t *start_pos_dev;   // when set, the start position is read here (device memory)
     const int64_t *token_map;
     int64_t vocab, pad_id;
     const int64_t *mult, *primes, *offsets;
@@ -119,6 +120,18 @@ struct HashArgs {
     int *err;
 };
 cudaError_t launch_hash(const HashArgs &a, cudaStream_t s);
+
+// The call's start position: the host value, or the device-resident one.
+// A device position that does not fit the cache raises ENGRAM_E_CAPACITY;
+// the caller then skips every cache access (false).
+__device__ __forceinline__ bool hash_start(const HashArgs &a, int64_t &sp) {
+    sp = a.start_pos_dev ? *a.start_pos_dev : a.start_pos;
+    if (sp < 0 || sp + a.T > a.max_seq) {
+        set_err(a.err, ENGRAM_E_CAPACITY);
+        return false;
+    }
+    return true;
+}
 
 // Compressed id of input token s of sequence b (the token_map lookup); an id
 // outside token_map raises ENGRAM_E_TOKEN and reads as unmapped (-1).
@@ -140,9 +153,9 @@ __device__ __forceinline__ int64_t hash_compress(const HashArgs &a, int b, int64
 // and the id is rem_euclid(rolling, prime) + offset, all i64 with wrap.  Ids
 // of this call come from the input through token_map, older positions from
 // the cache, so no thread depends on another thread's cache write.
-__device__ __forceinline__ int64_t hash_one(const HashArgs &a, int b, int s, int li, int col) {
+__device__ __forceinline__ int64_t hash_one(const HashArgs &a, int64_t sp, int b, int s, int li, int col) {
     const int C = (a.ng - 1) * a.H;
-    const int64_t pos = a.start_pos + s;
+    const int64_t pos = sp + s;
     const int n_top = col / a.H + 1;
     int64_t tok[kMaxNgram];
     bool blocked = false;
@@ -150,8 +163,8 @@ __device__ __forceinline__ int64_t hash_one(const HashArgs &a, int b, int s, int
         int64_t src;
         if (pos < shift) {
             src = 0;                                 // blocked below; value unused
-        } else if (pos - shift >= a.start_pos) {
-            src = hash_compress(a, b, pos - shift - a.start_pos);
+        } else if (pos - shift >= sp) {
+            src = hash_compress(a, b, pos - shift - sp);
         } else {
             src = a.cache[(int64_t)b * a.max_seq + (pos - shift)];
         }
@@ -227,6 +240,8 @@ cudaError_t launch_gemm_simt(const uint16_t *x, const uint16_t *wkv, uint16_t *k
 // Gate over several layers on one highway.
 struct GateArgs {
     float *h;                           // [M, hc, D]
+    int64_t *advance_pos;               // when set, block 0 adds advance_by once the projection is done
+    int64_t advance_by;
     const uint16_t *kv[kMaxLayers];     // [M, (hc+1) D]
     const float *qk[kMaxLayers];        // [hc, D]
     int32_t L, M, hc, D;

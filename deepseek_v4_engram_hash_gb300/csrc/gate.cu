@@ -101,6 +101,8 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constan
         griddep_wait();
         griddep_launch();
     }
+    if (a.advance_pos && blockIdx.x == 0 && threadIdx.x == 0)
+        *a.advance_pos += a.advance_by;     // every read of the position happened in the projection
     load_kv(a, 0, t, c, cur);
     for (int l = 0; l < a.L; ++l) {
         if (kPipe && l + 1 < a.L) {

@@ -105,14 +105,16 @@ __device__ __forceinline__ void stage_x(const GemvArgs &a, const GemvLayer &ly, 
 // them to the workspace, and the very first CTA writes the cache.
 __device__ __forceinline__ void hash_ids(const GemvArgs &a, int T, int li, int cta, int64_t *s_ids) {
     const HashArgs &h = a.hash;
+    int64_t sp;
+    const bool ok = hash_start(h, sp);       // a device position past the cache: ids read as -1 (rows 0)
     for (int j = threadIdx.x; j < T * a.C; j += blockDim.x) {
         const int m = j / a.C, col = j % a.C;
         const int b = m / h.T, s = m % h.T;
-        const int64_t id = hash_one(h, b, s, li, col);
+        const int64_t id = ok ? hash_one(h, sp, b, s, li, col) : -1;
         s_ids[j] = id;
         if (cta == 0) h.out[((int64_t)m * a.L + li) * a.C + col] = id;
-        if (cta == 0 && li == 0 && col == 0)
-            h.cache[(int64_t)b * h.max_seq + h.start_pos + s] = hash_compress(h, b, s);
+        if (ok && cta == 0 && li == 0 && col == 0)
+            h.cache[(int64_t)b * h.max_seq + sp + s] = hash_compress(h, b, s);
     }
 }
 

@@ -20,6 +20,8 @@ namespace engram {
 __global__ void __launch_bounds__(256) hash_kernel(const HashArgs a) {
     const int C = (a.ng - 1) * a.H;
     const int64_t total = (int64_t)a.B * a.T * a.L * C;
+    int64_t sp;
+    if (!hash_start(a, sp)) return;
     for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
          g += (int64_t)gridDim.x * blockDim.x) {
         const int col = (int)(g % C);
@@ -27,8 +29,8 @@ __global__ void __launch_bounds__(256) hash_kernel(const HashArgs a) {
         const int64_t bs = g / ((int64_t)C * a.L);
         const int s = (int)(bs % a.T);
         const int b = (int)(bs / a.T);
-        a.out[g] = hash_one(a, b, s, li, col);
-        if (li == 0 && col == 0) a.cache[(int64_t)b * a.max_seq + a.start_pos + s] = hash_compress(a, b, s);
+        a.out[g] = hash_one(a, sp, b, s, li, col);
+        if (li == 0 && col == 0) a.cache[(int64_t)b * a.max_seq + sp + s] = hash_compress(a, b, s);
     }
 }
 

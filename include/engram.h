@@ -187,6 +187,30 @@ int engram_forward(engram_hasher *hs, const engram_layer *layers, const int32_t 
                    int32_t T, int64_t start_pos, float *d_h, float eps, void *d_ws,
                    size_t ws_bytes, uintptr_t stream);
 
+/* engram_forward with the start position in device memory: *d_start_pos
+ * (int64, 8-byte aligned) is read on the device and advanced by T when the
+ * step's last kernel runs, so consecutive calls -- or replays of a captured
+ * graph -- walk the sequence without the host.  A position past the cache is
+ * reported on the device (ENGRAM_E_CAPACITY through engram_check) and the
+ * step touches no cache entry. */
+int engram_forward_dpos(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
+                        int64_t *d_start_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes,
+                        uintptr_t stream);
+
+/* The decode step as one CUDA graph (the single-token step capture of
+ * spark_model/layers/deepseek_v41_layer.rs, `GraphMode`): captures
+ * engram_forward_dpos with these arguments -- every pointer is baked into the
+ * graph -- and replays it with engram_graph_launch.  Between replays the
+ * caller updates the contents of d_ids (and of d_h if it wishes); the
+ * position advances by itself.  Replays give bit-identical results to eager
+ * engram_forward calls at the same positions. */
+typedef struct engram_graph engram_graph;
+int engram_graph_create(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
+                        int64_t *d_start_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes,
+                        engram_graph **out);
+int engram_graph_launch(engram_graph *g, uintptr_t stream);
+void engram_graph_destroy(engram_graph *g);
+
 /* engram_forward from host buffers: enqueues the copy of h_ids [batch, T]
  * and h_h [batch*T, hc, dim] (pinned host memory recommended) into the
  * device staging buffers d_ids / d_h, the forward, and the copy of d_h back

@@ -1,0 +1,80 @@
+"""The decode step as a CUDA graph with a device-resident position (NEXT: the
+pages' single-token graph capture and its eager-versus-graph comparison):
+replays are bit-identical to eager calls at the same positions, the position
+advances by itself, and a position past the cache is reported, not written."""
+import numpy as np
+import pytest
+import torch
+
+import oracle_glue as G
+from deepseek_v4_engram_hash_gb300 import configs, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def E():
+    import __graft_entry__
+    __graft_entry__.build()
+    from deepseek_v4_engram_hash_gb300 import _lib
+    return _lib
+
+
+@pytest.mark.parametrize("cfg,B,T", [(configs.V41_DECODE, 1, 1), (configs.TINY, 2, 3), (configs.TINY, 1, 12)],
+                         ids=["v41_T1", "tiny_B2_T3", "tiny_T12_gemm"])
+def test_graph_replay_bit_identical_to_eager(E, cfg, B, T):
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = cfg.with_(batch=B)
+    eng = runner.EngramSetup(cfg, batch=B, max_tokens=B * T)
+    hs2 = E.Hasher(eng.tables, B, cfg.max_seq)
+    ws2 = torch.empty_like(eng.ws)
+    pos = cfg.prefix
+    if pos:
+        pre = torch.from_numpy(eng.ids_for("prefix", pos)).cuda()
+        out = torch.empty((B, pos, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
+        E.engram_hash(eng.hasher, pre, pos, 0, out)
+        E.engram_hash(hs2, pre, pos, 0, out)
+    d_pos = torch.tensor([pos], dtype=torch.int64, device="cuda")
+    d_ids = torch.zeros((B, T), dtype=torch.int32, device="cuda")
+    d_hg = torch.zeros((B * T, cfg.hc, cfg.dim), dtype=torch.float32, device="cuda")
+    graph = E.Graph(hs2, eng.layers, d_ids, T, d_pos, d_hg, cfg.eps, ws2, eng.ws_bytes)
+    ref = G.hash_state(cfg, B)
+    if cfg.prefix:
+        ref.forward(eng.ids_for("prefix", pos), 0)
+    for step in range(5):
+        ids = eng.ids_for(f"g{step}", T)
+        h0 = torch.from_numpy(synth.highway(cfg, np.arange(step * B * T, (step + 1) * B * T)))
+        d_he = h0.cuda()
+        eng.forward(ids, pos, d_he)                               # eager
+        d_ids.copy_(torch.from_numpy(ids))
+        d_hg.copy_(h0)
+        graph.launch()                                            # replay
+        assert E.engram_check() == 0
+        assert torch.equal(d_he, d_hg), f"step {step}"
+        assert torch.equal(eng.row_ids(B * T), (ws2[:B * T * cfg.n_layers * cfg.cols * 8]
+                                                .view(torch.int64).view(B * T, cfg.n_layers, cfg.cols)))
+        want = ref.forward(ids, pos).reshape(B * T, cfg.n_layers, cfg.cols)
+        assert np.array_equal(eng.row_ids(B * T).cpu().numpy(), want)
+        pos += T
+    assert d_pos.item() == pos
+    graph.close()
+
+
+def test_device_position_past_the_cache_is_reported(E):
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = configs.TINY.with_(prefix=0, T=4, decode_steps=0)
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=4)
+    cache_len = cfg.max_seq
+    d_pos = torch.tensor([cache_len - 2], dtype=torch.int64, device="cuda")     # 2 + 4 > remaining
+    ids = torch.ones((1, 4), dtype=torch.int32, device="cuda")
+    d_h = torch.zeros((4, cfg.hc, cfg.dim), device="cuda")
+    E.engram_forward_dpos(eng.hasher, eng.layers, ids, 4, d_pos, d_h, cfg.eps, eng.ws, eng.ws_bytes)
+    assert E.engram_check() == -4
+    # a valid call afterwards still hashes exactly (the failed step wrote nothing)
+    d_pos.fill_(0)
+    E.engram_forward_dpos(eng.hasher, eng.layers, ids, 4, d_pos, d_h, cfg.eps, eng.ws, eng.ws_bytes)
+    assert E.engram_check() == 0
+    ref = G.hash_state(cfg, 1)
+    assert np.array_equal(eng.row_ids(4).cpu().numpy(),
+                          ref.forward(ids.cpu().numpy(), 0).reshape(4, cfg.n_layers, cfg.cols))
+    assert d_pos.item() == 4
