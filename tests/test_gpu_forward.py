@@ -202,3 +202,28 @@ def test_forward_all_unmapped_tokens_use_pad_windows(E):
     _check_call(eng, ref, ids, 0, d_h, d_h.cpu().numpy(), np.arange(12), np.arange(cfg.N), 0)
     got = eng.row_ids(12).cpu().numpy()
     assert (got == got[0]).all()
+
+
+@pytest.mark.parametrize("T", [1, 6])
+def test_forward_host_buffers_match_device_forward(E, T):
+    """engram_forward_host (ids and highway in pinned host memory, copied in
+    and out on the stream) gives the same highway as engram_forward."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = configs.TINY.with_(batch=2)
+    eng = runner.EngramSetup(cfg, batch=2, max_tokens=2 * T)
+    hs2 = E.Hasher(eng.tables, 2, cfg.max_seq)
+    pos = 0
+    for step in range(3):
+        ids = eng.ids_for(f"host{step}", T)
+        h0 = synth.highway(cfg, np.arange(2 * T * step, 2 * T * (step + 1)))
+        d_h = torch.from_numpy(h0).cuda()
+        eng.forward(ids, pos, d_h)
+        h_ids = torch.from_numpy(ids).pin_memory()
+        h_h = torch.from_numpy(h0.copy()).pin_memory()
+        d_ids2 = torch.empty((2, T), dtype=torch.int32, device="cuda")
+        d_h2 = torch.empty((2 * T, cfg.hc, cfg.dim), dtype=torch.float32, device="cuda")
+        E.engram_forward_host(hs2, eng.layers, h_ids, d_ids2, T, pos, h_h, d_h2, cfg.eps, eng.ws, eng.ws_bytes)
+        torch.cuda.synchronize()
+        assert E.engram_check() == 0
+        assert torch.equal(h_h, d_h.cpu())
+        pos += T
