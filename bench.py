@@ -288,21 +288,21 @@ def run_other(cfg, prefill_steps, decode_steps, warm=3, tables_on_host=False):
     return out
 
 
-def run_decode_only(cfg, steps, warm=10, tables_on_host=False):
-    """Single-token decode steps (batch 1) after the configured look-back."""
+def run_decode_only(cfg, steps, warm=10, tables_on_host=False, batch=1):
+    """Single-token decode steps of `batch` sequences after the configured look-back."""
     import torch
     from deepseek_v4_engram_hash_gb300 import _lib as E
     from deepseek_v4_engram_hash_gb300 import runner, synth
 
-    cfg = cfg.with_(decode_steps=steps + warm + 8)
-    eng = runner.EngramSetup(cfg, batch=1, max_tokens=1, tables_on_host=tables_on_host)
+    cfg = cfg.with_(decode_steps=steps + warm + 8, batch=batch)
+    eng = runner.EngramSetup(cfg, batch=batch, max_tokens=batch, tables_on_host=tables_on_host)
     if cfg.prefix:
         pre = torch.from_numpy(eng.ids_for("prefix", cfg.prefix)).cuda()
-        out = torch.empty((1, cfg.prefix, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
+        out = torch.empty((batch, cfg.prefix, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
         E.engram_hash(eng.hasher, pre, cfg.prefix, 0, out)
     n = warm + steps
-    ids = torch.from_numpy(eng.ids_for("decode", n).reshape(n, 1, 1)).cuda()
-    d_h = torch.from_numpy(synth.highway(cfg, [cfg.prefix])).cuda()
+    ids = torch.from_numpy(eng.ids_for("decode", n).T.copy().reshape(n, batch, 1)).cuda()
+    d_h = torch.from_numpy(synth.highway(cfg, np.arange(batch))).cuda()
     pos = cfg.prefix
     for i in range(warm):
         eng.forward(ids[i], pos, d_h)
@@ -318,10 +318,10 @@ def run_decode_only(cfg, steps, warm=10, tables_on_host=False):
     assert E.engram_check() == 0
     ms = t0.elapsed_time(t1) / steps
     wbytes = cfg.n_layers * cfg.N * (cfg.K // 256) * 84 if cfg.wkv_fmt == "q2k" else cfg.n_layers * cfg.N * cfg.K * 2
-    sb = step_bytes(cfg, 1) - cfg.n_layers * cfg.N * cfg.K * 2 + wbytes
+    sb = step_bytes(cfg, batch) - cfg.n_layers * cfg.N * cfg.K * 2 + wbytes
     del eng
     torch.cuda.empty_cache()
-    return {"tokens_per_step": 1, "ms_per_step": ms, "tokens_per_s": 1.0 / (ms * 1e-3),
+    return {"tokens_per_step": batch, "ms_per_step": ms, "tokens_per_s": batch / (ms * 1e-3),
             "step_algorithmic_bytes": sb, "step_gbs": sb / (ms * 1e-3) / 1e9}
 
 
@@ -454,7 +454,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true", help="skip the Q2_K and large-table lines")
-    ap.add_argument("--only", choices=["decode", "prefill", "wkvq2k"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill", "wkvq2k", "decode8"], default=None,
                     help="run one workload only (for profiling); prints its own JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -474,6 +474,10 @@ def main():
     __graft_entry__.build()
 
     hbm, bf16_burst, bf16_sust, peak_src = _peaks()
+    if args.only == "decode8":
+        from deepseek_v4_engram_hash_gb300 import configs
+        print(json.dumps(run_decode_only(configs.V41_DECODE, args.steps, batch=8)), flush=True)
+        return
     if args.only == "wkvq2k":
         from deepseek_v4_engram_hash_gb300 import configs
         r = run_decode_only(configs.V41_DECODE_WKVQ2K, args.steps)

@@ -77,11 +77,13 @@ __device__ __forceinline__ void load_kv(const GateArgs &a, int l, int t, int c, 
     }
 }
 
-// NV = float4 chunks per thread (D <= kGateThreads * 4 * NV).  Up to NV = 4
-// the next layer's operands are loaded while this layer reduces.
-template <int NV>
-__global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constant__ GateArgs a) {
-    constexpr bool kPipe = NV <= 4;
+// NV = float4 chunks per thread (D <= kGateThreads * 4 * NV).  PIPE: the next
+// layer's operands load while this layer reduces -- the latency choice for a
+// handful of rows (one token); without it the kernel stays under 64
+// registers, so four CTAs share an SM -- the throughput choice for many rows.
+template <int NV, bool PIPE>
+__global__ void __launch_bounds__(kGateThreads, PIPE ? 1 : 4) gate_kernel(const __grid_constant__ GateArgs a) {
+    constexpr bool kPipe = PIPE && NV <= 4;
     __shared__ float red[3 * kGateThreads / 32];
     const int row = blockIdx.x;                       // (t, c)
     const int t = row / a.hc, c = row % a.hc;
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const __grid_constan
     }
 }
 
-template <int NV>
+template <int NV, bool PIPE>
 static cudaError_t launch_nv(const GateArgs &a, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.M * a.hc);
@@ -160,18 +162,24 @@ static cudaError_t launch_nv(const GateArgs &a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gate_kernel<NV>, a);
+    return cudaLaunchKernelEx(&cfg, gate_kernel<NV, PIPE>, a);
+}
+
+template <bool PIPE>
+static cudaError_t launch_p(const GateArgs &a, cudaStream_t s) {
+    const int per = kGateThreads * 4;
+    if (a.D <= per) return launch_nv<1, PIPE>(a, s);
+    if (a.D <= 2 * per) return launch_nv<2, PIPE>(a, s);
+    if (a.D <= 4 * per) return launch_nv<4, PIPE>(a, s);
+    if (a.D <= 8 * per) return launch_nv<8, false>(a, s);
+    if (a.D <= 16 * per) return launch_nv<16, false>(a, s);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gate(const GateArgs &a, cudaStream_t s) {
     if (a.M == 0) return cudaSuccess;
-    const int per = kGateThreads * 4;
-    if (a.D <= per) return launch_nv<1>(a, s);
-    if (a.D <= 2 * per) return launch_nv<2>(a, s);
-    if (a.D <= 4 * per) return launch_nv<4>(a, s);
-    if (a.D <= 8 * per) return launch_nv<8>(a, s);
-    if (a.D <= 16 * per) return launch_nv<16>(a, s);
-    return cudaErrorInvalidValue;
+    // one CTA per (token, stream): pipeline the layers when there are few rows
+    return (int64_t)a.M * a.hc <= 512 ? launch_p<true>(a, s) : launch_p<false>(a, s);
 }
 
 }  // namespace engram

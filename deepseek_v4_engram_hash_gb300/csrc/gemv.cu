@@ -245,8 +245,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     const int K = a.K, N = a.N, T = a.T;
     const int xstride = K + 8;
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);
-    float *red = reinterpret_cast<float *>(smem_raw + (size_t)kMmaT * xstride * 2);    // [16][32][4]
-    int64_t *s_ids = reinterpret_cast<int64_t *>(red + kMmaWarps * 32 * 4);
+    float *red = reinterpret_cast<float *>(smem_raw + (size_t)kMmaT * xstride * 2);    // [2][16][32][4]
+    int64_t *s_ids = reinterpret_cast<int64_t *>(red + 2 * kMmaWarps * 32 * 4);
     const int ctas_per_layer = gridDim.x / a.L;
     const int li = blockIdx.x / ctas_per_layer;
     const int cta = blockIdx.x % ctas_per_layer;
@@ -304,20 +304,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
             }
         }
         if (grp + 1 < grp1) load_group(grp + 1);
-        float4 *rw = reinterpret_cast<float4 *>(red) + warp * 32 + lane;
-        *rw = make_float4(c[0], c[1], c[2], c[3]);
+        // Partials alternate between two buffers: the barrier of group i + 1
+        // also orders the reads of group i before the writes of group i + 2.
+        float *rb = red + ((grp - grp0) & 1) * (kMmaWarps * 32 * 4);
+        reinterpret_cast<float4 *>(rb)[warp * 32 + lane] = make_float4(c[0], c[1], c[2], c[3]);
         __syncthreads();
         if (threadIdx.x < 128) {
             // output (lane l, component j): c0 (row g, token 2q), c1 (row g, 2q+1), c2/c3 row g + 8
             const int l = threadIdx.x >> 2, j = threadIdx.x & 3;
             float v = 0.f;
 #pragma unroll
-            for (int w = 0; w < kMmaWarps; ++w) v += red[(w * 32 + l) * 4 + j];
+            for (int w = 0; w < kMmaWarps; ++w) v += rb[(w * 32 + l) * 4 + j];
             const int gg = l >> 2, qq = l & 3;
             const int r = grp * 16 + gg + ((j & 2) ? 8 : 0), t = 2 * qq + (j & 1);
             if (r < N && t < T) ly.kv[(size_t)t * N + r] = (uint16_t)f32_to_bf16_bits(v);
         }
-        __syncthreads();
     }
 }
 
@@ -327,7 +328,7 @@ static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (((a.K >> 5) + kMmaWarps - 1) / kMmaWarps > kMmaKbMax) return cudaErrorInvalidValue;
-    const size_t smem = (size_t)kMmaT * (a.K + 8) * 2 + kMmaWarps * 32 * 16 +
+    const size_t smem = (size_t)kMmaT * (a.K + 8) * 2 + 2 * kMmaWarps * 32 * 16 +
                         (HASH ? (size_t)a.T * a.C * 8 : 0);
     cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -518,7 +519,7 @@ cudaError_t launch_gemv_q2k(const GemvArgs &a, cudaStream_t s) {
 
 size_t gemv_smem_bytes(int T, int K) {
     if (T > 1 && ((K >> 5) + kMmaWarps - 1) / kMmaWarps > kMmaKbMax) return SIZE_MAX;   // GEMM path
-    return (T <= 1 ? (size_t)K * 2 : (size_t)kMmaT * (K + 8) * 2 + kMmaWarps * 32 * 16) +
+    return (T <= 1 ? (size_t)K * 2 : (size_t)kMmaT * (K + 8) * 2 + 2 * kMmaWarps * 32 * 16) +
            (size_t)kFusedHashMaxIds * 8;
 }
 
