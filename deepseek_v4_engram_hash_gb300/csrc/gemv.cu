@@ -118,11 +118,18 @@ __device__ __forceinline__ void hash_ids(const GemvArgs &a, int T, int li, int c
     }
 }
 
+// Work units: a row of wkv is split into parts of 256 chunks (2048 values);
+// warps take (row, part) units round-robin, so every warp streams the same
+// amount to within one part (whole rows would leave a warp 8 or 9 rows, the
+// last round a third full).  Lane l of a unit sums chunks part*256 + l + 32u,
+// u = 0..7, in that order; a butterfly gives the part's sum; the parts of a
+// row are added in part order.  gemv_q2k_kernel follows the same order.
 template <int T, bool HASH>
 __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_constant__ GemvArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);
     int64_t *s_ids = reinterpret_cast<int64_t *>(smem_raw + (size_t)T * a.K * 2);
+    float *psum = reinterpret_cast<float *>(smem_raw + (size_t)T * a.K * 2 + (HASH ? (size_t)T * a.C * 8 : 0));
     const int ctas_per_layer = gridDim.x / a.L;
     const int li = blockIdx.x / ctas_per_layer;
     const int cta = blockIdx.x % ctas_per_layer;
@@ -134,18 +141,22 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
     const int r0 = cta * rows_per_cta;
     const int r1 = min(N, r0 + rows_per_cta);
     const int chunks = K >> 3;
+    constexpr int kPart = 32 * kGemvUnroll;
+    const int P = (chunks + kPart - 1) / kPart;
+    const int units = max(r1 - r0, 0) * P;
 
-    // ---- the first batch of this warp's wkv stream needs nothing computed:
-    //      start it before waiting on the previous grid ------------------------
-    int o = r0 + warp;
+    // ---- the first unit of this warp needs nothing computed: start its loads
+    //      before waiting on the previous grid -------------------------------
+    int u = warp;
     uint4 wv[kGemvUnroll];
-    bool prefetched = o < r1;
+    bool prefetched = u < units;
     if (prefetched) {
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)o * K);
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)(r0 + u / P) * K);
+        const int base = (u % P) * kPart;
 #pragma unroll
-        for (int u = 0; u < kGemvUnroll; ++u) {
-            const int j = u * 32 + lane;
-            wv[u] = j < chunks ? ld_stream(wrow + j) : make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < kGemvUnroll; ++k) {
+            const int j = base + k * 32 + lane;
+            wv[k] = j < chunks ? ld_stream(wrow + j) : make_uint4(0, 0, 0, 0);
         }
     }
     if (a.pdl) {
@@ -165,29 +176,29 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
     stage_x(a, ly, T, ids, id_stride, xs, K);
     __syncthreads();
 
-    // ---- stream this CTA's wkv rows -------------------------------------------
+    // ---- stream this CTA's wkv units --------------------------------------------
     const uint4 *xs4 = reinterpret_cast<const uint4 *>(xs);
-    for (; o < r1; o += nwarps) {
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)o * K);
+    for (; u < units; u += nwarps) {
+        const int rl = u / P, part = u % P;
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)(r0 + rl) * K);
+        const int base = part * kPart;
+        if (!prefetched) {
+#pragma unroll
+            for (int k = 0; k < kGemvUnroll; ++k) {
+                const int j = base + k * 32 + lane;
+                wv[k] = j < chunks ? ld_stream(wrow + j) : make_uint4(0, 0, 0, 0);
+            }
+        }
+        prefetched = false;
         float acc[T];
 #pragma unroll
         for (int t = 0; t < T; ++t) acc[t] = 0.0f;
-        for (int base = 0; base < chunks; base += 32 * kGemvUnroll) {
-            if (!prefetched) {
 #pragma unroll
-                for (int u = 0; u < kGemvUnroll; ++u) {
-                    const int j = base + u * 32 + lane;
-                    wv[u] = j < chunks ? ld_stream(wrow + j) : make_uint4(0, 0, 0, 0);
-                }
-            }
-            prefetched = false;
+        for (int k = 0; k < kGemvUnroll; ++k) {
+            const int j = base + k * 32 + lane;
+            if (j < chunks) {
 #pragma unroll
-            for (int u = 0; u < kGemvUnroll; ++u) {
-                const int j = base + u * 32 + lane;
-                if (j < chunks) {
-#pragma unroll
-                    for (int t = 0; t < T; ++t) acc[t] = dot8(wv[u], xs4[t * chunks + j], acc[t]);
-                }
+                for (int t = 0; t < T; ++t) acc[t] = dot8(wv[k], xs4[t * chunks + j], acc[t]);
             }
         }
 #pragma unroll
@@ -195,14 +206,15 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
             float v = acc[t];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-            acc[t] = v;
+            if (lane == 0) psum[((size_t)rl * T + t) * P + part] = v;
         }
-        if (lane < T) {
-            float v = acc[0];
-#pragma unroll
-            for (int t = 1; t < T; ++t) if (lane == t) v = acc[t];
-            ly.kv[(size_t)lane * N + o] = (uint16_t)f32_to_bf16_bits(v);
-        }
+    }
+    __syncthreads();
+    for (int i = tid; i < (r1 - r0) * T; i += kGemvThreads) {
+        const int rl = i / T, t = i % T;
+        float v = psum[(size_t)i * P];
+        for (int part = 1; part < P; ++part) v += psum[(size_t)i * P + part];
+        ly.kv[(size_t)t * N + r0 + rl] = (uint16_t)f32_to_bf16_bits(v);
     }
 }
 
@@ -359,7 +371,7 @@ static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
 // sequence and the same butterfly, so kv is bit-identical to the bf16 GEMV on
 // the dequantised weights.
 // ---------------------------------------------------------------------------
-constexpr int kQ2kUnroll = 16;
+constexpr int kQ2kUnroll = 8;     // blocks a unit: 8 x 256 values = one part of gemv_kernel<1>
 
 // Small non-negative integer -> f32 without the quarter-rate conversion unit:
 // 2^23 + n has n in its low mantissa bits, so subtracting 2^23 is exact.
@@ -399,6 +411,10 @@ __device__ __forceinline__ void q2k_lane_weights(uint32_t word, int lane, float 
     }
 }
 
+// A warp takes whole rows (round-robin); within a row it walks the parts of
+// gemv_kernel<1> (8 blocks = 256 chunks each), loading part p + 1 while part
+// p decodes, reduces each part by butterfly and adds the parts in order --
+// the bf16 kernel's summation exactly, hence bit-identical kv.
 template <bool HASH>
 __global__ void __launch_bounds__(kGemvThreads, 2) gemv_q2k_kernel(const __grid_constant__ GemvArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -415,18 +431,17 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_q2k_kernel(const __grid_
     const int rows_per_cta = (N + ctas_per_layer - 1) / ctas_per_layer;
     const int r0 = cta * rows_per_cta;
     const int r1 = min(N, r0 + rows_per_cta);
+    const int P = (nblk + kQ2kUnroll - 1) / kQ2kUnroll;
 
-    auto row_words = [&](int o) {
-        return reinterpret_cast<const uint32_t *>(ly.wkv_q2k + (size_t)o * nblk * 84) + lane;
+    auto load_part = [&](int o, int part, uint32_t (&dst)[kQ2kUnroll]) {
+        const int bb = part * kQ2kUnroll;
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(ly.wkv_q2k + (size_t)o * nblk * 84) + lane;
+#pragma unroll
+        for (int k = 0; k < kQ2kUnroll; ++k) dst[k] = (bb + k < nblk && lane < 21) ? __ldg(w + 21 * (bb + k)) : 0u;
     };
     int o = r0 + warp;
     uint32_t wq[kQ2kUnroll];
-    bool prefetched = o < r1;
-    if (prefetched) {
-        const uint32_t *w = row_words(o);
-#pragma unroll
-        for (int u = 0; u < kQ2kUnroll; ++u) wq[u] = (u < nblk && lane < 21) ? __ldg(w + 21 * u) : 0u;
-    }
+    if (o < r1) load_part(o, 0, wq);
     if (a.pdl) {
         griddep_wait();
         griddep_launch();
@@ -449,21 +464,21 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_q2k_kernel(const __grid_
 
     const float4 *xf4 = reinterpret_cast<const float4 *>(xf);
     for (; o < r1; o += nwarps) {
-        const uint32_t *w = row_words(o);
-        float acc = 0.0f;
-        for (int b0 = 0; b0 < nblk; b0 += kQ2kUnroll) {
-            if (!prefetched) {
+        float row_sum = 0.0f;
+        for (int part = 0; part < P; ++part) {
+            // the next part (or the next row's first part) loads while this one decodes
+            uint32_t wn[kQ2kUnroll];
+            const bool more = part + 1 < P || o + nwarps < r1;
+            if (part + 1 < P) load_part(o, part + 1, wn);
+            else if (o + nwarps < r1) load_part(o + nwarps, 0, wn);
+            const int b0 = part * kQ2kUnroll;
+            float acc = 0.0f;
 #pragma unroll
-                for (int u = 0; u < kQ2kUnroll; ++u)
-                    wq[u] = (b0 + u < nblk && lane < 21) ? __ldg(w + 21 * (b0 + u)) : 0u;
-            }
-            prefetched = false;
-#pragma unroll
-            for (int u = 0; u < kQ2kUnroll; ++u) {
-                if (b0 + u < nblk) {                       // warp-uniform
+            for (int k = 0; k < kQ2kUnroll; ++k) {
+                if (b0 + k < nblk) {                     // warp-uniform
                     float wv[8];
-                    q2k_lane_weights(wq[u], lane, wv);
-                    const int c = (b0 + u) * 32 + lane;    // the lane's 8 k values: chunk 32 b + l
+                    q2k_lane_weights(wq[k], lane, wv);
+                    const int c = (b0 + k) * 32 + lane;  // the lane's 8 k values: chunk 32 b + l
                     const float4 xa = xf4[2 * c], xb = xf4[2 * c + 1];
                     acc = fmaf(wv[0], xa.x, acc);
                     acc = fmaf(wv[1], xa.y, acc);
@@ -475,11 +490,23 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_q2k_kernel(const __grid_
                     acc = fmaf(wv[7], xb.w, acc);
                 }
             }
-        }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-        if (lane == 0) ly.kv[o] = (uint16_t)f32_to_bf16_bits(acc);
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+            row_sum = part == 0 ? acc : row_sum + acc;
+            if (more) {
+#pragma unroll
+                for (int k = 0; k < kQ2kUnroll; ++k) wq[k] = wn[k];
+            }
+        }
+        if (lane == 0) ly.kv[o] = (uint16_t)f32_to_bf16_bits(row_sum);
     }
+}
+
+// Per-row part sums of one CTA: rows_per_cta x T x parts f32.
+static size_t gemv_psum_bytes(int T, int K, int N, int ctas_per_layer) {
+    const int P = ((K >> 3) + 32 * kGemvUnroll - 1) / (32 * kGemvUnroll);
+    const int rows = (N + ctas_per_layer - 1) / ctas_per_layer;
+    return (size_t)rows * T * P * 4;
 }
 
 template <bool HASH>
@@ -487,18 +514,15 @@ static cudaError_t launch_q2k_h(const GemvArgs &a, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const size_t smem = (size_t)a.K * 6 + (HASH ? (size_t)a.C * 8 : 0);
-    cudaError_t e = cudaFuncSetAttribute(gemv_q2k_kernel<HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_q2k_kernel<HASH>, kGemvThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    int ctas_per_layer = (sms * per_sm) / a.L;
+    int ctas_per_layer = (sms * 2) / a.L;
     const int max_useful = (a.N + 15) / 16;
     if (ctas_per_layer > max_useful) ctas_per_layer = max_useful;
     if (ctas_per_layer < 1) ctas_per_layer = 1;
+    const size_t smem = (size_t)a.K * 6 + (HASH ? (size_t)a.C * 8 : 0);
+    if (smem > 100 * 1024) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gemv_q2k_kernel<HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas_per_layer * a.L);
     cfg.blockDim = dim3(kGemvThreads);
@@ -528,18 +552,17 @@ static cudaError_t launch_th(const GemvArgs &a, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const size_t smem = (size_t)T * a.K * 2 + (HASH ? (size_t)T * a.C * 8 : 0);
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<T, HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_kernel<T, HASH>, kGemvThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    int ctas_per_layer = (sms * per_sm) / a.L;
+    const size_t base_smem = (size_t)T * a.K * 2 + (HASH ? (size_t)T * a.C * 8 : 0);
+    // two CTAs an SM (the launch bounds), each owning a contiguous block of rows
+    int ctas_per_layer = (sms * 2) / a.L;
     const int max_useful = (a.N + 15) / 16;          // at least 16 rows a CTA
     if (ctas_per_layer > max_useful) ctas_per_layer = max_useful;
     if (ctas_per_layer < 1) ctas_per_layer = 1;
+    const size_t smem = base_smem + gemv_psum_bytes(T, a.K, a.N, ctas_per_layer);
+    if (smem > 100 * 1024) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<T, HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas_per_layer * a.L);
     cfg.blockDim = dim3(kGemvThreads);
