@@ -47,7 +47,7 @@ def _src_hash(*names) -> str:
 
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by the
 # source hash of the kernel they were taken on; a changed kernel reports null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {("gemv", "d9c6a1e70819"): 506808576}   # 503.40 MB read + 3.41 MB written
 
 
 class Clocks:
