@@ -23,6 +23,10 @@ struct engram_hasher {
     int64_t max_seq;
     int64_t *cache;
     int device;
+    // engram_forward_host: the highway upload runs on `aux` while the
+    // projection streams wkv on the caller's stream; only the gate waits.
+    cudaStream_t aux;
+    cudaEvent_t ev_main, ev_h;
 };
 
 namespace engram {
@@ -184,7 +188,10 @@ int engram_hasher_create(const engram_tables *t, int32_t batch, int64_t max_seq,
     h->max_seq = max_seq;
     cudaGetDevice(&h->device);
     const size_t bytes = (size_t)batch * max_seq * sizeof(int64_t);
-    if (cudaMalloc(&h->cache, bytes) != cudaSuccess || cudaMemset(h->cache, 0, bytes) != cudaSuccess) {
+    if (cudaMalloc(&h->cache, bytes) != cudaSuccess || cudaMemset(h->cache, 0, bytes) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&h->aux, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_main, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_h, cudaEventDisableTiming) != cudaSuccess) {
         engram_hasher_destroy(h);
         return ENGRAM_E_CUDA;
     }
@@ -204,6 +211,9 @@ int engram_hasher_reset(engram_hasher *hs, uintptr_t stream) {
 void engram_hasher_destroy(engram_hasher *hs) {
     if (!hs) return;
     cudaFree(hs->cache);
+    if (hs->ev_h) cudaEventDestroy(hs->ev_h);
+    if (hs->ev_main) cudaEventDestroy(hs->ev_main);
+    if (hs->aux) cudaStreamDestroy(hs->aux);
     delete hs;
 }
 
@@ -431,7 +441,7 @@ namespace {
 // advanced by T at the end of the step.
 int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
                  int64_t start_pos, int64_t *d_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes,
-                 uintptr_t stream) {
+                 uintptr_t stream, cudaEvent_t gate_wait = nullptr) {
     if (!hs || !layers) return ENGRAM_E_NULL;
     int rc = check_hash(hs, d_ids, T, d_pos ? 0 : start_pos, d_ws);
     if (rc || T == 0) return rc;                  // T == 0: a valid no-op
@@ -561,6 +571,7 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
         }
         record(3, s);
     }
+    if (gate_wait && cudaStreamWaitEvent(s, gate_wait, 0) != cudaSuccess) return ENGRAM_E_CUDA;
     if (launch_gate(ga, s) != cudaSuccess) return ENGRAM_E_CUDA;
     record(4, s);
     return ENGRAM_OK;
@@ -648,11 +659,26 @@ int engram_forward_host(engram_hasher *hs, const engram_layer *layers, const int
     cudaStream_t s = S(stream);
     if (start_pos < 0 || start_pos + T > hs->max_seq) return ENGRAM_E_CAPACITY;
     if (ws_bytes < engram_workspace_bytes(&g, (int64_t)M)) return ENGRAM_E_WORKSPACE;
+    if (M == 0) return ENGRAM_OK;
+    // Page-locked, device-mapped host buffers: the kernels read the ids and
+    // update the highway in place over the CPU-GPU link -- no staging copies,
+    // and consecutive steps keep their launch overlap.
+    if (aligned(h_h, 16) && device_readable(h_ids) && device_readable(h_h))
+        return forward_impl(hs, layers, h_ids, T, start_pos, nullptr, h_h, eps, d_ws, ws_bytes, stream);
     if (cudaMemcpyAsync(d_ids, h_ids, M * sizeof(int32_t), cudaMemcpyHostToDevice, s) != cudaSuccess)
         return ENGRAM_E_CUDA;
-    if (cudaMemcpyAsync(d_h, h_h, hbytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return ENGRAM_E_CUDA;
-    int rc = engram_forward(hs, layers, d_ids, T, start_pos, d_h, eps, d_ws, ws_bytes, stream);
-    if (rc) return rc;
+    // The highway upload goes on the hasher's auxiliary stream, after all
+    // earlier work on the caller's stream (e.g. the previous read-back of
+    // d_h), so it overlaps the projection; only the gate waits for it.
+    if (cudaEventRecord(hs->ev_main, s) != cudaSuccess || cudaStreamWaitEvent(hs->aux, hs->ev_main, 0) != cudaSuccess ||
+        cudaMemcpyAsync(d_h, h_h, hbytes, cudaMemcpyHostToDevice, hs->aux) != cudaSuccess ||
+        cudaEventRecord(hs->ev_h, hs->aux) != cudaSuccess)
+        return ENGRAM_E_CUDA;
+    int rc = forward_impl(hs, layers, d_ids, T, start_pos, nullptr, d_h, eps, d_ws, ws_bytes, stream, hs->ev_h);
+    if (rc) {
+        cudaStreamWaitEvent(s, hs->ev_h, 0);         // leave no upload running past an error
+        return rc;
+    }
     return cuda_rc(cudaMemcpyAsync(h_h, d_h, hbytes, cudaMemcpyDeviceToHost, s));
 }
 

@@ -211,10 +211,15 @@ int engram_graph_create(engram_hasher *hs, const engram_layer *layers, const int
 int engram_graph_launch(engram_graph *g, uintptr_t stream);
 void engram_graph_destroy(engram_graph *g);
 
-/* engram_forward from host buffers: enqueues the copy of h_ids [batch, T]
- * and h_h [batch*T, hc, dim] (pinned host memory recommended) into the
- * device staging buffers d_ids / d_h, the forward, and the copy of d_h back
- * into h_h.  The caller synchronises `stream` before reading h_h. */
+/* engram_forward from host buffers h_ids [batch, T] and h_h [batch*T, hc, dim]
+ * (in/out).  When both are page-locked and mapped for the device (e.g.
+ * cudaHostAlloc), the kernels read the ids and update the highway in place
+ * over the CPU-GPU link and d_ids / d_h are not used.  Otherwise the call
+ * enqueues the copies into the device staging buffers d_ids / d_h, the
+ * forward and the copy of d_h back into h_h; the highway upload then runs on
+ * the hasher's own auxiliary stream (created with the hasher), ordered after
+ * the caller's earlier work, so it overlaps the projection.  Either way the
+ * caller synchronises `stream` before reading h_h. */
 int engram_forward_host(engram_hasher *hs, const engram_layer *layers, const int32_t *h_ids,
                         int32_t *d_ids, int32_t T, int64_t start_pos, float *h_h, float *d_h,
                         float eps, void *d_ws, size_t ws_bytes, uintptr_t stream);

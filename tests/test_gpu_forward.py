@@ -204,10 +204,11 @@ def test_forward_all_unmapped_tokens_use_pad_windows(E):
     assert (got == got[0]).all()
 
 
-@pytest.mark.parametrize("T", [1, 6])
-def test_forward_host_buffers_match_device_forward(E, T):
-    """engram_forward_host (ids and highway in pinned host memory, copied in
-    and out on the stream) gives the same highway as engram_forward."""
+@pytest.mark.parametrize("T,pinned", [(1, True), (6, True), (1, False), (6, False)])
+def test_forward_host_buffers_match_device_forward(E, T, pinned):
+    """engram_forward_host gives the same highway as engram_forward: from
+    page-locked buffers (read and updated in place by the kernels) and from
+    pageable ones (staged through device buffers)."""
     from deepseek_v4_engram_hash_gb300 import runner
     cfg = configs.TINY.with_(batch=2)
     eng = runner.EngramSetup(cfg, batch=2, max_tokens=2 * T)
@@ -218,8 +219,10 @@ def test_forward_host_buffers_match_device_forward(E, T):
         h0 = synth.highway(cfg, np.arange(2 * T * step, 2 * T * (step + 1)))
         d_h = torch.from_numpy(h0).cuda()
         eng.forward(ids, pos, d_h)
-        h_ids = torch.from_numpy(ids).pin_memory()
-        h_h = torch.from_numpy(h0.copy()).pin_memory()
+        h_ids = torch.from_numpy(ids.copy())
+        h_h = torch.from_numpy(h0.copy())
+        if pinned:
+            h_ids, h_h = h_ids.pin_memory(), h_h.pin_memory()
         d_ids2 = torch.empty((2, T), dtype=torch.int32, device="cuda")
         d_h2 = torch.empty((2 * T, cfg.hc, cfg.dim), dtype=torch.float32, device="cuda")
         E.engram_forward_host(hs2, eng.layers, h_ids, d_ids2, T, pos, h_h, d_h2, cfg.eps, eng.ws, eng.ws_bytes)
