@@ -230,3 +230,65 @@ def test_forward_host_buffers_match_device_forward(E, T, pinned):
         assert E.engram_check() == 0
         assert torch.equal(h_h, d_h.cpu())
         pos += T
+
+
+MAX_GEO = configs.TINY.with_(
+    name="max_geometry", layer_ids=(1, 2, 3, 4), max_ngram=16, n_heads=1, prime_target=97,
+    head_dim=64, scale_block=32, dim=64, hc=4, batch=1, T=20, seed=9)
+
+
+def test_forward_maximum_geometry(E):
+    """Four layers (the most the kernels take), 16-gram windows (C = 15), hc = 4."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = MAX_GEO
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=cfg.T)
+    ref = G.hash_state(cfg, 1)
+    pos = 0
+    for T in (cfg.T, 1, 3):
+        ids = eng.ids_for(f"max{pos}", T)
+        d_h = _h_device(cfg, pos, T, True)
+        _check_call(eng, ref, ids, pos, d_h, d_h.cpu().numpy(), np.arange(T), np.arange(cfg.N), pos)
+        pos += T
+
+
+def test_long_decode_carries_lookback(E):
+    """512 single-token steps of 8 sequences after a 1536-token prefill (the
+    large-table workload's decode, on V4.1-sized tables): every step's row
+    ids equal the oracle's."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = configs.V41_DECODE.with_(batch=8, prefix=0, T=1536, ids="uniform", decode_steps=512)
+    B = cfg.batch
+    eng = runner.EngramSetup(cfg, batch=B, max_tokens=B * cfg.T)
+    ref = G.hash_state(cfg, B)
+    ids = eng.ids_for("prefill", cfg.T)
+    d_h = _h_device(cfg, 0, B * cfg.T, False)
+    eng.forward(ids, 0, d_h)
+    assert np.array_equal(eng.row_ids(B * cfg.T).cpu().numpy(),
+                          ref.forward(ids, 0).reshape(B * cfg.T, cfg.n_layers, cfg.cols))
+    steps = eng.ids_for("decode", 512)
+    d_h = _h_device(cfg, 0, B, True)
+    got = []
+    for k in range(512):
+        eng.forward(np.ascontiguousarray(steps[:, k:k + 1]), cfg.T + k, d_h)
+        got.append(eng.row_ids(B).clone())
+    assert E.engram_check() == 0
+    for k in range(512):
+        want = ref.forward(steps[:, k:k + 1], cfg.T + k).reshape(B, cfg.n_layers, cfg.cols)
+        assert np.array_equal(got[k].cpu().numpy(), want), f"step {k}"
+
+
+@pytest.mark.parametrize("name,T", [("v41_decode_T1", 1), ("tiny", 16), ("v41_prefill_T4096", 4096)])
+def test_forward_is_bit_reproducible(E, name, T):
+    """Fixed reduction orders everywhere: two runs give the same bits."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = configs.CONFIGS[name]
+    outs = []
+    for _ in range(2):
+        eng = runner.EngramSetup(cfg, batch=1, max_tokens=T)
+        d_h = _h_device(cfg, 0, T, False)
+        eng.forward(eng.ids_for("repro", T), 0, d_h)
+        outs.append((d_h.clone(), [eng.kv(T, l).clone() for l in range(cfg.n_layers)]))
+        del eng
+    assert torch.equal(outs[0][0], outs[1][0])
+    for a, b in zip(outs[0][1], outs[1][1]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
