@@ -544,9 +544,14 @@ def main():
         wkv_host = [d["eng"].layer_data[l]["wkv"].view(torch.int16).cpu().numpy().view(np.uint16)
                     for l in range(cfg.n_layers)]
         rate, threads, n = oracle_decode_rate(12.0, wkv_host)
+        import oracle
+        oracle.set_num_threads(1)
+        rate1, _, n1 = oracle_decode_rate(6.0, wkv_host)
+        oracle.set_num_threads(threads)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{n} V4.1 decode steps (T=1) of the plain C oracle, projection + gate of both "
-                         f"layers timed; hash and row regeneration untimed"}
+                         f"layers timed; hash and row regeneration untimed",
+               "single_thread": {"value": rate1, "unit": "tokens/s", "cores": 1, "steps": n1}}
 
     if rank == 0:
         line = {

@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
             i64 = ctypes.c_int64
             i32 = ctypes.c_int
             L.orc_num_threads.restype = i32
+            L.orc_set_num_threads.argtypes = [i32]
+            L.orc_set_num_threads.restype = None
             L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
             L.orc_f32_to_bf16.restype = ctypes.c_uint16
             L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
@@ -97,6 +99,10 @@ def _c(a, dtype) -> np.ndarray:
 
 def num_threads() -> int:
     return lib().orc_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    lib().orc_set_num_threads(int(n))
 
 
 # ---- scalar codecs ---------------------------------------------------------

@@ -41,6 +41,15 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* Threads for the OpenMP loops (no effect without OpenMP). */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------ */
 /* Number formats                                                       */
 /* ------------------------------------------------------------------ */
