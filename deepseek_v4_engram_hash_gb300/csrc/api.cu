@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 using namespace engram;
 
@@ -15,6 +16,7 @@ struct engram_tables {
     int64_t pad_id;
     int device;
     int64_t *token_map, *mult, *primes, *offsets;
+    uint64_t *bm, *wrap;      // Barrett constants of the primes (see rem_euclid_barrett)
 };
 
 struct engram_hasher {
@@ -161,6 +163,16 @@ int engram_tables_create(const engram_geom *geom, const int64_t *h_token_map, in
     if (!rc) rc = dev_copy(&t->mult, reinterpret_cast<const int64_t *>(h_multipliers), nm);
     if (!rc) rc = dev_copy(&t->primes, reinterpret_cast<const int64_t *>(h_primes), nc);
     if (!rc) rc = dev_copy(&t->offsets, reinterpret_cast<const int64_t *>(h_offsets), nc);
+    if (!rc) {
+        std::vector<uint64_t> bm(nc), wrap(nc);
+        for (size_t i = 0; i < nc; ++i) {
+            const unsigned __int128 two64 = (unsigned __int128)1 << 64;
+            bm[i] = h_primes[i] == 1 ? 0 : (uint64_t)(two64 / h_primes[i]);
+            wrap[i] = (uint64_t)(two64 % h_primes[i]);
+        }
+        rc = dev_copy(&t->bm, bm.data(), nc);
+        if (!rc) rc = dev_copy(&t->wrap, wrap.data(), nc);
+    }
     if (rc) {
         engram_tables_destroy(t);
         return rc;
@@ -175,6 +187,8 @@ void engram_tables_destroy(engram_tables *t) {
     cudaFree(t->mult);
     cudaFree(t->primes);
     cudaFree(t->offsets);
+    cudaFree(t->bm);
+    cudaFree(t->wrap);
     delete t;
 }
 
@@ -255,6 +269,8 @@ HashArgs hash_args(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t s
     a.mult = t->mult;
     a.primes = t->primes;
     a.offsets = t->offsets;
+    a.bm = t->bm;
+    a.wrap = t->wrap;
     a.L = t->g.n_layers;
     a.ng = t->g.max_ngram;
     a.H = t->g.n_heads;

@@ -113,6 +113,8 @@ struct HashArgs {
     const int64_t *token_map;
     int64_t vocab, pad_id;
     const int64_t *mult, *primes, *offsets;
+    const uint64_t *bm;       // per prime: floor(2^64 / p) (0 for p = 1)
+    const uint64_t *wrap;     // per prime: 2^64 mod p
     int32_t L, ng, H;
     int64_t *cache;
     int64_t max_seq;
@@ -144,13 +146,28 @@ __device__ __forceinline__ int64_t hash_compress(const HashArgs &a, int b, int64
     return a.token_map[id];
 }
 
+// rem_euclid(x, p) for the i64 value whose bits are `u` and 0 < p < 2^63, by
+// Barrett reduction (no 64-bit division): with m = floor(2^64 / p),
+// q = floor(u m / 2^64) is floor(u / p) or one less, so u - q p lies in
+// [0, 2p) and one subtraction finishes u mod p.  A negative x is u - 2^64,
+// so its remainder is (u mod p) - (2^64 mod p), lifted into [0, p).
+__device__ __forceinline__ uint64_t rem_euclid_barrett(uint64_t u, uint64_t p, uint64_t m, uint64_t wrap) {
+    if (p == 1) return 0;
+    const uint64_t q = __umul64hi(u, m);
+    uint64_t r = u - q * p;
+    if (r >= p) r -= p;
+    if ((int64_t)u < 0) r = r >= wrap ? r - wrap : r + p - wrap;
+    return r;
+}
+
 // Row id of (sequence b, position start_pos + s, layer li, column col):
 // `EngramHasher::hash` (spark_model/layers/engram_v41.rs) and
 // `NgramHashState::forward` (metrale_model_arch/deepseek_v41_ref/engram.rs).
 // The window holds the compressed ids at shifts 0..n (n = col / H + 1);
 // once a shift reaches before position 0 or an unmapped (-1) id, it and every
 // larger shift take pad_id.  rolling = tok0 * m0, then rolling ^= tok_k * m_k,
-// and the id is rem_euclid(rolling, prime) + offset, all i64 with wrap.  Ids
+// and the id is rem_euclid(rolling, prime) + offset, all i64 with wrap (the
+// remainder by Barrett reduction, rem_euclid_barrett).  Ids
 // of this call come from the input through token_map, older positions from
 // the cache, so no thread depends on another thread's cache write.
 __device__ __forceinline__ int64_t hash_one(const HashArgs &a, int64_t sp, int b, int s, int li, int col) {
@@ -174,10 +191,9 @@ __device__ __forceinline__ int64_t hash_one(const HashArgs &a, int64_t sp, int b
     const int64_t *m = a.mult + (int64_t)li * a.ng;
     uint64_t rolling = (uint64_t)tok[0] * (uint64_t)m[0];
     for (int n = 1; n <= n_top; ++n) rolling ^= (uint64_t)tok[n] * (uint64_t)m[n];
-    const int64_t p = a.primes[(int64_t)li * C + col];
-    int64_t r = (int64_t)rolling % p;
-    if (r < 0) r += p;
-    return (int64_t)((uint64_t)r + (uint64_t)a.offsets[(int64_t)li * C + col]);
+    const int64_t slot = (int64_t)li * C + col;
+    return (int64_t)(rem_euclid_barrett(rolling, (uint64_t)a.primes[slot], a.bm[slot], a.wrap[slot]) +
+                     (uint64_t)a.offsets[slot]);
 }
 
 // Programmatic dependent launch: wait for the grids this one depends on, and

@@ -188,3 +188,22 @@ def test_gate_value_zero_keeps_h_bits(E):
     qk = torch.ones((hc, D), dtype=torch.float32, device="cuda")
     E.engram_gate(d_h, torch.from_numpy(kv.view(np.int16)).cuda(), qk, T, hc, D, 1e-6)
     assert np.array_equal(d_h.cpu().numpy().view(np.uint32), h.view(np.uint32))
+
+
+def test_hash_remainder_extreme_primes(E):
+    """The Euclidean remainder for moduli from 1 to just below 2^63, on wrapped
+    products of both signs: bit-exact against the oracle."""
+    primes = np.array([1, 2, 3, (1 << 31) - 1, (1 << 40) + 15, (1 << 62) + 135, (1 << 63) - 25, 509],
+                      dtype=np.int64)
+    L, ng, H = 2, 3, 2
+    offs = np.zeros(8, dtype=np.int64)
+    rng = np.random.default_rng(3)
+    mult = rng.integers(1, 1 << 62, size=L * ng, dtype=np.int64) | 1
+    tm = rng.integers(0, 1 << 40, size=64, dtype=np.int64)
+    g = E.make_geom(L, ng, H, 64, 128, 2, 32, 64)
+    hs = E.Hasher(E.Tables(g, tm, 0, mult, primes, offs), 16, 64)
+    ref = oracle.HashState(tm, tm[0], mult, primes, offs, L, ng, H, 16, 64)
+    ids = rng.integers(0, 64, size=(16, 40)).astype(np.int32)
+    out = torch.empty((16, 40, L, 4), dtype=torch.int64, device="cuda")
+    E.engram_hash(hs, torch.from_numpy(ids).cuda(), 40, 0, out)
+    assert np.array_equal(out.cpu().numpy(), ref.forward(ids, 0))
