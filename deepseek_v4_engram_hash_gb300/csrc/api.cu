@@ -113,7 +113,7 @@ bool device_readable(const void *p) {
 
 // The projection of one layer's x [M, K] (or of its fused gather) into kv.
 bool gemv_fits(int M, int K) {
-    return M >= 1 && M <= kSmallT && gemv_smem_bytes(M, K) <= 200 * 1024;
+    return M >= 1 && M <= kSmallT && gemv_smem_bytes(M, K) != SIZE_MAX;
 }
 
 }  // namespace

@@ -223,19 +223,37 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_cons
 // accumulate).  With several tokens a CUDA-core dot product needs one
 // shared-memory read of x per token for every 16 bytes of wkv, more
 // shared-memory traffic than the SM can serve at HBM rate; one mma covers 16
-// wkv rows x 16 k x 8 tokens from registers, so the kernel stays HBM-bound.
+// wkv rows x 16 k x 8 tokens, so the kernel stays HBM-bound.
 //
-// Each warp owns 16-row tasks.  The dot product runs over k, so any
-// permutation of k applied to both operands gives the same sum; we let lane
-// (g = lane/4, q = lane%4) hold physical k 8q .. 8q+7 of each 32-wide k
-// block: one 16-byte load of wkv rows g and g+8 (straight from HBM) and one
-// 16-byte load of token g's x (from shared memory, rows padded by 16 bytes so
-// the 32 lanes spread over all banks) feed two mma instructions.
+// wkv is streamed by the bulk-copy engine, not through registers: one
+// producer warp copies 16-row x 1536-wide pieces of the CTA's rows (3 KB
+// contiguous a row) into a 4-stage shared-memory ring, each stage completing
+// an mbarrier by its byte count; 16 MMA warps read the pieces from shared
+// memory and hand each stage back through a second mbarrier.  x is loop
+// invariant for a warp (its k blocks are the same in every row group), so it
+// lives in registers: staged once through the ring's upper half, then loaded
+// as mma B fragments.
+//
+// The dot product runs over k, so any permutation of k applied to both
+// operands gives the same sum; lane (g = lane/4, q = lane%4) holds physical k
+// 8q .. 8q+7 of each 32-wide k block: one 16-byte shared-memory read of rows
+// g and g + 8 (ring rows padded by 64 bytes, so 8 lanes of a phase hit 8
+// distinct 16-byte bank groups) and token g's x feed two mma instructions.
 // ---------------------------------------------------------------------------
 constexpr int kMmaT = 8;
-constexpr int kMmaThreads = 512;
-constexpr int kMmaWarps = kMmaThreads / 32;
-constexpr int kMmaKbMax = 12;        // 32-wide k blocks a warp holds in flight per row group
+constexpr int kMmaWarps = 16;                           // MMA warps; one more warp copies
+constexpr int kMmaThreads = (kMmaWarps + 1) * 32;
+constexpr int kMmaJ = 3;                                // 32-wide k blocks a warp per stage
+constexpr int kStageKb = kMmaWarps * kMmaJ;             // 48 k blocks (1536 values) a stage
+constexpr int kMmaSubMax = 4;                           // stages a 16-row group: K <= 6144
+constexpr int kMmaStages = 4;
+constexpr uint32_t kRowBytes = kStageKb * 64 + 64;      // one row's piece + bank padding
+constexpr uint32_t kMmaStageBytes = 16 * kRowBytes;     // 50 176
+constexpr uint32_t kRedBytes = 2 * kMmaWarps * 32 * 16; // partial tiles, double-buffered
+constexpr size_t kMmaSmemBytes = (size_t)kMmaStages * kMmaStageBytes + kRedBytes + 2 * kMmaStages * 8 + 16;
+static_assert((size_t)kFusedHashMaxIds * 8 <= kRedBytes, "hashed ids are staged in the partial buffer");
+static_assert((size_t)kMmaT * (kMmaSubMax * kStageKb * 32 + 8) * 2 <= 2 * (size_t)kMmaStageBytes,
+              "x is staged in the ring's upper half");
 
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
@@ -246,19 +264,54 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One CTA per SM and layer slice; the CTA walks its contiguous wkv rows 16 at a
-// time, and all 16 warps share each 16-row group: warp w takes k blocks
-// w*kpw .. (w+1)*kpw-1 with every load of them in flight at once, the 16
-// partial 16 x 8 tiles are summed in warp order through shared memory, and the
-// next group's loads are issued before that reduction.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Contiguous global -> shared copy by the bulk-copy engine, completing `bytes`
+// on the mbarrier (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// The 16 MMA warps only (the copy warp does not take part).
+__device__ __forceinline__ void mma_warps_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(kMmaWarps * 32) : "memory");
+}
+
+// One CTA per SM, each owning a contiguous run of 16-row groups of one layer.
+// Stage i of the CTA is group grp0 + i / nsub, k blocks 48 (i % nsub) .. +47;
+// MMA warp w takes k blocks 3w .. 3w + 2 of every stage, and the 16 partial
+// 16 x 8 tiles of a group are summed in warp order through shared memory.
 template <bool HASH>
 __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_constant__ GemvArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int K = a.K, N = a.N, T = a.T;
     const int xstride = K + 8;
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);
-    float *red = reinterpret_cast<float *>(smem_raw + (size_t)kMmaT * xstride * 2);    // [2][16][32][4]
-    int64_t *s_ids = reinterpret_cast<int64_t *>(red + 2 * kMmaWarps * 32 * 4);
+    const uint32_t ring = smem_u32(smem_raw);
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw + 2 * kMmaStageBytes);          // prologue only
+    float *red = reinterpret_cast<float *>(smem_raw + kMmaStages * kMmaStageBytes);
+    int64_t *s_ids = reinterpret_cast<int64_t *>(red);                                   // prologue only
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + kMmaStages * kMmaStageBytes + kRedBytes);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * kMmaStages);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full = [&](int b) { return bar0 + 8u * b; };
+    auto empty = [&](int b) { return bar0 + 8u * (kMmaStages + b); };
+
     const int ctas_per_layer = gridDim.x / a.L;
     const int li = blockIdx.x / ctas_per_layer;
     const int cta = blockIdx.x % ctas_per_layer;
@@ -266,26 +319,47 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
     const int kblocks = K >> 5;
-    const int kpw = (kblocks + kMmaWarps - 1) / kMmaWarps;   // <= kMmaKbMax (host-checked)
-    const int kb_lo = warp * kpw;
+    const int nsub = (kblocks + kStageKb - 1) / kStageKb;                // <= kMmaSubMax (host-checked)
     const int groups_total = (N + 15) / 16;
     const int gpc = (groups_total + ctas_per_layer - 1) / ctas_per_layer;
     const int grp0 = cta * gpc, grp1 = min(groups_total, grp0 + gpc);
+    const int ngroups = max(grp1 - grp0, 0);
+    const int nstages = ngroups * nsub;
+    const bool producer = warp == kMmaWarps;
 
-    uint4 wa[kMmaKbMax], wb[kMmaKbMax];
-    auto load_group = [&](int grp) {
-        const int r0 = grp * 16;
-        const uint4 *pa = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)min(r0 + g, N - 1) * K) + q;
-        const uint4 *pb = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)min(r0 + g + 8, N - 1) * K) + q;
-#pragma unroll
-        for (int u = 0; u < kMmaKbMax; ++u) {
-            const int kb = kb_lo + u;
-            const bool ok = u < kpw && kb < kblocks;
-            wa[u] = ok ? ld_stream(pa + 4 * kb) : make_uint4(0, 0, 0, 0);
-            wb[u] = ok ? ld_stream(pb + 4 * kb) : make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kMmaStages; ++b) {
+            mbar_init(full(b), 1);
+            mbar_init(empty(b), kMmaWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    const uint64_t pol = l2_evict_first();
+    int issued = 0;
+    // Producer: stage i into slot i % 4 once the MMA warps have released it.
+    auto issue_until = [&](int stop) {
+        for (; issued < stop; ++issued) {
+            const int i = issued, b = i % kMmaStages;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(empty(b), ((i / kMmaStages) & 1) ^ 1, abort_flag, a.err);
+            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+            const int grp = grp0 + i / nsub, kb0 = (i % nsub) * kStageKb;
+            const uint32_t bytes = (uint32_t)min(kStageKb, kblocks - kb0) * 64u;
+            const int r0 = grp * 16, nrows = min(16, N - r0);
+            if (lane == 0) mbar_expect_tx(full(b), bytes * (uint32_t)nrows);
+            __syncwarp();
+            if (lane < nrows)
+                bulk_load(ring + b * kMmaStageBytes + lane * kRowBytes, ly.wkv + (size_t)(r0 + lane) * K + kb0 * 32,
+                          bytes, full(b), pol);
         }
     };
-    if (grp0 < grp1) load_group(grp0);          // needs nothing computed: before the wait
+    // the first two stages need nothing computed and do not overlap x: before the wait
+    if (producer) issue_until(min(nstages, 2));
+
     if (a.pdl) {
         griddep_wait();
         griddep_launch();
@@ -299,36 +373,73 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
         id_stride = a.C;
     }
     stage_x(a, ly, T, ids, id_stride, xs, xstride);
-    for (int i = threadIdx.x; i < (kMmaT - T) * (xstride >> 3); i += kMmaThreads)   // zero the padding tokens
-        reinterpret_cast<uint4 *>(xs + (size_t)T * xstride)[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
-    const uint16_t *xg = xs + (size_t)g * xstride + 8 * q;
-    for (int grp = grp0; grp < grp1; ++grp) {
+    uint4 xr[kMmaSubMax][kMmaJ];
+#pragma unroll
+    for (int sub = 0; sub < kMmaSubMax; ++sub)
+#pragma unroll
+        for (int jj = 0; jj < kMmaJ; ++jj) {
+            const int kb = sub * kStageKb + warp * kMmaJ + jj;
+            xr[sub][jj] = (!producer && g < T && sub < nsub && kb < kblocks)
+                              ? *reinterpret_cast<const uint4 *>(xs + (size_t)g * xstride + kb * 32 + 8 * q)
+                              : make_uint4(0, 0, 0, 0);
+        }
+    __syncthreads();                       // x is in registers: the ring's upper half is free
+
+    if (producer) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // x staging writes before the copies
+        issue_until(nstages);
+        // Let every copy already issued land before the CTA can leave.
+        if (lane == 0)
+            for (int d = 1; d <= kMmaStages && issued - d >= 0; ++d) {
+                const int i = issued - d;
+                const uint64_t t0 = now_ns();
+                while (!mbar_try(full(i % kMmaStages), (i / kMmaStages) & 1) && now_ns() - t0 < 10000000ull) {
+                }
+            }
+        return;
+    }
+
+    bool live = true;
+    const uint32_t a_off = g * kRowBytes + (warp * kMmaJ) * 64 + 16 * q;
+    for (int gi = 0; gi < ngroups; ++gi) {
         float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int u = 0; u < kMmaKbMax; ++u) {
-            const int kb = kb_lo + u;
-            if (u < kpw && kb < kblocks) {
-                const uint4 xb = *reinterpret_cast<const uint4 *>(xg + 32 * kb);
-                mma_16816(c, wa[u].x, wb[u].x, wa[u].y, wb[u].y, xb.x, xb.y);
-                mma_16816(c, wa[u].z, wb[u].z, wa[u].w, wb[u].w, xb.z, xb.w);
+        for (int sub = 0; sub < kMmaSubMax; ++sub) {
+            if (sub < nsub) {
+                const int i = gi * nsub + sub, b = i % kMmaStages;
+                const bool ok = live && mbar_wait(full(b), (i / kMmaStages) & 1, abort_flag, a.err);
+                live = __all_sync(0xFFFFFFFFu, ok);
+                if (live) {
+                    const uint32_t sa = ring + b * kMmaStageBytes + a_off;
+#pragma unroll
+                    for (int jj = 0; jj < kMmaJ; ++jj) {
+                        if (sub * kStageKb + warp * kMmaJ + jj < kblocks) {
+                            const uint4 lo = lds128(sa + jj * 64), hi = lds128(sa + 8 * kRowBytes + jj * 64);
+                            const uint4 xb = xr[sub][jj];
+                            mma_16816(c, lo.x, hi.x, lo.y, hi.y, xb.x, xb.y);
+                            mma_16816(c, lo.z, hi.z, lo.w, hi.w, xb.z, xb.w);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty(b));
+                }
             }
         }
-        if (grp + 1 < grp1) load_group(grp + 1);
         // Partials alternate between two buffers: the barrier of group i + 1
         // also orders the reads of group i before the writes of group i + 2.
-        float *rb = red + ((grp - grp0) & 1) * (kMmaWarps * 32 * 4);
+        float *rb = red + (gi & 1) * (kMmaWarps * 32 * 4);
         reinterpret_cast<float4 *>(rb)[warp * 32 + lane] = make_float4(c[0], c[1], c[2], c[3]);
-        __syncthreads();
-        if (threadIdx.x < 128) {
+        mma_warps_sync();
+        if (threadIdx.x < 128 && live) {
             // output (lane l, component j): c0 (row g, token 2q), c1 (row g, 2q+1), c2/c3 row g + 8
             const int l = threadIdx.x >> 2, j = threadIdx.x & 3;
             float v = 0.f;
 #pragma unroll
             for (int w = 0; w < kMmaWarps; ++w) v += rb[(w * 32 + l) * 4 + j];
             const int gg = l >> 2, qq = l & 3;
-            const int r = grp * 16 + gg + ((j & 2) ? 8 : 0), t = 2 * qq + (j & 1);
+            const int r = (grp0 + gi) * 16 + gg + ((j & 2) ? 8 : 0), t = 2 * qq + (j & 1);
             if (r < N && t < T) ly.kv[(size_t)t * N + r] = (uint16_t)f32_to_bf16_bits(v);
         }
     }
@@ -339,11 +450,12 @@ static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (((a.K >> 5) + kMmaWarps - 1) / kMmaWarps > kMmaKbMax) return cudaErrorInvalidValue;
-    const size_t smem = (size_t)kMmaT * (a.K + 8) * 2 + 2 * kMmaWarps * 32 * 16 +
-                        (HASH ? (size_t)a.T * a.C * 8 : 0);
+    if (a.T < 1 || a.T > kMmaT || a.K % 32 || (a.K >> 5) > kMmaSubMax * kStageKb) return cudaErrorInvalidValue;
+    if (HASH && (size_t)a.T * a.C > (size_t)kFusedHashMaxIds) return cudaErrorInvalidValue;
+    for (int l = 0; l < a.L; ++l)
+        if (reinterpret_cast<uintptr_t>(a.layer[l].wkv) % 16) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+                                         (int)kMmaSmemBytes);
     if (e != cudaSuccess) return e;
     int ctas_per_layer = sms / a.L;
     const int groups = (a.N + 15) / 16;
@@ -352,7 +464,7 @@ static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas_per_layer * a.L);
     cfg.blockDim = dim3(kMmaThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = kMmaSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -542,9 +654,12 @@ cudaError_t launch_gemv_q2k(const GemvArgs &a, cudaStream_t s) {
 }
 
 size_t gemv_smem_bytes(int T, int K) {
-    if (T > 1 && ((K >> 5) + kMmaWarps - 1) / kMmaWarps > kMmaKbMax) return SIZE_MAX;   // GEMM path
-    return (T <= 1 ? (size_t)K * 2 : (size_t)kMmaT * (K + 8) * 2 + 2 * kMmaWarps * 32 * 16) +
-           (size_t)kFusedHashMaxIds * 8;
+    if (T <= 1) {
+        const size_t b = (size_t)K * 2 + (size_t)kFusedHashMaxIds * 8;
+        return b <= 96 * 1024 ? b : SIZE_MAX;           // the rest of 100 KB holds part sums
+    }
+    if (T > kMmaT || K % 32 || (K >> 5) > kMmaSubMax * kStageKb) return SIZE_MAX;   // GEMM path
+    return kMmaSmemBytes;
 }
 
 template <int T, bool HASH>
@@ -584,7 +699,7 @@ static cudaError_t launch_t(const GemvArgs &a, cudaStream_t s) {
 cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;
     if (a.T == 1) return launch_t<1>(a, s);
-    if (a.T <= kMmaT && a.K % 32 == 0 && ((a.K >> 5) + kMmaWarps - 1) / kMmaWarps <= kMmaKbMax)
+    if (gemv_smem_bytes(a.T, a.K) != SIZE_MAX)
         return a.fuse_hash ? launch_mma<true>(a, s) : launch_mma<false>(a, s);
     return cudaErrorInvalidValue;
 }
