@@ -384,8 +384,8 @@ int engram_project_q2k(const uint16_t *d_x, const uint8_t *d_wkv_q2k, int32_t K,
                        uintptr_t stream) {
     if (!d_x || !d_wkv_q2k || !d_kv) return ENGRAM_E_NULL;
     if (K < 256 || K % 256 || N < 1 || K > (1 << 20)) return ENGRAM_E_INVALID;
-    if (!aligned(d_x, 16) || !aligned(d_wkv_q2k, 4) || !aligned(d_kv, 2)) return ENGRAM_E_ALIGN;
-    if ((size_t)K * 2 > 200 * 1024) return ENGRAM_E_UNSUPPORTED;
+    if (!aligned(d_x, 16) || !aligned(d_wkv_q2k, 16) || !aligned(d_kv, 2)) return ENGRAM_E_ALIGN;
+    if (K > kGemvMaxK) return ENGRAM_E_UNSUPPORTED;
     int *err = err_ptr();
     if (!err) return ENGRAM_E_CUDA;
     GemvArgs a{};
@@ -470,11 +470,12 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
     const int64_t M = (int64_t)hs->batch * T;
     bool all_q2k = K % 256 == 0;
     for (int l = 0; l < L; ++l) all_q2k = all_q2k && layers[l].wkv_q2k != nullptr;
-    const bool use_q2k = all_q2k && M == 1;
+    const bool use_q2k = all_q2k && M == 1 && K <= kGemvMaxK;
     for (int l = 0; l < L; ++l) {
         const engram_layer &ly = layers[l];
-        if (!ly.table || !ly.qk || (!ly.wkv && !use_q2k)) return ENGRAM_E_NULL;
-        if (ly.wkv_q2k && !aligned(ly.wkv_q2k, 4)) return ENGRAM_E_ALIGN;
+        if (!ly.table || !ly.qk) return ENGRAM_E_NULL;
+        if (!ly.wkv && !use_q2k) return all_q2k && M == 1 ? ENGRAM_E_UNSUPPORTED : ENGRAM_E_NULL;
+        if (ly.wkv_q2k && !aligned(ly.wkv_q2k, 16)) return ENGRAM_E_ALIGN;
         if (ly.rows < 1) return ENGRAM_E_INVALID;
         if (ly.fmt == ENGRAM_FMT_FP8 || ly.fmt == ENGRAM_FMT_FP8_E8M0) {
             if (!ly.scales) return ENGRAM_E_NULL;

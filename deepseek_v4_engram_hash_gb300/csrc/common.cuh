@@ -287,6 +287,7 @@ struct GemvArgs {
     int *err;
 };
 constexpr int kFusedHashMaxIds = 2048;  // T * C row ids a CTA may hash for its layer
+constexpr int kGemvMaxK = 6144;         // widest x the 1..8-token GEMV holds in registers
 cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t s);
 cudaError_t launch_gemv_q2k(const GemvArgs &a, cudaStream_t s);   // one token, Q2_K wkv
 size_t gemv_smem_bytes(int T, int K);

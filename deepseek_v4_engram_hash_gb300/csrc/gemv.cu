@@ -1,47 +1,26 @@
-// gemv.cu -- the wkv projection for a few tokens (stage 3, T <= 8), with the
-// row gather and dequantisation (stage 2) fused into the x staging.
+// gemv.cu -- the wkv projection for a few tokens (stage 3, 1 <= T <= 8), with
+// the row gather and dequantisation (stage 2) fused into the x staging.
 //
 // kv[t, o] = bf16_rne(sum_i x[t, i] * wkv[o, i]), f32 accumulation
-// (`linear_bf16`, metrale_model_arch/deepseek_v41_ref/engram.rs).  At one
-// token the projection is a pass over wkv (251.7 MB a layer at V4.1 shape),
+// (`linear_bf16`, metrale_model_arch/deepseek_v41_ref/engram.rs).  At a few
+// tokens the projection is a pass over wkv (251.7 MB a layer at V4.1 shape),
 // so this kernel is shaped for HBM bandwidth, as the pages choose a GEMV over
 // a tiled GEMM at m = 1 (spark_model/layers/attn_v41.rs, `Kernels.gemv`).
 //
-// Grid: the layers' CTAs side by side; each CTA owns a contiguous block of
-// wkv rows of one layer.  Prologue: the CTA gathers that layer's T * C table
-// rows (fp8 codes x pow2 scale, or Q2_K blocks) straight into x [T, K] bf16 in
-// shared memory -- the [T * C, head_dim] rows never touch HBM.  Main loop:
-// each warp takes one wkv row at a time; lane l streams the row's 16-byte
-// chunks l, l + 32, ... with U loads in flight, multiplies them by x from
-// shared memory and keeps a per-lane f32 sum in chunk order; a butterfly
-// shuffle reduction then gives the dot product.  The order is fixed, so the
-// fused and the plain-x launches give identical bits.
+// Grid: the layers' CTAs side by side, one an SM; each CTA owns a contiguous
+// run of 16-row groups of one layer's wkv.  Prologue: the CTA gathers that
+// layer's T * C table rows (fp8 codes x pow2 scale, or Q2_K blocks) straight
+// into x [T, K] bf16 in shared memory -- the [T * C, head_dim] rows never
+// touch HBM.  Main loop: a copy warp streams the CTA's wkv rows into a
+// shared-memory ring with bulk copies; 16 MMA warps multiply them by x on
+// mma.sync m16n8k16 (bf16 in, f32 accumulate).  wkv may also be held as Q2_K
+// blocks (`wkv_q2k` on spark_model/layers/engram_v41.rs, 6x fewer bytes): the
+// same kernel then copies the blocks and decodes each lane's weights into its
+// mma fragments, in the same order, so kv is bit-identical to the bf16 path on
+// the dequantised weights.
 #include "common.cuh"
 
 namespace engram {
-
-constexpr int kGemvThreads = 512;
-constexpr int kGemvUnroll = 8;
-
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ float dot8(const uint4 &w, const uint4 &x, float acc) {
-    acc = fmaf(bf16_lo(w.x), bf16_lo(x.x), acc);
-    acc = fmaf(bf16_hi(w.x), bf16_hi(x.x), acc);
-    acc = fmaf(bf16_lo(w.y), bf16_lo(x.y), acc);
-    acc = fmaf(bf16_hi(w.y), bf16_hi(x.y), acc);
-    acc = fmaf(bf16_lo(w.z), bf16_lo(x.z), acc);
-    acc = fmaf(bf16_hi(w.z), bf16_hi(x.z), acc);
-    acc = fmaf(bf16_lo(w.w), bf16_lo(x.w), acc);
-    acc = fmaf(bf16_hi(w.w), bf16_hi(x.w), acc);
-    return acc;
-}
 
 // Q2_K decode of one 256-wide row by one warp into shared memory.
 __device__ __forceinline__ void q2k_row_to_smem(const uint8_t *blk, bool ok, int lane,
@@ -118,142 +97,59 @@ __device__ __forceinline__ void hash_ids(const GemvArgs &a, int T, int li, int c
     }
 }
 
-// Work units: a row of wkv is split into parts of 256 chunks (2048 values);
-// warps take (row, part) units round-robin, so every warp streams the same
-// amount to within one part (whole rows would leave a warp 8 or 9 rows, the
-// last round a third full).  Lane l of a unit sums chunks part*256 + l + 32u,
-// u = 0..7, in that order; a butterfly gives the part's sum; the parts of a
-// row are added in part order.  gemv_q2k_kernel follows the same order.
-template <int T, bool HASH>
-__global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const __grid_constant__ GemvArgs a) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);
-    int64_t *s_ids = reinterpret_cast<int64_t *>(smem_raw + (size_t)T * a.K * 2);
-    float *psum = reinterpret_cast<float *>(smem_raw + (size_t)T * a.K * 2 + (HASH ? (size_t)T * a.C * 8 : 0));
-    const int ctas_per_layer = gridDim.x / a.L;
-    const int li = blockIdx.x / ctas_per_layer;
-    const int cta = blockIdx.x % ctas_per_layer;
-    const GemvLayer &ly = a.layer[li];
-    const int K = a.K, N = a.N;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwarps = kGemvThreads / 32;
-    const int rows_per_cta = (N + ctas_per_layer - 1) / ctas_per_layer;
-    const int r0 = cta * rows_per_cta;
-    const int r1 = min(N, r0 + rows_per_cta);
-    const int chunks = K >> 3;
-    constexpr int kPart = 32 * kGemvUnroll;
-    const int P = (chunks + kPart - 1) / kPart;
-    const int units = max(r1 - r0, 0) * P;
-
-    // ---- the first unit of this warp needs nothing computed: start its loads
-    //      before waiting on the previous grid -------------------------------
-    int u = warp;
-    uint4 wv[kGemvUnroll];
-    bool prefetched = u < units;
-    if (prefetched) {
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)(r0 + u / P) * K);
-        const int base = (u % P) * kPart;
-#pragma unroll
-        for (int k = 0; k < kGemvUnroll; ++k) {
-            const int j = base + k * 32 + lane;
-            wv[k] = j < chunks ? ld_stream(wrow + j) : make_uint4(0, 0, 0, 0);
-        }
-    }
-    if (a.pdl) {
-        griddep_wait();          // ids, cache, workspace: ready once the previous grid is done
-        griddep_launch();        // the gate may now launch and prefetch the highway
-    }
-
-    // ---- row ids: hashed here (one thread per id), or read; then x -----------
-    const int64_t *ids = ly.ids;
-    int64_t id_stride = a.id_stride;
-    if (HASH) {
-        hash_ids(a, T, li, cta, s_ids);
-        __syncthreads();
-        ids = s_ids;
-        id_stride = a.C;
-    }
-    stage_x(a, ly, T, ids, id_stride, xs, K);
-    __syncthreads();
-
-    // ---- stream this CTA's wkv units --------------------------------------------
-    const uint4 *xs4 = reinterpret_cast<const uint4 *>(xs);
-    for (; u < units; u += nwarps) {
-        const int rl = u / P, part = u % P;
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(ly.wkv + (size_t)(r0 + rl) * K);
-        const int base = part * kPart;
-        if (!prefetched) {
-#pragma unroll
-            for (int k = 0; k < kGemvUnroll; ++k) {
-                const int j = base + k * 32 + lane;
-                wv[k] = j < chunks ? ld_stream(wrow + j) : make_uint4(0, 0, 0, 0);
-            }
-        }
-        prefetched = false;
-        float acc[T];
-#pragma unroll
-        for (int t = 0; t < T; ++t) acc[t] = 0.0f;
-#pragma unroll
-        for (int k = 0; k < kGemvUnroll; ++k) {
-            const int j = base + k * 32 + lane;
-            if (j < chunks) {
-#pragma unroll
-                for (int t = 0; t < T; ++t) acc[t] = dot8(wv[k], xs4[t * chunks + j], acc[t]);
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-            float v = acc[t];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-            if (lane == 0) psum[((size_t)rl * T + t) * P + part] = v;
-        }
-    }
-    __syncthreads();
-    for (int i = tid; i < (r1 - r0) * T; i += kGemvThreads) {
-        const int rl = i / T, t = i % T;
-        float v = psum[(size_t)i * P];
-        for (int part = 1; part < P; ++part) v += psum[(size_t)i * P + part];
-        ly.kv[(size_t)t * N + r0 + rl] = (uint16_t)f32_to_bf16_bits(v);
-    }
-}
 
 // ---------------------------------------------------------------------------
-// 2..8 tokens: the same stream of wkv through mma.sync m16n8k16 (bf16 in, f32
-// accumulate).  With several tokens a CUDA-core dot product needs one
+// The ring.  With several tokens a CUDA-core dot product needs one
 // shared-memory read of x per token for every 16 bytes of wkv, more
 // shared-memory traffic than the SM can serve at HBM rate; one mma covers 16
-// wkv rows x 16 k x 8 tokens, so the kernel stays HBM-bound.
+// wkv rows x 16 k x 8 tokens, so the kernel stays HBM-bound (at one token the
+// unused seven token columns cost nothing: the tensor pipe is idle anyway).
 //
-// wkv is streamed by the bulk-copy engine, not through registers: one
-// producer warp copies 16-row x 1536-wide pieces of the CTA's rows (3 KB
-// contiguous a row) into a 4-stage shared-memory ring, each stage completing
-// an mbarrier by its byte count; 16 MMA warps read the pieces from shared
-// memory and hand each stage back through a second mbarrier.  x is loop
-// invariant for a warp (its k blocks are the same in every row group), so it
-// lives in registers: staged once through the ring's upper half, then loaded
-// as mma B fragments.
+// bf16 wkv: the copy warp copies 16-row x 1536-wide pieces of the CTA's rows
+// (3 KB contiguous a row) into a 4-stage ring, each stage completing an
+// mbarrier by its byte count; the MMA warps read the pieces from shared memory
+// and hand each stage back through a second mbarrier.  Q2_K wkv: a stage is a
+// whole 16-row group (16 x K/256 blocks of 84 bytes, contiguous in memory: one
+// copy), six stages.  x is loop invariant for a warp (its k blocks are the
+// same in every row group), so it lives in registers: staged once through the
+// ring's upper half, then loaded as mma B fragments.
 //
 // The dot product runs over k, so any permutation of k applied to both
 // operands gives the same sum; lane (g = lane/4, q = lane%4) holds physical k
 // 8q .. 8q+7 of each 32-wide k block: one 16-byte shared-memory read of rows
-// g and g + 8 (ring rows padded by 64 bytes, so 8 lanes of a phase hit 8
-// distinct 16-byte bank groups) and token g's x feed two mma instructions.
+// g and g + 8 (bf16 ring rows padded by 64 bytes, so the 8 lanes of a phase
+// hit distinct 16-byte bank groups) and token g's x feed two mma instructions.
 // ---------------------------------------------------------------------------
 constexpr int kMmaT = 8;
 constexpr int kMmaWarps = 16;                           // MMA warps; one more warp copies
 constexpr int kMmaThreads = (kMmaWarps + 1) * 32;
 constexpr int kMmaJ = 3;                                // 32-wide k blocks a warp per stage
-constexpr int kStageKb = kMmaWarps * kMmaJ;             // 48 k blocks (1536 values) a stage
-constexpr int kMmaSubMax = 4;                           // stages a 16-row group: K <= 6144
-constexpr int kMmaStages = 4;
+constexpr int kStageKb = kMmaWarps * kMmaJ;             // 48 k blocks (1536 values) a bf16 stage
+constexpr int kMmaSubMax = 4;                           // bf16 stages a 16-row group
+static_assert(kMmaSubMax * kStageKb * 32 == kGemvMaxK, "x fragments cover K");
 constexpr uint32_t kRowBytes = kStageKb * 64 + 64;      // one row's piece + bank padding
-constexpr uint32_t kMmaStageBytes = 16 * kRowBytes;     // 50 176
 constexpr uint32_t kRedBytes = 2 * kMmaWarps * 32 * 16; // partial tiles, double-buffered
-constexpr size_t kMmaSmemBytes = (size_t)kMmaStages * kMmaStageBytes + kRedBytes + 2 * kMmaStages * 8 + 16;
 static_assert((size_t)kFusedHashMaxIds * 8 <= kRedBytes, "hashed ids are staged in the partial buffer");
-static_assert((size_t)kMmaT * (kMmaSubMax * kStageKb * 32 + 8) * 2 <= 2 * (size_t)kMmaStageBytes,
-              "x is staged in the ring's upper half");
+
+template <bool WQ2K>
+struct Ring;
+template <>
+struct Ring<false> {
+    static constexpr int kStages = 4;
+    static constexpr uint32_t kStageBytes = 16 * kRowBytes;                   // 50 176
+};
+template <>
+struct Ring<true> {
+    static constexpr int kStages = 6;
+    static constexpr uint32_t kStageBytes = 16 * (kGemvMaxK / 256) * 84;      // 32 256
+};
+template <bool WQ2K>
+constexpr size_t ring_smem_bytes() {
+    return (size_t)Ring<WQ2K>::kStages * Ring<WQ2K>::kStageBytes + kRedBytes + 2 * Ring<WQ2K>::kStages * 8 + 16;
+}
+static_assert((size_t)kMmaT * (kGemvMaxK + 8) * 2 <= 2 * (size_t)Ring<false>::kStageBytes &&
+                  (size_t)kMmaT * (kGemvMaxK + 8) * 2 <= 4 * (size_t)Ring<true>::kStageBytes,
+              "x is staged in the ring's upper stages");
 
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
@@ -293,24 +189,65 @@ __device__ __forceinline__ void mma_warps_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(kMmaWarps * 32) : "memory");
 }
 
+// Small non-negative integer -> f32 without the quarter-rate conversion unit:
+// 2^23 + n has n in its low mantissa bits, so subtracting 2^23 is exact.
+__device__ __forceinline__ float small_u2f(uint32_t n) {
+    return __uint_as_float(0x4B000000u | n) - 8388608.0f;
+}
+
+// Lane (g, q)'s A-fragment words for 32-wide k block kb of one Q2_K row in
+// shared memory: values v = 32 (kb % 8) + 8q + e, e = 0..7, of block kb / 8,
+// each rounded to bf16, packed in pairs (the words a bf16 row holds there).
+// With kk = kb % 8 the values share half = kk / 4, j = kk % 4 and sub-block
+// 8 half + 2j + q/2; their quant bytes are qs[32 half + 8q + e] (block words
+// 4 + 8 half + 2q and the next) and the quant is (byte >> 2j) & 3.
+// y = fma(d*sc, q, -dmin*m) equals d*sc*q - dmin*m rounded once (d*sc*q and
+// dmin*m are exact in f32), as the row decoder computes it.
+__device__ __forceinline__ uint4 q2k_frag(const uint8_t *row, int kb, int q) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (kb >> 3) * 84);
+    const int kk = kb & 7, half = kk >> 2, j = kk & 3;
+    const uint32_t q0 = w[4 + 8 * half + 2 * q], q1 = w[5 + 8 * half + 2 * q];
+    const int sb = 8 * half + 2 * j + (q >> 1);
+    const uint32_t sc = (w[sb >> 2] >> (8 * (sb & 3))) & 0xFFu;
+    const uint32_t dw = w[20];
+    const float d = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
+    const float dl = __fmul_rn(d, small_u2f(sc & 15u));
+    const float nml = -__fmul_rn(dmin, small_u2f(sc >> 4));
+    const uint32_t t0 = (q0 >> (2 * j)) & 0x03030303u, t1 = (q1 >> (2 * j)) & 0x03030303u;
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        const uint32_t t = e < 4 ? t0 : t1;
+        // byte e of t into the low byte of 0x4B000000: the f32 2^23 + q, minus 2^23
+        const float f0 = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7540u | (e & 3))) - 8388608.0f;
+        const float f1 = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7540u | ((e + 1) & 3))) - 8388608.0f;
+        o[e >> 1] = pack_bf16x2(__fmaf_rn(dl, f0, nml), __fmaf_rn(dl, f1, nml));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // One CTA per SM, each owning a contiguous run of 16-row groups of one layer.
-// Stage i of the CTA is group grp0 + i / nsub, k blocks 48 (i % nsub) .. +47;
-// MMA warp w takes k blocks 3w .. 3w + 2 of every stage, and the 16 partial
-// 16 x 8 tiles of a group are summed in warp order through shared memory.
-template <bool HASH>
+// MMA warp w takes k blocks 48 s + 3w + j (s = 0 .. nsub-1, j = 0..2) of
+// every row group, in that order, and the 16 partial 16 x 8 tiles of a group
+// are summed in warp order through shared memory; both weight formats follow
+// this order exactly.  bf16: stage i is group grp0 + i / nsub, k blocks
+// 48 (i % nsub) .. +47.  Q2_K: stage i is group grp0 + i.
+template <bool HASH, bool WQ2K>
 __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_constant__ GemvArgs a) {
+    using R = Ring<WQ2K>;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int K = a.K, N = a.N, T = a.T;
     const int xstride = K + 8;
     const uint32_t ring = smem_u32(smem_raw);
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw + 2 * kMmaStageBytes);          // prologue only
-    float *red = reinterpret_cast<float *>(smem_raw + kMmaStages * kMmaStageBytes);
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw + 2 * R::kStageBytes);          // prologue only
+    float *red = reinterpret_cast<float *>(smem_raw + R::kStages * R::kStageBytes);
     int64_t *s_ids = reinterpret_cast<int64_t *>(red);                                   // prologue only
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + kMmaStages * kMmaStageBytes + kRedBytes);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * kMmaStages);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::kStages * R::kStageBytes + kRedBytes);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * R::kStages);
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int b) { return bar0 + 8u * b; };
-    auto empty = [&](int b) { return bar0 + 8u * (kMmaStages + b); };
+    auto empty = [&](int b) { return bar0 + 8u * (R::kStages + b); };
 
     const int ctas_per_layer = gridDim.x / a.L;
     const int li = blockIdx.x / ctas_per_layer;
@@ -320,15 +257,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     const int g = lane >> 2, q = lane & 3;
     const int kblocks = K >> 5;
     const int nsub = (kblocks + kStageKb - 1) / kStageKb;                // <= kMmaSubMax (host-checked)
+    const uint32_t q2k_row = (uint32_t)(K >> 8) * 84u;                  // bytes of a Q2_K row
     const int groups_total = (N + 15) / 16;
     const int gpc = (groups_total + ctas_per_layer - 1) / ctas_per_layer;
     const int grp0 = cta * gpc, grp1 = min(groups_total, grp0 + gpc);
     const int ngroups = max(grp1 - grp0, 0);
-    const int nstages = ngroups * nsub;
+    const int spg = WQ2K ? 1 : nsub;                                     // stages a group
+    const int nstages = ngroups * spg;
     const bool producer = warp == kMmaWarps;
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < kMmaStages; ++b) {
+        for (int b = 0; b < R::kStages; ++b) {
             mbar_init(full(b), 1);
             mbar_init(empty(b), kMmaWarps);
         }
@@ -340,21 +279,37 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
 
     const uint64_t pol = l2_evict_first();
     int issued = 0;
-    // Producer: stage i into slot i % 4 once the MMA warps have released it.
+    // Copy warp: stage i into slot i % kStages once the MMA warps have released it.
     auto issue_until = [&](int stop) {
         for (; issued < stop; ++issued) {
-            const int i = issued, b = i % kMmaStages;
+            const int i = issued, b = i % R::kStages;
             bool ok = true;
-            if (lane == 0) ok = mbar_wait(empty(b), ((i / kMmaStages) & 1) ^ 1, abort_flag, a.err);
+            if (lane == 0) ok = mbar_wait(empty(b), ((i / R::kStages) & 1) ^ 1, abort_flag, a.err);
             if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
-            const int grp = grp0 + i / nsub, kb0 = (i % nsub) * kStageKb;
-            const uint32_t bytes = (uint32_t)min(kStageKb, kblocks - kb0) * 64u;
-            const int r0 = grp * 16, nrows = min(16, N - r0);
-            if (lane == 0) mbar_expect_tx(full(b), bytes * (uint32_t)nrows);
-            __syncwarp();
-            if (lane < nrows)
-                bulk_load(ring + b * kMmaStageBytes + lane * kRowBytes, ly.wkv + (size_t)(r0 + lane) * K + kb0 * 32,
-                          bytes, full(b), pol);
+            const uint32_t dst = ring + b * R::kStageBytes;
+            if (WQ2K) {
+                // the group's rows are contiguous: one copy of the 16-byte multiple,
+                // the last 4..12 bytes (a short last group only) by plain stores
+                const int r0 = (grp0 + i) * 16, nrows = min(16, N - r0);
+                const uint32_t total = (uint32_t)nrows * q2k_row, bulk = total & ~15u;
+                const uint8_t *src = ly.wkv_q2k + (size_t)r0 * q2k_row;
+                if (lane < (int)(total - bulk) / 4)
+                    reinterpret_cast<uint32_t *>(smem_raw + b * R::kStageBytes + bulk)[lane] =
+                        __ldg(reinterpret_cast<const uint32_t *>(src + bulk) + lane);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_expect_tx(full(b), bulk);
+                    if (bulk) bulk_load(dst, src, bulk, full(b), pol);
+                }
+            } else {
+                const int grp = grp0 + i / nsub, kb0 = (i % nsub) * kStageKb;
+                const uint32_t bytes = (uint32_t)min(kStageKb, kblocks - kb0) * 64u;
+                const int r0 = grp * 16, nrows = min(16, N - r0);
+                if (lane == 0) mbar_expect_tx(full(b), bytes * (uint32_t)nrows);
+                __syncwarp();
+                if (lane < nrows)
+                    bulk_load(dst + lane * kRowBytes, ly.wkv + (size_t)(r0 + lane) * K + kb0 * 32, bytes, full(b), pol);
+            }
         }
     };
     // the first two stages need nothing computed and do not overlap x: before the wait
@@ -385,45 +340,73 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
                               ? *reinterpret_cast<const uint4 *>(xs + (size_t)g * xstride + kb * 32 + 8 * q)
                               : make_uint4(0, 0, 0, 0);
         }
-    __syncthreads();                       // x is in registers: the ring's upper half is free
+    __syncthreads();                       // x is in registers: the ring's upper stages are free
 
     if (producer) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // x staging writes before the copies
         issue_until(nstages);
         // Let every copy already issued land before the CTA can leave.
         if (lane == 0)
-            for (int d = 1; d <= kMmaStages && issued - d >= 0; ++d) {
+            for (int d = 1; d <= R::kStages && issued - d >= 0; ++d) {
                 const int i = issued - d;
                 const uint64_t t0 = now_ns();
-                while (!mbar_try(full(i % kMmaStages), (i / kMmaStages) & 1) && now_ns() - t0 < 10000000ull) {
+                while (!mbar_try(full(i % R::kStages), (i / R::kStages) & 1) && now_ns() - t0 < 10000000ull) {
                 }
             }
         return;
     }
 
     bool live = true;
+    // wait for stage i: false (for the whole warp) once the CTA is aborting
+    auto acquire = [&](int i) {
+        const bool ok = live && mbar_wait(full(i % R::kStages), (i / R::kStages) & 1, abort_flag, a.err);
+        live = __all_sync(0xFFFFFFFFu, ok);
+        return live;
+    };
+    auto release = [&](int i) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(i % R::kStages));
+    };
     const uint32_t a_off = g * kRowBytes + (warp * kMmaJ) * 64 + 16 * q;
     for (int gi = 0; gi < ngroups; ++gi) {
         float c[4] = {0.f, 0.f, 0.f, 0.f};
+        if (WQ2K) {
+            if (acquire(gi)) {
+                const uint8_t *row_lo = smem_raw + (gi % R::kStages) * R::kStageBytes + g * q2k_row;
+                const uint8_t *row_hi = row_lo + 8 * q2k_row;
 #pragma unroll
-        for (int sub = 0; sub < kMmaSubMax; ++sub) {
-            if (sub < nsub) {
-                const int i = gi * nsub + sub, b = i % kMmaStages;
-                const bool ok = live && mbar_wait(full(b), (i / kMmaStages) & 1, abort_flag, a.err);
-                live = __all_sync(0xFFFFFFFFu, ok);
-                if (live) {
-                    const uint32_t sa = ring + b * kMmaStageBytes + a_off;
+                for (int sub = 0; sub < kMmaSubMax; ++sub) {
 #pragma unroll
                     for (int jj = 0; jj < kMmaJ; ++jj) {
-                        if (sub * kStageKb + warp * kMmaJ + jj < kblocks) {
-                            const uint4 lo = lds128(sa + jj * 64), hi = lds128(sa + 8 * kRowBytes + jj * 64);
+                        const int kb = sub * kStageKb + warp * kMmaJ + jj;
+                        if (sub < nsub && kb < kblocks) {
+                            const uint4 lo = q2k_frag(row_lo, kb, q), hi = q2k_frag(row_hi, kb, q);
                             const uint4 xb = xr[sub][jj];
                             mma_16816(c, lo.x, hi.x, lo.y, hi.y, xb.x, xb.y);
                             mma_16816(c, lo.z, hi.z, lo.w, hi.w, xb.z, xb.w);
                         }
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty(b));
+                }
+                release(gi);
+            }
+        } else {
+#pragma unroll
+            for (int sub = 0; sub < kMmaSubMax; ++sub) {
+                if (sub < nsub) {
+                    const int i = gi * nsub + sub;
+                    if (acquire(i)) {
+                        const uint32_t sa = ring + (i % R::kStages) * R::kStageBytes + a_off;
+#pragma unroll
+                        for (int jj = 0; jj < kMmaJ; ++jj) {
+                            if (sub * kStageKb + warp * kMmaJ + jj < kblocks) {
+                                const uint4 lo = lds128(sa + jj * 64), hi = lds128(sa + 8 * kRowBytes + jj * 64);
+                                const uint4 xb = xr[sub][jj];
+                                mma_16816(c, lo.x, hi.x, lo.y, hi.y, xb.x, xb.y);
+                                mma_16816(c, lo.z, hi.z, lo.w, hi.w, xb.z, xb.w);
+                            }
+                        }
+                        release(i);
+                    }
                 }
             }
         }
@@ -445,17 +428,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     }
 }
 
-template <bool HASH>
+template <bool HASH, bool WQ2K>
 static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (a.T < 1 || a.T > kMmaT || a.K % 32 || (a.K >> 5) > kMmaSubMax * kStageKb) return cudaErrorInvalidValue;
+    if (a.T < 1 || a.T > kMmaT || a.K % (WQ2K ? 256 : 32) || a.K > kGemvMaxK) return cudaErrorInvalidValue;
     if (HASH && (size_t)a.T * a.C > (size_t)kFusedHashMaxIds) return cudaErrorInvalidValue;
-    for (int l = 0; l < a.L; ++l)
-        if (reinterpret_cast<uintptr_t>(a.layer[l].wkv) % 16) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kMmaSmemBytes);
+    for (int l = 0; l < a.L; ++l) {
+        const void *w = WQ2K ? static_cast<const void *>(a.layer[l].wkv_q2k) : static_cast<const void *>(a.layer[l].wkv);
+        if (!w || reinterpret_cast<uintptr_t>(w) % 16) return cudaErrorInvalidValue;
+    }
+    const size_t smem = ring_smem_bytes<WQ2K>();
+    cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<HASH, WQ2K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
     int ctas_per_layer = sms / a.L;
     const int groups = (a.N + 15) / 16;
@@ -464,180 +450,6 @@ static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas_per_layer * a.L);
     cfg.blockDim = dim3(kMmaThreads);
-    cfg.dynamicSmemBytes = kMmaSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = a.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<HASH>, a);
-}
-
-// ---------------------------------------------------------------------------
-// One token against Q2_K-quantised wkv ([N, K/256] blocks of 84 bytes, a row's
-// blocks contiguous): `wkv_q2k` on spark_model/layers/engram_v41.rs, read by
-// the single-token projection in place of the bf16 expansion, 6x fewer bytes.
-// Lane l decodes weights 8l .. 8l+7 of every block -- exactly the k values it
-// owns in gemv_kernel<1> (chunk 32 b + l) -- to bf16 and runs the same FMA
-// sequence and the same butterfly, so kv is bit-identical to the bf16 GEMV on
-// the dequantised weights.
-// ---------------------------------------------------------------------------
-constexpr int kQ2kUnroll = 8;     // blocks a unit: 8 x 256 values = one part of gemv_kernel<1>
-
-// Small non-negative integer -> f32 without the quarter-rate conversion unit:
-// 2^23 + n has n in its low mantissa bits, so subtracting 2^23 is exact.
-__device__ __forceinline__ float small_u2f(uint32_t n) {
-    return __uint_as_float(0x4B000000u | n) - 8388608.0f;
-}
-
-// Lane l's eight weights 8l .. 8l+7 of one Q2_K block, each rounded to bf16
-// and widened back to f32 (the values the bf16 GEMV multiplies).  Same layout
-// as q2k_lane_decode; y = fma(d*sc, q, -dmin*m) equals d*sc*q - dmin*m rounded
-// once because d*sc*q is exact in f32.
-__device__ __forceinline__ void q2k_lane_weights(uint32_t word, int lane, float (&w)[8]) {
-    const int half = lane >> 4, j = (lane & 15) >> 2, m = lane & 3;
-    const int qw = 4 + 8 * half + 2 * m;
-    const uint32_t q0 = __shfl_sync(0xFFFFFFFFu, word, qw);
-    const uint32_t q1 = __shfl_sync(0xFFFFFFFFu, word, qw + 1);
-    const int sb = 8 * half + 2 * j + (m >> 1);
-    const uint32_t scw = __shfl_sync(0xFFFFFFFFu, word, sb >> 2);
-    const uint32_t dw = __shfl_sync(0xFFFFFFFFu, word, 20);
-    const uint32_t sc = (scw >> (8 * (sb & 3))) & 0xFFu;
-    const float d = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFFu)));
-    const float dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
-    const float dl = __fmul_rn(d, small_u2f(sc & 15u));
-    const float nml = -__fmul_rn(dmin, small_u2f(sc >> 4));
-    const uint32_t t0 = (q0 >> (2 * j)) & 0x03030303u, t1 = (q1 >> (2 * j)) & 0x03030303u;
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-        const uint32_t t = e < 4 ? t0 : t1;
-        // byte e of t into the low byte of 0x4B000000: the f32 2^23 + q, minus 2^23
-        const float f0 = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7540u | (e & 3))) - 8388608.0f;
-        const float f1 = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7540u | ((e + 1) & 3))) - 8388608.0f;
-        const float y0 = __fmaf_rn(dl, f0, nml);
-        const float y1 = __fmaf_rn(dl, f1, nml);
-        const uint32_t p = pack_bf16x2(y0, y1);
-        w[e] = bf16_lo(p);
-        w[e + 1] = bf16_hi(p);
-    }
-}
-
-// A warp takes whole rows (round-robin); within a row it walks the parts of
-// gemv_kernel<1> (8 blocks = 256 chunks each), loading part p + 1 while part
-// p decodes, reduces each part by butterfly and adds the parts in order --
-// the bf16 kernel's summation exactly, hence bit-identical kv.
-template <bool HASH>
-__global__ void __launch_bounds__(kGemvThreads, 2) gemv_q2k_kernel(const __grid_constant__ GemvArgs a) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    float *xf = reinterpret_cast<float *>(smem_raw);                       // x widened to f32 [K]
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw + (size_t)a.K * 4);
-    int64_t *s_ids = reinterpret_cast<int64_t *>(smem_raw + (size_t)a.K * 6);
-    const int ctas_per_layer = gridDim.x / a.L;
-    const int li = blockIdx.x / ctas_per_layer;
-    const int cta = blockIdx.x % ctas_per_layer;
-    const GemvLayer &ly = a.layer[li];
-    const int K = a.K, N = a.N, nblk = K >> 8;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwarps = kGemvThreads / 32;
-    const int rows_per_cta = (N + ctas_per_layer - 1) / ctas_per_layer;
-    const int r0 = cta * rows_per_cta;
-    const int r1 = min(N, r0 + rows_per_cta);
-    const int P = (nblk + kQ2kUnroll - 1) / kQ2kUnroll;
-
-    auto load_part = [&](int o, int part, uint32_t (&dst)[kQ2kUnroll]) {
-        const int bb = part * kQ2kUnroll;
-        const uint32_t *w = reinterpret_cast<const uint32_t *>(ly.wkv_q2k + (size_t)o * nblk * 84) + lane;
-#pragma unroll
-        for (int k = 0; k < kQ2kUnroll; ++k) dst[k] = (bb + k < nblk && lane < 21) ? __ldg(w + 21 * (bb + k)) : 0u;
-    };
-    int o = r0 + warp;
-    uint32_t wq[kQ2kUnroll];
-    if (o < r1) load_part(o, 0, wq);
-    if (a.pdl) {
-        griddep_wait();
-        griddep_launch();
-    }
-    const int64_t *ids = ly.ids;
-    int64_t id_stride = a.id_stride;
-    if (HASH) {
-        hash_ids(a, 1, li, cta, s_ids);
-        __syncthreads();
-        ids = s_ids;
-        id_stride = a.C;
-    }
-    stage_x(a, ly, 1, ids, id_stride, xs, K);
-    __syncthreads();
-    for (int i = tid; i < K / 2; i += kGemvThreads) {
-        const uint32_t v = reinterpret_cast<const uint32_t *>(xs)[i];
-        reinterpret_cast<float2 *>(xf)[i] = make_float2(bf16_lo(v), bf16_hi(v));
-    }
-    __syncthreads();
-
-    const float4 *xf4 = reinterpret_cast<const float4 *>(xf);
-    for (; o < r1; o += nwarps) {
-        float row_sum = 0.0f;
-        for (int part = 0; part < P; ++part) {
-            // the next part (or the next row's first part) loads while this one decodes
-            uint32_t wn[kQ2kUnroll];
-            const bool more = part + 1 < P || o + nwarps < r1;
-            if (part + 1 < P) load_part(o, part + 1, wn);
-            else if (o + nwarps < r1) load_part(o + nwarps, 0, wn);
-            const int b0 = part * kQ2kUnroll;
-            float acc = 0.0f;
-#pragma unroll
-            for (int k = 0; k < kQ2kUnroll; ++k) {
-                if (b0 + k < nblk) {                     // warp-uniform
-                    float wv[8];
-                    q2k_lane_weights(wq[k], lane, wv);
-                    const int c = (b0 + k) * 32 + lane;  // the lane's 8 k values: chunk 32 b + l
-                    const float4 xa = xf4[2 * c], xb = xf4[2 * c + 1];
-                    acc = fmaf(wv[0], xa.x, acc);
-                    acc = fmaf(wv[1], xa.y, acc);
-                    acc = fmaf(wv[2], xa.z, acc);
-                    acc = fmaf(wv[3], xa.w, acc);
-                    acc = fmaf(wv[4], xb.x, acc);
-                    acc = fmaf(wv[5], xb.y, acc);
-                    acc = fmaf(wv[6], xb.z, acc);
-                    acc = fmaf(wv[7], xb.w, acc);
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-            row_sum = part == 0 ? acc : row_sum + acc;
-            if (more) {
-#pragma unroll
-                for (int k = 0; k < kQ2kUnroll; ++k) wq[k] = wn[k];
-            }
-        }
-        if (lane == 0) ly.kv[o] = (uint16_t)f32_to_bf16_bits(row_sum);
-    }
-}
-
-// Per-row part sums of one CTA: rows_per_cta x T x parts f32.
-static size_t gemv_psum_bytes(int T, int K, int N, int ctas_per_layer) {
-    const int P = ((K >> 3) + 32 * kGemvUnroll - 1) / (32 * kGemvUnroll);
-    const int rows = (N + ctas_per_layer - 1) / ctas_per_layer;
-    return (size_t)rows * T * P * 4;
-}
-
-template <bool HASH>
-static cudaError_t launch_q2k_h(const GemvArgs &a, cudaStream_t s) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    int ctas_per_layer = (sms * 2) / a.L;
-    const int max_useful = (a.N + 15) / 16;
-    if (ctas_per_layer > max_useful) ctas_per_layer = max_useful;
-    if (ctas_per_layer < 1) ctas_per_layer = 1;
-    const size_t smem = (size_t)a.K * 6 + (HASH ? (size_t)a.C * 8 : 0);
-    if (smem > 100 * 1024) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gemv_q2k_kernel<HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(ctas_per_layer * a.L);
-    cfg.blockDim = dim3(kGemvThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -645,63 +457,22 @@ static cudaError_t launch_q2k_h(const GemvArgs &a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemv_q2k_kernel<HASH>, a);
-}
-
-cudaError_t launch_gemv_q2k(const GemvArgs &a, cudaStream_t s) {
-    if (a.T != 1 || a.K % 256) return cudaErrorInvalidValue;
-    return a.fuse_hash ? launch_q2k_h<true>(a, s) : launch_q2k_h<false>(a, s);
+    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<HASH, WQ2K>, a);
 }
 
 size_t gemv_smem_bytes(int T, int K) {
-    if (T <= 1) {
-        const size_t b = (size_t)K * 2 + (size_t)kFusedHashMaxIds * 8;
-        return b <= 96 * 1024 ? b : SIZE_MAX;           // the rest of 100 KB holds part sums
-    }
-    if (T > kMmaT || K % 32 || (K >> 5) > kMmaSubMax * kStageKb) return SIZE_MAX;   // GEMM path
-    return kMmaSmemBytes;
-}
-
-template <int T, bool HASH>
-static cudaError_t launch_th(const GemvArgs &a, cudaStream_t s) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const size_t base_smem = (size_t)T * a.K * 2 + (HASH ? (size_t)T * a.C * 8 : 0);
-    // two CTAs an SM (the launch bounds), each owning a contiguous block of rows
-    int ctas_per_layer = (sms * 2) / a.L;
-    const int max_useful = (a.N + 15) / 16;          // at least 16 rows a CTA
-    if (ctas_per_layer > max_useful) ctas_per_layer = max_useful;
-    if (ctas_per_layer < 1) ctas_per_layer = 1;
-    const size_t smem = base_smem + gemv_psum_bytes(T, a.K, a.N, ctas_per_layer);
-    if (smem > 100 * 1024) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<T, HASH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(ctas_per_layer * a.L);
-    cfg.blockDim = dim3(kGemvThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = a.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<T, HASH>, a);
-}
-
-template <int T>
-static cudaError_t launch_t(const GemvArgs &a, cudaStream_t s) {
-    return a.fuse_hash ? launch_th<T, true>(a, s) : launch_th<T, false>(a, s);
+    if (T < 1 || T > kMmaT || K % 32 || K > kGemvMaxK) return SIZE_MAX;   // GEMM path
+    return ring_smem_bytes<false>();
 }
 
 cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;
-    if (a.T == 1) return launch_t<1>(a, s);
-    if (gemv_smem_bytes(a.T, a.K) != SIZE_MAX)
-        return a.fuse_hash ? launch_mma<true>(a, s) : launch_mma<false>(a, s);
-    return cudaErrorInvalidValue;
+    return a.fuse_hash ? launch_mma<true, false>(a, s) : launch_mma<false, false>(a, s);
+}
+
+cudaError_t launch_gemv_q2k(const GemvArgs &a, cudaStream_t s) {
+    if (a.T == 0) return cudaSuccess;
+    return a.fuse_hash ? launch_mma<true, true>(a, s) : launch_mma<false, true>(a, s);
 }
 
 }  // namespace engram

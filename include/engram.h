@@ -139,8 +139,8 @@ int engram_rows_q2k(const uint8_t *d_blocks, int64_t R, const int64_t *d_row_ids
 /* Stage 3 (engram.rs CPU reference, `linear_bf16`): d_kv[t, o] =
  * bf16_rne(sum_i d_x[t, i] * d_wkv[o, i]) with f32 accumulation.
  *   d_x [T, K] bf16, d_wkv [N, K] bf16, d_kv [T, N] bf16; all 16-byte aligned.
- * K % 64 == 0, N % 16 == 0.  T <= 8 runs the bandwidth-bound GEMV, larger T
- * the tcgen05 tensor-core GEMM. */
+ * K % 64 == 0, N % 16 == 0.  T <= 8 with K <= 6144 runs the bandwidth-bound
+ * GEMV, anything else the tcgen05 tensor-core GEMM. */
 int engram_project(const uint16_t *d_x, const uint16_t *d_wkv, int32_t T, int32_t K, int32_t N,
                    uint16_t *d_kv, uintptr_t stream);
 
@@ -155,7 +155,8 @@ int engram_gate(float *d_h, const uint16_t *d_kv, const float *d_qk, int32_t T, 
  * `EngramLayerWeights.wkv_q2k`: the weight as the GGUF ships it, read by the
  * single-token projection in place of the bf16 expansion, 6x fewer bytes):
  *   d_wkv_q2k [N, K / 256] 84-byte ggml Q2_K blocks (a row's blocks contiguous,
- *   4-byte aligned); d_x [1, K] bf16; d_kv [1, N] bf16.  K % 256 == 0.
+ *   16-byte aligned); d_x [1, K] bf16; d_kv [1, N] bf16.  K % 256 == 0 and
+ *   K <= 6144 (ENGRAM_E_UNSUPPORTED above).
  * kv is bit-identical to engram_project(d_x, W) where W is the bf16
  * dequantisation of the blocks (engram_rows_q2k). */
 int engram_project_q2k(const uint16_t *d_x, const uint8_t *d_wkv_q2k, int32_t K, int32_t N,
@@ -171,8 +172,9 @@ typedef struct {
     const uint16_t *wkv;    /* [dim * (hc + 1), C * head_dim] bf16; may be NULL when wkv_q2k
                                is set and every call has batch * T == 1 */
     const float *qk;        /* [hc, dim] f32 */
-    const uint8_t *wkv_q2k; /* optional [dim * (hc + 1), C * head_dim / 256] Q2_K blocks: when
-                               every layer has it, single-token calls project from it */
+    const uint8_t *wkv_q2k; /* optional [dim * (hc + 1), C * head_dim / 256] Q2_K blocks,
+                               16-byte aligned: when every layer has it and C * head_dim
+                               <= 6144, single-token calls project from it */
 } engram_layer;
 
 /* The whole forward for n_layers engram layers (in `layers` order) on one

@@ -103,5 +103,9 @@ def test_compute_calls_refuse_before_launch(E):
     assert L.engram_rows_fp8(odd, a16, 10, 64, 32, a16, 1, 4, 4, a16, None) == -3
     assert L.engram_rows_fp8(a16, a16, 10, 64, 32, a16, 1, 3, 4, a16, None) == -1
     assert L.engram_rows_q2k(P((1 << 20) + 1), 10, a16, 1, 4, 4, a16, None) == -3
+    # Q2_K weights are copied by the bulk-copy engine: 16-byte aligned, K % 256, K <= 6144
+    assert L.engram_project_q2k(a16, P((1 << 20) + 4), 256, 16, a16, None) == -3
+    assert L.engram_project_q2k(a16, a16, 320, 16, a16, None) == -1
+    assert L.engram_project_q2k(a16, a16, 6400, 16, a16, None) == -11
     assert L.engram_hash(None, a16, 1, 0, a16, None) == -2
     assert L.engram_set_profile_events(a16, 3) == -1
