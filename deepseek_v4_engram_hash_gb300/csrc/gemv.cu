@@ -201,8 +201,12 @@ __device__ __forceinline__ float small_u2f(uint32_t n) {
 // With kk = kb % 8 the values share half = kk / 4, j = kk % 4 and sub-block
 // 8 half + 2j + q/2; their quant bytes are qs[32 half + 8q + e] (block words
 // 4 + 8 half + 2q and the next) and the quant is (byte >> 2j) & 3.
-// y = fma(d*sc, q, -dmin*m) equals d*sc*q - dmin*m rounded once (d*sc*q and
-// dmin*m are exact in f32), as the row decoder computes it.
+// A value is y = d*sc*q - dmin*m rounded once (d*sc*q and dmin*m are exact in
+// f32, so fma(d*sc, q, -dmin*m) is that), then bf16: with one sub-block the
+// lane's eight values take one of four, v[q].  v[0..3] are built once and
+// each pair (v[q_e], v[q_e+1]) is one byte permute of them, its selector
+// nibbles 2q_e, 2q_e + 1, 2q_e+1, 2q_e+1 + 1 = h * 0x22 + 0x1010 for the
+// two quant bytes h = q_e + 256 q_e+1.
 __device__ __forceinline__ uint4 q2k_frag(const uint8_t *row, int kb, int q) {
     const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (kb >> 3) * 84);
     const int kk = kb & 7, half = kk >> 2, j = kk & 3;
@@ -214,17 +218,13 @@ __device__ __forceinline__ uint4 q2k_frag(const uint8_t *row, int kb, int q) {
     const float dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
     const float dl = __fmul_rn(d, small_u2f(sc & 15u));
     const float nml = -__fmul_rn(dmin, small_u2f(sc >> 4));
+    const uint32_t v01 = pack_bf16x2(__fmaf_rn(dl, 0.0f, nml), __fmaf_rn(dl, 1.0f, nml));
+    const uint32_t v23 = pack_bf16x2(__fmaf_rn(dl, 2.0f, nml), __fmaf_rn(dl, 3.0f, nml));
     const uint32_t t0 = (q0 >> (2 * j)) & 0x03030303u, t1 = (q1 >> (2 * j)) & 0x03030303u;
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-        const uint32_t t = e < 4 ? t0 : t1;
-        // byte e of t into the low byte of 0x4B000000: the f32 2^23 + q, minus 2^23
-        const float f0 = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7540u | (e & 3))) - 8388608.0f;
-        const float f1 = __uint_as_float(__byte_perm(t, 0x4B000000u, 0x7540u | ((e + 1) & 3))) - 8388608.0f;
-        o[e >> 1] = pack_bf16x2(__fmaf_rn(dl, f0, nml), __fmaf_rn(dl, f1, nml));
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
+    return make_uint4(__byte_perm(v01, v23, t0 * 0x22u + 0x1010u),
+                      __byte_perm(v01, v23, (t0 >> 16) * 0x22u + 0x1010u),
+                      __byte_perm(v01, v23, t1 * 0x22u + 0x1010u),
+                      __byte_perm(v01, v23, (t1 >> 16) * 0x22u + 0x1010u));
 }
 
 // One CTA per SM, each owning a contiguous run of 16-row groups of one layer.
