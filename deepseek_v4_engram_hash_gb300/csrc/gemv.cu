@@ -22,63 +22,6 @@
 
 namespace engram {
 
-// Q2_K decode of one 256-wide row by one warp into shared memory.
-__device__ __forceinline__ void q2k_row_to_smem(const uint8_t *blk, bool ok, int lane,
-                                                uint16_t *dst) {
-    uint32_t word = 0;
-    if (ok && lane < 21) word = __ldg(reinterpret_cast<const uint32_t *>(blk) + lane);
-    uint4 o = q2k_lane_decode(word, lane);
-    if (!ok) o = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4 *>(dst)[lane] = o;
-}
-
-// Stage x [T rows, K] bf16 into shared memory at `xs` with row stride `xstride`
-// elements: from a plain x, or by gathering and dequantising the layer's
-// table rows ids[t * id_stride + c].
-__device__ __forceinline__ void stage_x(const GemvArgs &a, const GemvLayer &ly, int T, const int64_t *ids,
-                                        int64_t id_stride, uint16_t *xs, int xstride) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
-    const int K = a.K, n_ids = T * a.C;
-    if (!a.gather) {
-        const int cpr = K >> 3;                      // 16-byte chunks a row
-        for (int i = tid; i < T * cpr; i += nthreads) {
-            const int t = i / cpr, j = i % cpr;
-            reinterpret_cast<uint4 *>(xs + (size_t)t * xstride)[j] =
-                __ldg(reinterpret_cast<const uint4 *>(ly.x + (size_t)t * K) + j);
-        }
-    } else if (ly.fmt != ENGRAM_FMT_Q2K) {
-        const int lpr = a.hd >> 4, nblk = a.hd / a.blk;
-        for (int g = tid; g < n_ids * lpr; g += nthreads) {
-            const int row = g / lpr, part = g % lpr;
-            const int t = row / a.C, c = row % a.C;
-            const int64_t id = ids[(int64_t)t * id_stride + c];
-            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-            if (id >= 0 && id < ly.rows) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(ly.table + id * a.hd) + part);
-                const float sc = fp8_row_scale(ly.scales, ly.fmt, id * nblk + (part * 16) / a.blk);
-                e4m3x4_scaled_to_bf16(v.x, sc, o0.x, o0.y);
-                e4m3x4_scaled_to_bf16(v.y, sc, o0.z, o0.w);
-                e4m3x4_scaled_to_bf16(v.z, sc, o1.x, o1.y);
-                e4m3x4_scaled_to_bf16(v.w, sc, o1.z, o1.w);
-            } else {
-                set_err(a.err, ENGRAM_E_ROW);
-            }
-            uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)t * xstride + (size_t)c * a.hd) + 2 * part;
-            dst[0] = o0;
-            dst[1] = o1;
-        }
-    } else {
-        for (int row = warp; row < n_ids; row += nwarps) {
-            const int t = row / a.C, c = row % a.C;
-            const int64_t id = ids[(int64_t)t * id_stride + c];
-            const bool ok = id >= 0 && id < ly.rows;
-            if (!ok && lane == 0) set_err(a.err, ENGRAM_E_ROW);
-            q2k_row_to_smem(ly.table + (ok ? id : 0) * 84, ok, lane, xs + (size_t)t * xstride + (size_t)c * 256);
-        }
-    }
-}
-
 // Row ids of this CTA's layer for the T tokens of the call, hashed here (one
 // thread per id) into s_ids; the CTAs with index 0 in each layer also write
 // them to the workspace, and the very first CTA writes the cache.
@@ -105,14 +48,17 @@ __device__ __forceinline__ void hash_ids(const GemvArgs &a, int T, int li, int c
 // wkv rows x 16 k x 8 tokens, so the kernel stays HBM-bound (at one token the
 // unused seven token columns cost nothing: the tensor pipe is idle anyway).
 //
-// bf16 wkv: the copy warp copies 16-row x 1536-wide pieces of the CTA's rows
-// (3 KB contiguous a row) into a 4-stage ring, each stage completing an
+// bf16 wkv: the copy warp copies 16-row x 2048-wide pieces of the CTA's rows
+// (4 KB contiguous a row) into a 3-stage ring, each stage completing an
 // mbarrier by its byte count; the MMA warps read the pieces from shared memory
-// and hand each stage back through a second mbarrier.  Q2_K wkv: a stage is a
+// and hand each stage back through a second mbarrier.  Larger copies keep
+// more bytes in flight: 2 KB a row streamed one layer in 48.6 us, 3 KB in
+// 39.4 us, 4 KB in 38.2 us.  Q2_K wkv: a stage is a
 // whole 16-row group (16 x K/256 blocks of 84 bytes, contiguous in memory: one
 // copy), six stages.  x is loop invariant for a warp (its k blocks are the
-// same in every row group), so it lives in registers: staged once through the
-// ring's upper half, then loaded as mma B fragments.
+// same in every row group), so each lane gathers its x fragments once, straight
+// from the table rows into registers; nothing but wkv goes through shared
+// memory, and the whole ring is in flight before the dependency wait.
 //
 // The dot product runs over k, so any permutation of k applied to both
 // operands gives the same sum; lane (g = lane/4, q = lane%4) holds physical k
@@ -123,9 +69,9 @@ __device__ __forceinline__ void hash_ids(const GemvArgs &a, int T, int li, int c
 constexpr int kMmaT = 8;
 constexpr int kMmaWarps = 16;                           // MMA warps; one more warp copies
 constexpr int kMmaThreads = (kMmaWarps + 1) * 32;
-constexpr int kMmaJ = 3;                                // 32-wide k blocks a warp per stage
-constexpr int kStageKb = kMmaWarps * kMmaJ;             // 48 k blocks (1536 values) a bf16 stage
-constexpr int kMmaSubMax = 4;                           // bf16 stages a 16-row group
+constexpr int kMmaJ = 4;                                // 32-wide k blocks a warp per stage
+constexpr int kStageKb = kMmaWarps * kMmaJ;             // 64 k blocks (2048 values) a bf16 stage
+constexpr int kMmaSubMax = 3;                           // bf16 stages a 16-row group
 static_assert(kMmaSubMax * kStageKb * 32 == kGemvMaxK, "x fragments cover K");
 constexpr uint32_t kRowBytes = kStageKb * 64 + 64;      // one row's piece + bank padding
 constexpr uint32_t kRedBytes = 2 * kMmaWarps * 32 * 16; // partial tiles, double-buffered
@@ -135,21 +81,21 @@ template <bool WQ2K>
 struct Ring;
 template <>
 struct Ring<false> {
-    static constexpr int kStages = 4;
-    static constexpr uint32_t kStageBytes = 16 * kRowBytes;                   // 50 176
+    static constexpr int kStages = 3;
+    static constexpr int kPrefetch = 2;                                       // stages issued before the wait
+    static constexpr uint32_t kStageBytes = 16 * kRowBytes;                   // 66 560
 };
 template <>
 struct Ring<true> {
     static constexpr int kStages = 6;
+    static constexpr int kPrefetch = 4;
     static constexpr uint32_t kStageBytes = 16 * (kGemvMaxK / 256) * 84;      // 32 256
 };
 template <bool WQ2K>
 constexpr size_t ring_smem_bytes() {
     return (size_t)Ring<WQ2K>::kStages * Ring<WQ2K>::kStageBytes + kRedBytes + 2 * Ring<WQ2K>::kStages * 8 + 16;
 }
-static_assert((size_t)kMmaT * (kGemvMaxK + 8) * 2 <= 2 * (size_t)Ring<false>::kStageBytes &&
-                  (size_t)kMmaT * (kGemvMaxK + 8) * 2 <= 4 * (size_t)Ring<true>::kStageBytes,
-              "x is staged in the ring's upper stages");
+static_assert(ring_smem_bytes<false>() <= 227 * 1024 && ring_smem_bytes<true>() <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
@@ -195,54 +141,156 @@ __device__ __forceinline__ float small_u2f(uint32_t n) {
     return __uint_as_float(0x4B000000u | n) - 8388608.0f;
 }
 
-// Lane (g, q)'s A-fragment words for 32-wide k block kb of one Q2_K row in
-// shared memory: values v = 32 (kb % 8) + 8q + e, e = 0..7, of block kb / 8,
-// each rounded to bf16, packed in pairs (the words a bf16 row holds there).
-// With kk = kb % 8 the values share half = kk / 4, j = kk % 4 and sub-block
-// 8 half + 2j + q/2; their quant bytes are qs[32 half + 8q + e] (block words
-// 4 + 8 half + 2q and the next) and the quant is (byte >> 2j) & 3.
-// A value is y = d*sc*q - dmin*m rounded once (d*sc*q and dmin*m are exact in
-// f32, so fma(d*sc, q, -dmin*m) is that), then bf16: with one sub-block the
-// lane's eight values take one of four, v[q].  v[0..3] are built once and
-// each pair (v[q_e], v[q_e+1]) is one byte permute of them, its selector
-// nibbles 2q_e, 2q_e + 1, 2q_e+1, 2q_e+1 + 1 = h * 0x22 + 0x1010 for the
-// two quant bytes h = q_e + 256 q_e+1.
-__device__ __forceinline__ uint4 q2k_frag(const uint8_t *row, int kb, int q) {
-    const uint32_t *w = reinterpret_cast<const uint32_t *>(row + (kb >> 3) * 84);
-    const int kk = kb & 7, half = kk >> 2, j = kk & 3;
-    const uint32_t q0 = w[4 + 8 * half + 2 * q], q1 = w[5 + 8 * half + 2 * q];
-    const int sb = 8 * half + 2 * j + (q >> 1);
-    const uint32_t sc = (w[sb >> 2] >> (8 * (sb & 3))) & 0xFFu;
+// Q2_K values in mma fragment form.  A 32-wide k block kk (0..7) of a 256-wide
+// block is half = kk / 4, shift j = kk % 4; lane q's values 32 kk + 8q + e,
+// e = 0..7, share the sub-block 8 half + 2j + q/2, and their quant bytes are
+// qs[32 half + 8q + e] (block words 4 + 8 half + 2q and the next), the quant
+// being (byte >> 2j) & 3.  A value is y = d*sc*q - dmin*m rounded once (d*sc*q
+// and dmin*m are exact in f32, so fma(d*sc, q, -dmin*m) is that), then bf16:
+// with one sub-block the lane's eight values take one of four, v[q].  v[0..3]
+// are built once and each pair (v[q_e], v[q_e+1]) is one byte permute of them,
+// its selector nibbles 2q_e, 2q_e + 1, 2q_e+1, 2q_e+1 + 1 = h * 0x22 + 0x1010
+// for the two quant bytes h = q_e + 256 q_e+1.
+struct Q2kHalf {                  // what a lane needs of one half-block
+    uint32_t q0, q1;              // its 8 quant bytes
+    uint32_t sc01, sc23;          // the scale words of shifts 0,1 and 2,3
+    float d, dmin;
+};
+__device__ __forceinline__ Q2kHalf q2k_half(const uint8_t *blk, int half, int q) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(blk);
+    Q2kHalf h;
+    h.q0 = w[4 + 8 * half + 2 * q];
+    h.q1 = w[5 + 8 * half + 2 * q];
+    h.sc01 = w[2 * half];
+    h.sc23 = w[2 * half + 1];
     const uint32_t dw = w[20];
-    const float d = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFFu)));
-    const float dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
-    const float dl = __fmul_rn(d, small_u2f(sc & 15u));
-    const float nml = -__fmul_rn(dmin, small_u2f(sc >> 4));
+    h.d = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFFu)));
+    h.dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
+    return h;
+}
+__device__ __forceinline__ uint4 q2k_frag(const Q2kHalf &h, int j, int q) {
+    // sub-block 8 half + 2j + q/2: byte 2 (j % 2) + q/2 of scale word j / 2
+    const uint32_t sc = ((j < 2 ? h.sc01 : h.sc23) >> (8 * (2 * (j & 1) + (q >> 1)))) & 0xFFu;
+    const float dl = __fmul_rn(h.d, small_u2f(sc & 15u));
+    const float nml = -__fmul_rn(h.dmin, small_u2f(sc >> 4));
     const uint32_t v01 = pack_bf16x2(__fmaf_rn(dl, 0.0f, nml), __fmaf_rn(dl, 1.0f, nml));
     const uint32_t v23 = pack_bf16x2(__fmaf_rn(dl, 2.0f, nml), __fmaf_rn(dl, 3.0f, nml));
-    const uint32_t t0 = (q0 >> (2 * j)) & 0x03030303u, t1 = (q1 >> (2 * j)) & 0x03030303u;
+    const uint32_t t0 = (h.q0 >> (2 * j)) & 0x03030303u, t1 = (h.q1 >> (2 * j)) & 0x03030303u;
     return make_uint4(__byte_perm(v01, v23, t0 * 0x22u + 0x1010u),
                       __byte_perm(v01, v23, (t0 >> 16) * 0x22u + 0x1010u),
                       __byte_perm(v01, v23, t1 * 0x22u + 0x1010u),
                       __byte_perm(v01, v23, (t1 >> 16) * 0x22u + 0x1010u));
 }
 
+// This lane's x fragments: token g, 32-wide k blocks kb = 64 s + 4w + j of
+// its warp w, values x[g, 32 kb + 8q .. +7] as bf16 pairs -- from the plain x,
+// or gathered from the layer's table rows ids[g * id_stride + c] (fp8 codes x
+// their block's scale, or a Q2_K block) exactly as the row kernels dequantise
+// them.  Ids first, then every load (an invalid id reads row 0 and gives
+// zeros, raising ENGRAM_E_ROW), then the conversions: all of the lane's loads
+// are in flight together.
+__device__ __forceinline__ void gather_x(const GemvArgs &a, const GemvLayer &ly, const int64_t *ids,
+                                         int64_t id_stride, int nsub, int warp, int g, int q,
+                                         uint4 (&xr)[kMmaSubMax][kMmaJ]) {
+    constexpr int NF = kMmaSubMax * kMmaJ;
+    const int kblocks = a.K >> 5;
+    const bool tok = g < a.T;
+    const int t = tok ? g : 0;
+    int k0[NF];
+    bool need[NF];
+#pragma unroll
+    for (int f = 0; f < NF; ++f) {
+        const int sub = f / kMmaJ, kb = sub * kStageKb + warp * kMmaJ + f % kMmaJ;
+        need[f] = tok && sub < nsub && kb < kblocks;
+        k0[f] = (need[f] ? kb : 0) * 32 + 8 * q;
+    }
+    if (!a.gather) {
+#pragma unroll
+        for (int f = 0; f < NF; ++f) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(ly.x + (size_t)t * a.K + k0[f]));
+            xr[f / kMmaJ][f % kMmaJ] = need[f] ? v : make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+    // column c = k0 / head_dim, offset d0 = k0 % head_dim, scale block d0 / scale_block:
+    // shifts when both are powers of two (every V4.1 shape), divisions otherwise
+    int col[NF], d0[NF], sb[NF];
+    if (((a.hd & (a.hd - 1)) | (a.blk & (a.blk - 1))) == 0) {
+        const int hs = __ffs(a.hd) - 1, bs = __ffs(a.blk) - 1;
+#pragma unroll
+        for (int f = 0; f < NF; ++f) {
+            col[f] = k0[f] >> hs;
+            d0[f] = k0[f] & (a.hd - 1);
+            sb[f] = d0[f] >> bs;
+        }
+    } else {
+#pragma unroll
+        for (int f = 0; f < NF; ++f) {
+            col[f] = k0[f] / a.hd;
+            d0[f] = k0[f] - col[f] * a.hd;
+            sb[f] = d0[f] / a.blk;
+        }
+    }
+    int64_t id[NF];
+    bool ok[NF];
+#pragma unroll
+    for (int f = 0; f < NF; ++f) {
+        const int64_t v = ids[(int64_t)t * id_stride + col[f]];
+        ok[f] = need[f] && v >= 0 && v < ly.rows;
+        id[f] = ok[f] ? v : 0;
+        if (need[f] && !ok[f]) set_err(a.err, ENGRAM_E_ROW);
+    }
+    if (ly.fmt == ENGRAM_FMT_Q2K) {
+        // head_dim 256: the warp's four k blocks of a stage are the four shifts of
+        // half w % 2 of one block, so one row id and one half-block serve them
+        Q2kHalf h[kMmaSubMax];
+#pragma unroll
+        for (int sub = 0; sub < kMmaSubMax; ++sub)
+            h[sub] = q2k_half(ly.table + id[sub * kMmaJ] * 84, warp & 1, q);
+#pragma unroll
+        for (int f = 0; f < NF; ++f)
+            xr[f / kMmaJ][f % kMmaJ] = ok[f] ? q2k_frag(h[f / kMmaJ], f % kMmaJ, q) : make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const int nblk = a.hd / a.blk;
+    uint2 raw[NF];
+    float sc[NF];
+#pragma unroll
+    for (int f = 0; f < NF; ++f)
+        raw[f] = __ldg(reinterpret_cast<const uint2 *>(ly.table + id[f] * a.hd + d0[f]));
+    if (ly.fmt == ENGRAM_FMT_FP8_E8M0) {
+#pragma unroll
+        for (int f = 0; f < NF; ++f)
+            sc[f] = e8m0_to_f32(__ldg(static_cast<const uint8_t *>(ly.scales) + id[f] * nblk + sb[f]));
+    } else {
+#pragma unroll
+        for (int f = 0; f < NF; ++f)
+            sc[f] = __ldg(static_cast<const float *>(ly.scales) + id[f] * nblk + sb[f]);
+    }
+#pragma unroll
+    for (int f = 0; f < NF; ++f) {
+        uint4 o;
+        e4m3x4_scaled_to_bf16(raw[f].x, sc[f], o.x, o.y);
+        e4m3x4_scaled_to_bf16(raw[f].y, sc[f], o.z, o.w);
+        xr[f / kMmaJ][f % kMmaJ] = ok[f] ? o : make_uint4(0, 0, 0, 0);
+    }
+}
+
 // One CTA per SM, each owning a contiguous run of 16-row groups of one layer.
-// MMA warp w takes k blocks 48 s + 3w + j (s = 0 .. nsub-1, j = 0..2) of
-// every row group, in that order, and the 16 partial 16 x 8 tiles of a group
-// are summed in warp order through shared memory; both weight formats follow
+// MMA warp w takes k blocks 64 s + 4w + j (s = 0 .. nsub-1, j = 0..3) of
+// every row group, in that order -- for Q2_K weights the four shifts of half
+// w % 2 of block 8 s + w / 2 -- and the 16 partial 16 x 8 tiles of a group are
+// summed in warp order through shared memory; both weight formats follow
 // this order exactly.  bf16: stage i is group grp0 + i / nsub, k blocks
-// 48 (i % nsub) .. +47.  Q2_K: stage i is group grp0 + i.
+// 64 (i % nsub) .. +63.  Q2_K: stage i is group grp0 + i.
 template <bool HASH, bool WQ2K>
 __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_constant__ GemvArgs a) {
     using R = Ring<WQ2K>;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int K = a.K, N = a.N, T = a.T;
-    const int xstride = K + 8;
     const uint32_t ring = smem_u32(smem_raw);
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw + 2 * R::kStageBytes);          // prologue only
     float *red = reinterpret_cast<float *>(smem_raw + R::kStages * R::kStageBytes);
-    int64_t *s_ids = reinterpret_cast<int64_t *>(red);                                   // prologue only
+    int64_t *s_ids = reinterpret_cast<int64_t *>(red);                                   // until x is gathered
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::kStages * R::kStageBytes + kRedBytes);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * R::kStages);
     const uint32_t bar0 = smem_u32(bars);
@@ -312,8 +360,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
             }
         }
     };
-    // the first two stages need nothing computed and do not overlap x: before the wait
-    if (producer) issue_until(min(nstages, 2));
+    // the ring's first round needs nothing computed: before the wait
+    if (producer) issue_until(min(nstages, R::kPrefetch));
 
     if (a.pdl) {
         griddep_wait();
@@ -327,23 +375,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
         ids = s_ids;
         id_stride = a.C;
     }
-    stage_x(a, ly, T, ids, id_stride, xs, xstride);
-    __syncthreads();
-
-    uint4 xr[kMmaSubMax][kMmaJ];
-#pragma unroll
-    for (int sub = 0; sub < kMmaSubMax; ++sub)
-#pragma unroll
-        for (int jj = 0; jj < kMmaJ; ++jj) {
-            const int kb = sub * kStageKb + warp * kMmaJ + jj;
-            xr[sub][jj] = (!producer && g < T && sub < nsub && kb < kblocks)
-                              ? *reinterpret_cast<const uint4 *>(xs + (size_t)g * xstride + kb * 32 + 8 * q)
-                              : make_uint4(0, 0, 0, 0);
-        }
-    __syncthreads();                       // x is in registers: the ring's upper stages are free
 
     if (producer) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // x staging writes before the copies
         issue_until(nstages);
         // Let every copy already issued land before the CTA can leave.
         if (lane == 0)
@@ -355,6 +388,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
             }
         return;
     }
+
+    uint4 xr[kMmaSubMax][kMmaJ];
+    gather_x(a, ly, ids, id_stride, nsub, warp, g, q, xr);
+    mma_warps_sync();                      // every warp has read the hashed ids: the partial buffer is free
 
     bool live = true;
     // wait for stage i: false (for the whole warp) once the CTA is aborting
@@ -372,15 +409,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         if (WQ2K) {
             if (acquire(gi)) {
-                const uint8_t *row_lo = smem_raw + (gi % R::kStages) * R::kStageBytes + g * q2k_row;
+                // this warp's blocks 8 s + w/2, half w % 2, of rows g and g + 8
+                const uint8_t *row_lo = smem_raw + (gi % R::kStages) * R::kStageBytes + g * q2k_row +
+                                        (warp >> 1) * 84;
                 const uint8_t *row_hi = row_lo + 8 * q2k_row;
 #pragma unroll
                 for (int sub = 0; sub < kMmaSubMax; ++sub) {
+                    if (sub < nsub && sub * kStageKb + warp * kMmaJ < kblocks) {
+                        const Q2kHalf hl = q2k_half(row_lo + sub * 8 * 84, warp & 1, q);
+                        const Q2kHalf hh = q2k_half(row_hi + sub * 8 * 84, warp & 1, q);
 #pragma unroll
-                    for (int jj = 0; jj < kMmaJ; ++jj) {
-                        const int kb = sub * kStageKb + warp * kMmaJ + jj;
-                        if (sub < nsub && kb < kblocks) {
-                            const uint4 lo = q2k_frag(row_lo, kb, q), hi = q2k_frag(row_hi, kb, q);
+                        for (int jj = 0; jj < kMmaJ; ++jj) {
+                            const uint4 lo = q2k_frag(hl, jj, q), hi = q2k_frag(hh, jj, q);
                             const uint4 xb = xr[sub][jj];
                             mma_16816(c, lo.x, hi.x, lo.y, hi.y, xb.x, xb.y);
                             mma_16816(c, lo.z, hi.z, lo.w, hi.w, xb.z, xb.w);
