@@ -47,7 +47,7 @@ def _src_hash(*names) -> str:
 
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by the
 # source hash of the kernel they were taken on; a changed kernel reports null.
-NCU_TRAFFIC = {("gemv", "d9c6a1e70819"): 506808576}   # 503.40 MB read + 3.41 MB written
+NCU_TRAFFIC = {("gemv", "fff56fb49961"): 506461696}   # 503.42 MB read + 3.04 MB written
 
 
 class Clocks:
@@ -494,7 +494,7 @@ def main():
     e2e_ms = _max_over_ranks(d["e2e_ms"], world)
     gemv_gbs = gemv_bytes(cfg, M) / (d["gemv_ms"] * 1e-3) / 1e9
     step_gbs = step_bytes(cfg, M) / (ms * 1e-3) / 1e9
-    key = _src_hash("gemv.cu")
+    key = _src_hash("gemv.cu", "common.cuh")
     traffic = NCU_TRAFFIC.get(("gemv", key))
 
     pre = None
@@ -564,7 +564,7 @@ def main():
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "roofline": {"bound": "hbm", "achieved": gemv_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": gemv_gbs / hbm, "traffic": traffic,
-                         "kernel": "gemv_kernel<1> (fused row gather + wkv GEMV, both layers)",
+                         "kernel": "gemv_mma_kernel<1, 0> (fused hash, row gather and wkv GEMV, both layers)",
                          "algorithmic_bytes": gemv_bytes(cfg, M), "peak_source": f"{peak_src} hbm_gbs"},
             "step_roofline": {"achieved": step_gbs, "frac": step_gbs / hbm, "algorithmic_bytes": step_bytes(cfg, M)},
             "stage_ms": dict(zip(["hash", "gather", "gemv", "gate"], d["stage_ms"])),
