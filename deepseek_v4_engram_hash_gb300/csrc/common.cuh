@@ -174,7 +174,9 @@ __device__ __forceinline__ int64_t hash_one(const HashArgs &a, int64_t sp, int b
     const int C = (a.ng - 1) * a.H;
     const int64_t pos = sp + s;
     const int n_top = col / a.H + 1;
-    int64_t tok[kMaxNgram];
+    const int64_t *m = a.mult + (int64_t)li * a.ng;
+    // the window's token at each shift, folded into the rolling XOR as it is formed
+    uint64_t rolling = 0;
     bool blocked = false;
     for (int shift = 0; shift <= n_top; ++shift) {
         int64_t src;
@@ -186,11 +188,9 @@ __device__ __forceinline__ int64_t hash_one(const HashArgs &a, int64_t sp, int b
             src = a.cache[(int64_t)b * a.max_seq + (pos - shift)];
         }
         blocked = blocked || pos < shift || src == -1;
-        tok[shift] = blocked ? a.pad_id : src;
+        const uint64_t term = (uint64_t)(blocked ? a.pad_id : src) * (uint64_t)m[shift];
+        rolling = shift == 0 ? term : rolling ^ term;
     }
-    const int64_t *m = a.mult + (int64_t)li * a.ng;
-    uint64_t rolling = (uint64_t)tok[0] * (uint64_t)m[0];
-    for (int n = 1; n <= n_top; ++n) rolling ^= (uint64_t)tok[n] * (uint64_t)m[n];
     const int64_t slot = (int64_t)li * C + col;
     return (int64_t)(rem_euclid_barrett(rolling, (uint64_t)a.primes[slot], a.bm[slot], a.wrap[slot]) +
                      (uint64_t)a.offsets[slot]);

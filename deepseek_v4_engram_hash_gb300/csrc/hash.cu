@@ -17,31 +17,39 @@
 
 namespace engram {
 
+// 32-bit indices (the launcher splits larger calls by sequence): the split
+// of a thread index into (token, layer, column) is two 32-bit divisions.
 __global__ void __launch_bounds__(256) hash_kernel(const HashArgs a) {
-    const int C = (a.ng - 1) * a.H;
-    const int64_t total = (int64_t)a.B * a.T * a.L * C;
+    const uint32_t C = (uint32_t)((a.ng - 1) * a.H), LC = (uint32_t)a.L * C, T = (uint32_t)a.T;
+    const uint32_t total = (uint32_t)a.B * T * LC;
     int64_t sp;
     if (!hash_start(a, sp)) return;
-    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
-         g += (int64_t)gridDim.x * blockDim.x) {
-        const int col = (int)(g % C);
-        const int li = (int)((g / C) % a.L);
-        const int64_t bs = g / ((int64_t)C * a.L);
-        const int s = (int)(bs % a.T);
-        const int b = (int)(bs / a.T);
-        a.out[g] = hash_one(a, sp, b, s, li, col);
-        if (li == 0 && col == 0) a.cache[(int64_t)b * a.max_seq + sp + s] = hash_compress(a, b, s);
+    for (uint32_t g = blockIdx.x * blockDim.x + threadIdx.x; g < total; g += gridDim.x * blockDim.x) {
+        const uint32_t m = g / LC, j = g - m * LC;
+        const uint32_t li = j / C, col = j - li * C;
+        const uint32_t b = m / T, s = m - b * T;
+        a.out[g] = hash_one(a, sp, (int)b, (int)s, (int)li, (int)col);
+        if (j == 0) a.cache[(int64_t)b * a.max_seq + sp + s] = hash_compress(a, (int)b, s);
     }
 }
 
 cudaError_t launch_hash(const HashArgs &a, cudaStream_t s) {
-    const int C = (a.ng - 1) * a.H;
-    const int64_t total = (int64_t)a.B * a.T * a.L * C;
-    if (total == 0) return cudaSuccess;
-    const int threads = 256;
-    const int64_t blocks = (total + threads - 1) / threads;
-    hash_kernel<<<(unsigned)(blocks < 65535 ? blocks : 65535), threads, 0, s>>>(a);
-    return cudaGetLastError();
+    const int64_t per_seq = (int64_t)a.T * a.L * (a.ng - 1) * a.H;
+    if (per_seq * a.B == 0) return cudaSuccess;
+    if (per_seq >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+    const int64_t seqs = ((int64_t)1 << 31) / per_seq;               // sequences a launch
+    for (int64_t b0 = 0; b0 < a.B; b0 += seqs) {
+        HashArgs h = a;
+        h.B = (int32_t)(a.B - b0 < seqs ? a.B - b0 : seqs);
+        h.ids = a.ids + b0 * a.T;
+        h.cache = a.cache + b0 * a.max_seq;
+        h.out = a.out + b0 * per_seq;
+        const int64_t blocks = (per_seq * h.B + 255) / 256;
+        hash_kernel<<<(unsigned)(blocks < 65535 ? blocks : 65535), 256, 0, s>>>(h);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace engram
