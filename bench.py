@@ -47,7 +47,7 @@ def _src_hash(*names) -> str:
 
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by the
 # source hash of the kernel they were taken on; a changed kernel reports null.
-NCU_TRAFFIC = {("gemv", "fff56fb49961"): 506461696}   # 503.42 MB read + 3.04 MB written
+NCU_TRAFFIC = {("gemv", "3b4992606baf"): 506805248}   # 503.42 MB read + 3.39 MB written
 
 
 class Clocks:
@@ -454,7 +454,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true", help="skip the Q2_K and large-table lines")
-    ap.add_argument("--only", choices=["decode", "prefill", "wkvq2k", "decode8"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill", "wkvq2k", "wkvq2k8", "decode8"], default=None,
                     help="run one workload only (for profiling); prints its own JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -478,9 +478,9 @@ def main():
         from deepseek_v4_engram_hash_gb300 import configs
         print(json.dumps(run_decode_only(configs.V41_DECODE, args.steps, batch=8)), flush=True)
         return
-    if args.only == "wkvq2k":
+    if args.only in ("wkvq2k", "wkvq2k8"):
         from deepseek_v4_engram_hash_gb300 import configs
-        r = run_decode_only(configs.V41_DECODE_WKVQ2K, args.steps)
+        r = run_decode_only(configs.V41_DECODE_WKVQ2K, args.steps, batch=8 if args.only == "wkvq2k8" else 1)
         print(json.dumps(r), flush=True)
         return
     if args.only == "prefill":
@@ -538,6 +538,10 @@ def main():
         r["workload"] = configs.V41_DECODE_WKVQ2K.name
         r["note"] = "projection read from Q2_K-quantised wkv (82.6 MB a step instead of 503.3 MB)"
         others[configs.V41_DECODE_WKVQ2K.name] = r
+        r = run_decode_only(configs.V41_DECODE_WKVQ2K, 1000, batch=8)
+        r["workload"] = "v41_decode_B8_wkv_q2k"
+        r["note"] = "8 sequences x 1 token a step, projection from Q2_K-quantised wkv"
+        others["v41_decode_B8_wkv_q2k"] = r
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and args.only is None:

@@ -470,11 +470,11 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
     const int64_t M = (int64_t)hs->batch * T;
     bool all_q2k = K % 256 == 0;
     for (int l = 0; l < L; ++l) all_q2k = all_q2k && layers[l].wkv_q2k != nullptr;
-    const bool use_q2k = all_q2k && M == 1 && K <= kGemvMaxK;
+    const bool use_q2k = all_q2k && M >= 1 && M <= kSmallT && K <= kGemvMaxK;
     for (int l = 0; l < L; ++l) {
         const engram_layer &ly = layers[l];
         if (!ly.table || !ly.qk) return ENGRAM_E_NULL;
-        if (!ly.wkv && !use_q2k) return all_q2k && M == 1 ? ENGRAM_E_UNSUPPORTED : ENGRAM_E_NULL;
+        if (!ly.wkv && !use_q2k) return all_q2k && M >= 1 && M <= kSmallT ? ENGRAM_E_UNSUPPORTED : ENGRAM_E_NULL;
         if (ly.wkv_q2k && !aligned(ly.wkv_q2k, 16)) return ENGRAM_E_ALIGN;
         if (ly.rows < 1) return ENGRAM_E_INVALID;
         if (ly.fmt == ENGRAM_FMT_FP8 || ly.fmt == ENGRAM_FMT_FP8_E8M0) {

@@ -170,11 +170,12 @@ typedef struct {
     int64_t rows;           /* table rows (sum of the layer's primes) */
     int32_t fmt;            /* ENGRAM_FMT_FP8, ENGRAM_FMT_Q2K or ENGRAM_FMT_FP8_E8M0 */
     const uint16_t *wkv;    /* [dim * (hc + 1), C * head_dim] bf16; may be NULL when wkv_q2k
-                               is set and every call has batch * T == 1 */
+                               is set and every call has batch * T <= 8 */
     const float *qk;        /* [hc, dim] f32 */
     const uint8_t *wkv_q2k; /* optional [dim * (hc + 1), C * head_dim / 256] Q2_K blocks,
                                16-byte aligned: when every layer has it and C * head_dim
-                               <= 6144, single-token calls project from it */
+                               <= 6144, calls of 1..8 tokens (batch * T) project from it,
+                               bit-identical to the bf16 path on the dequantised blocks */
 } engram_layer;
 
 /* The whole forward for n_layers engram layers (in `layers` order) on one

@@ -50,29 +50,33 @@ def test_project_q2k_bit_identical_to_bf16_on_dequantised(E, K, N):
     assert G.kv_rel_err(_u16(kv_q)[:, rows], want) <= G.KV_TOL
 
 
-def test_forward_wkv_q2k_matches_bf16_path_and_oracle(E):
+@pytest.mark.parametrize("B", [1, 3, 8])
+def test_forward_wkv_q2k_matches_bf16_path_and_oracle(E, B):
+    """Decode steps of B sequences (B tokens a call): the projection from Q2_K
+    wkv gives the bf16 path's kv and highway bit for bit, and the oracle's
+    within tolerance."""
     from deepseek_v4_engram_hash_gb300 import _lib, runner
-    cfg = configs.V41_DECODE_WKVQ2K
-    eng = runner.EngramSetup(cfg, batch=1, max_tokens=1)
+    cfg = configs.V41_DECODE_WKVQ2K.with_(batch=B)
+    eng = runner.EngramSetup(cfg, batch=B, max_tokens=B)
     plain = _lib.layers_array([{k: v for k, v in d.items() if k != "wkv_q2k"} for d in eng.layer_data])
-    hs2 = _lib.Hasher(eng.tables, 1, cfg.max_seq)
-    ref = G.hash_state(cfg, 1)
+    hs2 = _lib.Hasher(eng.tables, B, cfg.max_seq)
+    ref = G.hash_state(cfg, B)
     pos = 0
     for step in range(3):
         ids = torch.from_numpy(eng.ids_for(f"q{step}", 1)).cuda()
-        h0 = synth.highway(cfg, [pos])
+        h0 = synth.highway(cfg, pos * B + np.arange(B))
         d_q = torch.from_numpy(h0).cuda()
         d_b = torch.from_numpy(h0).cuda()
         eng.forward(ids, pos, d_q)                                   # Q2_K wkv
-        kv_q = [_u16(eng.kv(1, l)) for l in range(cfg.n_layers)]
+        kv_q = [_u16(eng.kv(B, l)) for l in range(cfg.n_layers)]
         _lib.engram_forward(hs2, plain, ids, 1, pos, d_b, cfg.eps, eng.ws, eng.ws_bytes)   # bf16 wkv
         assert E.engram_check() == 0
         assert torch.equal(d_q, d_b)
-        want_ids = ref.forward(ids.cpu().numpy(), pos).reshape(1, cfg.n_layers, cfg.cols)
+        want_ids = ref.forward(ids.cpu().numpy(), pos).reshape(B, cfg.n_layers, cfg.cols)
         h = h0
         outs = np.unique(np.concatenate([np.arange(0, cfg.N, 211), [cfg.N - 1]]))
         for l in range(cfg.n_layers):
-            assert np.array_equal(kv_q[l], _u16(eng.kv(1, l)))
+            assert np.array_equal(kv_q[l], _u16(eng.kv(B, l)))
             x = G.x_of(cfg, l, want_ids)
             assert G.kv_rel_err(kv_q[l][:, outs], G.kv(cfg, l, x, outs)) <= G.KV_TOL
             h = G.gate(cfg, l, h, kv_q[l])
