@@ -163,11 +163,17 @@ ODD_Q2K = configs.TINY.with_(
     head_dim=256, scale_block=32, dim=64, hc=1, fmt="q2k", batch=3, T=9, ids="uniform", seed=6)
 
 
-@pytest.mark.parametrize("cfg", [ODD_FP8, ODD_Q2K], ids=lambda c: c.name)
+# N = 40 x 3 = 120: the last 16-row group of wkv holds 8 rows (the GEMV's
+# short last group, the GEMM's partial column tile).
+ODD_N = configs.TINY.with_(name="odd_n", dim=40, hc=2, batch=3, T=7, seed=7)
+
+
+@pytest.mark.parametrize("cfg", [ODD_FP8, ODD_Q2K, ODD_N], ids=lambda c: c.name)
 def test_forward_odd_geometry_all_paths(E, cfg):
-    """Three layers / pad id -1 / 5-grams / 64-wide scale blocks, and Q2_K at
-    C = 5; the call sequence crosses both projection paths (GEMM above 8
-    tokens, fused GEMV at or below) and checks every output."""
+    """Three layers / pad id -1 / 5-grams / 64-wide scale blocks, Q2_K at
+    C = 5, and N = 120 (a short last row group); the call sequence crosses
+    both projection paths (GEMM above 8 tokens, fused GEMV at or below) and
+    checks every output."""
     from deepseek_v4_engram_hash_gb300 import runner
     B = cfg.batch
     eng = runner.EngramSetup(cfg, batch=B, max_tokens=B * cfg.T)
