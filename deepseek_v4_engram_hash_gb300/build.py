@@ -20,7 +20,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                 "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]
 
-ENGRAM_SRCS = ["api.cu", "hash.cu", "rows.cu", "gemv.cu", "gemm.cu", "gemm_simt.cu", "gemm_tc.cu",
+ENGRAM_SRCS = ["api.cu", "hash.cu", "rows.cu", "gemv.cu", "gemm.cu", "gemm_simt.cu", "gemm_tc.cu", "gemm_tc2.cu",
                "gate.cu", "noalloc.cu"]
 SYNTH_SRCS = ["synth.cu"]
 

@@ -298,6 +298,9 @@ cudaError_t launch_gemm(const uint16_t *x, const uint16_t *wkv, uint16_t *kv, in
 bool gemm_tc_supported(int M, int N, int K);
 cudaError_t launch_gemm_tc(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
                            int M, int N, int K, int *err, cudaStream_t s);
+// The same on CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles).
+cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
+                           int M, int N, int K, int *err, cudaStream_t s);
 cudaError_t launch_gemm_simt(const uint16_t *x, const uint16_t *wkv, uint16_t *kv, int M, int N,
                              int K, cudaStream_t s);
 

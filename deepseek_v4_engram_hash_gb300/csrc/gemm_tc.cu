@@ -321,6 +321,7 @@ cudaError_t launch_gemm_tc(int L, const uint16_t *const *x, const uint16_t *cons
                            int M, int N, int K, int *err, cudaStream_t s) {
     using namespace tc;
     if (L < 1 || L > kMaxL) return cudaErrorInvalidValue;
+    if (M >= 256) return launch_gemm_tc2(L, x, wkv, kv, M, N, K, err, s);
     Params p{};
     for (int l = 0; l < L; ++l) {
         if (!make_map(&p.ta[l], x[l], (uint64_t)K, (uint64_t)M, BM)) return cudaErrorInvalidValue;

@@ -1,0 +1,352 @@
+// gemm_tc2.cu -- the prefill wkv projection on CTA pairs (tcgen05 cta_group::2).
+//
+// kv [M, N] = bf16_rne(x [M, K] . wkv [N, K]^T) with f32 accumulation
+// (`linear_bf16`, metrale_model_arch/deepseek_v41_ref/engram.rs), as in
+// gemm_tc.cu, but a cluster of two CTAs computes one 256 x 256 tile: CTA r of
+// the pair holds x rows m0 + 128 r .. +127 and wkv rows n0 + 128 r .. +127 of
+// every 64-wide k step in its own shared memory, and one thread of CTA 0
+// issues tcgen05.mma.cta_group::2 (M 256, N 256, K 16), which reads both
+// CTAs' halves and accumulates each CTA's 128 rows x 256 columns in that CTA's
+// tensor memory.  A CTA stages 32 KB a k step for the same 4.2 MFLOP a CTA
+// that gemm_tc.cu stages 48 KB for, so six stages fit where four did.
+//
+// Roles (6 warps a CTA):
+//   warp 0      TMA producer of this CTA's halves; the copies of both CTAs
+//               complete their bytes on CTA 0's "full" barrier (cta_group::2
+//               copies), whose expected count CTA 0's producer sets;
+//   warp 1      CTA 0: owns the MMA; waits on its full barrier, commits each
+//               stage back to both CTAs' "empty" barriers and each finished
+//               tile to both CTAs' "tfull" barriers.  CTA 1: idle;
+//   warps 2..5  epilogue of this CTA's 128 rows; CTA 0's "tempty" barrier
+//               counts the epilogue warps of both CTAs.
+// Every mbarrier wait is bounded (2 s); on expiry the kernel raises
+// ENGRAM_E_TIMEOUT, every role of both CTAs runs out its loops, and both CTAs
+// meet at the final cluster barrier before the tensor memory is freed.
+#include "common.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+namespace engram {
+
+namespace tc2 {
+
+constexpr int BMC = 128;                            // rows a CTA (M 256 a pair)
+constexpr int BN = 256, BK = 64, STAGES = 6;
+constexpr int kThreads = 192;
+constexpr uint32_t kStageA = BMC * BK * 2;          // 16 KB
+constexpr uint32_t kStageB = (BN / 2) * BK * 2;     // 16 KB: this CTA's half of the wkv tile
+constexpr uint32_t kStageBytes = kStageA + kStageB;
+constexpr int kAcc = 2;                             // accumulators in tensor memory (512 columns)
+constexpr uint32_t kTmemCols = kAcc * BN;
+constexpr int kMaxL = kMaxLayers;
+constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + 256;
+
+struct Params {
+    CUtensorMap ta[kMaxL];
+    CUtensorMap tb[kMaxL];
+    uint16_t *kv[kMaxL];
+    int L, M, N, K;
+    int m_tiles, n_tiles, group_m;                  // m_tiles: 256-row pair tiles
+    int *err;
+};
+
+// 2D tile load into this CTA's shared memory whose bytes complete on an
+// mbarrier of either CTA of the pair (`bar`: a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                                 uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on an mbarrier of either CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Shared-memory matrix descriptor, K-major with the 128-byte swizzle (as in gemm_tc.cu).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1u << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, both
+// K-major, N = 256 (N >> 3 in bits 17..22), M = 256 for the pair (M >> 4 in
+// bits 24..28).
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(2 * BMC >> 4) << 24);
+
+__device__ __forceinline__ void mma_pair(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the mbarrier at this offset in both CTAs of the pair when
+// every MMA issued so far has completed.
+__device__ __forceinline__ void commit_both(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(bar), "h"((uint16_t)0x3)
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tile_coords(int r, int m_tiles, int n_tiles, int group_m, int &mt, int &nt) {
+    const int per_group = group_m * n_tiles;
+    const int g = r / per_group, idx = r % per_group;
+    const int gsz = min(group_m, m_tiles - g * group_m);
+    mt = g * group_m + idx % gsz;
+    nt = idx / gsz;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_tc2_kernel(const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;       // the same offset in both CTAs
+    uint8_t *aux = smem_raw + (base - raw) + STAGES * kStageBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(aux);  // full[S] empty[S] tfull[2] tempty[2] drain
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(aux + (2 * STAGES + 5) * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(aux + (2 * STAGES + 5) * 8 + 4);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t drain = bar0 + 8u * (2 * STAGES + 4);
+
+    const uint32_t rank = cluster_rank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 1);                      // CTA 0's: its producer; bytes of both CTAs
+            mbar_init(empty(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull(a), 1);
+            mbar_init(tempty(a), 8);                    // four epilogue warps in each CTA
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32((const void *)tmem_slot)), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                                     // both CTAs' barriers exist before any remote arrival
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int tiles_per_layer = p.m_tiles * p.n_tiles;
+    const int n_tiles_total = tiles_per_layer * p.L;
+    const int kblocks = p.K / BK;
+    const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int it = 0;
+            for (int tile = pair; tile < n_tiles_total && !*abort_flag; tile += n_pairs) {
+                const int l = tile / tiles_per_layer, r = tile % tiles_per_layer;
+                int mt, nt;
+                tile_coords(r, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+                const int m0 = mt * 2 * BMC + (int)rank * BMC, n0 = nt * BN + (int)rank * (BN / 2);
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait(empty(s), ((it / STAGES) & 1) ^ 1, abort_flag, p.err)) break;
+                    if (rank == 0) mbar_expect_tx(full(s), 2 * kStageBytes);
+                    const uint32_t sa = base + s * kStageBytes, fb = mapa(full(s), 0);
+                    tma_load_2d_pair(sa, &p.ta[l], kb * BK, m0, fb);
+                    tma_load_2d_pair(sa + kStageA, &p.tb[l], kb * BK, n0, fb);
+                }
+            }
+            // Let the copies already issued land before the pair can leave (CTA 0's
+            // full barriers count the bytes of both CTAs).
+            for (int d = 1; rank == 0 && d <= STAGES && it - d >= 0; ++d) {
+                const int last = it - d;
+                const uint64_t t0 = now_ns();
+                while (!mbar_try(full(last % STAGES), (last / STAGES) & 1) && now_ns() - t0 < 10000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            int it = 0, i = 0;
+            for (int tile = pair; tile < n_tiles_total && !*abort_flag; tile += n_pairs, ++i) {
+                const int acc = i % kAcc;
+                if (!mbar_wait(tempty(acc), ((i / kAcc) & 1) ^ 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + acc * BN;
+                bool ok = true;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait(full(s), (it / STAGES) & 1, abort_flag, p.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = base + s * kStageBytes;
+                    const uint64_t da = sdesc(sa), db = sdesc(sa + kStageA);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)                 // +32 bytes = 2 in the address field
+                        mma_pair(d, da + 2u * k, db + 2u * k, (kb | k) != 0);
+                    commit_both(empty(s));
+                }
+                if (!ok) break;
+                commit_both(tfull(acc));
+            }
+            // Drain: every MMA issued so far has finished before the pair can free tensor memory.
+            commit_both(drain);
+            const uint64_t t0 = now_ns();
+            while (!mbar_try(drain, 0) && now_ns() - t0 < 100000000ull) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // Epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 -- rows of this CTA's half.
+        const int q = warp & 3;
+        const int row = (int)rank * BMC + 32 * q + lane;
+        int i = 0;
+        for (int tile = pair; tile < n_tiles_total; tile += n_pairs, ++i) {
+            const int acc = i % kAcc;
+            const bool ok = mbar_wait(tfull(acc), (i / kAcc) & 1, abort_flag, p.err);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;          // reconverge before .sync.aligned loads
+            tc_fence_after();
+            const int l = tile / tiles_per_layer, r = tile % tiles_per_layer;
+            int mt, nt;
+            tile_coords(r, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+            const int m = mt * 2 * BMC + row, n0 = nt * BN;
+            uint16_t *out = p.kv[l] + (size_t)m * p.N;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + acc * BN + c, v);
+                if (m < p.M) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int n = n0 + c + 8 * j;
+                        if (n < p.N) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+                            o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+                            o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+                            o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+                            *reinterpret_cast<uint4 *>(out + n) = o;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa(tempty(acc), 0));
+        }
+    }
+
+    // Both CTAs meet here: no remote arrival, copy or MMA of either is still in flight.
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+}  // namespace tc2
+
+namespace tc {
+bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer);
+}
+
+// L layers: x[l] [M, K] and wkv[l] [N, K] -> kv[l] [M, N], one persistent
+// launch of CTA pairs.
+cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
+                            int M, int N, int K, int *err, cudaStream_t s) {
+    using namespace tc2;
+    if (L < 1 || L > kMaxL || M < 1 || K < BK || K % BK || N < 8 || N % 8) return cudaErrorInvalidValue;
+    Params p{};
+    for (int l = 0; l < L; ++l) {
+        if (!tc::make_map(&p.ta[l], x[l], (uint64_t)K, (uint64_t)M, BMC)) return cudaErrorInvalidValue;
+        if (!tc::make_map(&p.tb[l], wkv[l], (uint64_t)K, (uint64_t)N, BN / 2)) return cudaErrorInvalidValue;
+        p.kv[l] = kv[l];
+    }
+    p.L = L;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.m_tiles = (M + 2 * BMC - 1) / (2 * BMC);
+    p.n_tiles = (N + BN - 1) / BN;
+    // the group rule of gemm_tc.cu in 128-row tiles (all up to 32, else equal
+    // groups of about 24), halved for 256-row pair tiles
+    const int rows128 = 2 * p.m_tiles;
+    int g128 = rows128;
+    if (rows128 > 32) {
+        const int groups = (rows128 + 23) / 24;
+        g128 = (rows128 + groups - 1) / groups;
+    }
+    p.group_m = g128 / 2 > 0 ? g128 / 2 : 1;
+    p.err = err;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    static bool attr[64] = {};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr[dev] = true;
+    }
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int tiles = p.m_tiles * p.n_tiles * L;
+    const int pairs = tiles < sms / 2 ? tiles : sms / 2;
+    gemm_tc2_kernel<<<2 * pairs, kThreads, kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace engram
