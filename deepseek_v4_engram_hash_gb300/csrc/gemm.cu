@@ -1,6 +1,7 @@
-// gemm.cu -- dispatch of the projection GEMM: the tcgen05 tensor-core kernel
-// (gemm_tc.cu) for every shape it takes (K % 64 == 0, N % 8 == 0), the
-// CUDA-core kernel (gemm_simt.cu) otherwise.
+// gemm.cu -- dispatch of the projection GEMM: the tcgen05 tensor-core kernels
+// for every shape they take (K % 64 == 0, N % 8 == 0) -- CTA pairs from 256
+// tokens (gemm_tc2.cu), one CTA below (gemm_tc.cu) -- and the CUDA-core
+// kernel (gemm_simt.cu) otherwise.
 #include "common.cuh"
 
 namespace engram {

@@ -1,4 +1,6 @@
-// gemm_tc.cu -- the prefill wkv projection on the 5th-generation tensor cores.
+// gemm_tc.cu -- the wkv projection on the 5th-generation tensor cores, one
+// CTA a 128 x 256 tile (9..255 tokens; from 256 tokens the CTA-pair kernel of
+// gemm_tc2.cu takes over, bit-identically).
 //
 // kv [M, N] = bf16_rne(x [M, K] . wkv [N, K]^T) with f32 accumulation
 // (`linear_bf16`, metrale_model_arch/deepseek_v41_ref/engram.rs), the dense
@@ -14,22 +16,21 @@
 //               producer and each finished tile to the epilogue;
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, bf16 round, store.
 // The epilogue of tile i overlaps the main loop of tile i + 1.  Tiles are
-// grouped (16 row tiles x all column tiles) so CTAs running together share
-// x row blocks and wkv column blocks through L2.
+// grouped (group_rows128 row tiles x all column tiles) so CTAs running
+// together share x row blocks and wkv column blocks through L2.
 //
 // Every mbarrier wait is bounded (2 s on %globaltimer); on expiry the kernel
 // sets ENGRAM_E_TIMEOUT, lets every role drain, frees its tensor memory and
 // returns.
-#include "common.cuh"
-
-#include <cuda.h>
-#include <cudaTypedefs.h>
+#include "tcgen05.cuh"
 
 namespace engram {
 
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+using namespace tcg;
+
+constexpr int BM = 128, BN = 256, STAGES = 4;
 constexpr int kThreads = 192;
 constexpr uint32_t kStageA = BM * BK * 2;          // 16 KB
 constexpr uint32_t kStageB = BN * BK * 2;          // 32 KB
@@ -55,25 +56,7 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// Shared-memory matrix descriptor, K-major operand with the 128-byte swizzle:
-// rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), the
-// leading byte offset unused for this layout (encoded 1), version 1 in bits
-// 46..47, layout type 2 (SWIZZLE_128B) in bits 61..63.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)1u << 16;
-    d |= (uint64_t)(1024u >> 4) << 32;
-    d |= (uint64_t)1u << 46;
-    d |= (uint64_t)2u << 61;
-    return d;
-}
-
-// Instruction descriptor, kind::f16: f32 accumulator (bits 4..5 = 1), bf16 A
-// and B (bits 7..9 = 1, 10..12 = 1), both K-major, N >> 3 in bits 17..22,
-// M >> 4 in bits 24..28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
 
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
     asm volatile(
@@ -87,50 +70,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Tile order within a layer: groups of group_m row tiles; inside a group,
-// row tiles fastest, then column tiles.  The CTAs running at one time then
-// share a few x row blocks and a few wkv column blocks, both L2-resident, even
-// when x itself is larger than L2.  The host picks group_m (group_m_for).
-__device__ __forceinline__ void tile_coords(int r, int m_tiles, int n_tiles, int group_m, int &mt, int &nt) {
-    const int per_group = group_m * n_tiles;
-    const int g = r / per_group, idx = r % per_group;
-    const int gsz = min(group_m, m_tiles - g * group_m);
-    mt = g * group_m + idx % gsz;
-    nt = idx / gsz;
-}
-
-// All row tiles in one group up to 32 (x of one group <= 50 MB at K = 6144,
-// so wkv streams from DRAM once); beyond, equal groups of about 24.  Measured
-// on one V4.1 layer: 4096 tokens 1.73 PF/s with one group of 32 against 1.69
-// with 16; 12 288 tokens 1.83 PF/s with four groups of 24 against 1.78 with
-// three of 32 and 1.73 with six of 16.
-static int group_m_for(int m_tiles) {
-    if (m_tiles <= 32) return m_tiles < 1 ? 1 : m_tiles;
-    const int groups = (m_tiles + 23) / 24;
-    return (m_tiles + groups - 1) / groups;
-}
-
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -282,10 +221,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
 }
 
+}  // namespace tc
+
+namespace tcg {
+
 // ---------------------------------------------------------------------------
 // Host side: tensor maps through the driver entry point (no -lcuda link).
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void *p = nullptr;
@@ -310,10 +253,12 @@ bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace tc
+bool have_tensor_maps() { return encode_fn() != nullptr; }
+
+}  // namespace tcg
 
 bool gemm_tc_supported(int M, int N, int K) {
-    return M >= 1 && K >= tc::BK && K % tc::BK == 0 && N % 8 == 0 && N >= 8 && tc::encode_fn() != nullptr;
+    return M >= 1 && K >= tcg::BK && K % tcg::BK == 0 && N % 8 == 0 && N >= 8 && tcg::have_tensor_maps();
 }
 
 // L layers: x[l] [M, K] and wkv[l] [N, K] -> kv[l] [M, N], one persistent launch.
@@ -321,6 +266,7 @@ cudaError_t launch_gemm_tc(int L, const uint16_t *const *x, const uint16_t *cons
                            int M, int N, int K, int *err, cudaStream_t s) {
     using namespace tc;
     if (L < 1 || L > kMaxL) return cudaErrorInvalidValue;
+    // 256 tokens and up: 256 x 256 tiles on CTA pairs (gemm_tc2.cu), bit-identical
     if (M >= 256) return launch_gemm_tc2(L, x, wkv, kv, M, N, K, err, s);
     Params p{};
     for (int l = 0; l < L; ++l) {
@@ -334,7 +280,7 @@ cudaError_t launch_gemm_tc(int L, const uint16_t *const *x, const uint16_t *cons
     p.K = K;
     p.m_tiles = (M + BM - 1) / BM;
     p.n_tiles = (N + BN - 1) / BN;
-    p.group_m = group_m_for(p.m_tiles);
+    p.group_m = group_rows128(p.m_tiles);
     p.err = err;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);

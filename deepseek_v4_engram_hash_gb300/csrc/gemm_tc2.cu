@@ -22,17 +22,16 @@
 // Every mbarrier wait is bounded (2 s); on expiry the kernel raises
 // ENGRAM_E_TIMEOUT, every role of both CTAs runs out its loops, and both CTAs
 // meet at the final cluster barrier before the tensor memory is freed.
-#include "common.cuh"
-
-#include <cuda.h>
-#include <cudaTypedefs.h>
+#include "tcgen05.cuh"
 
 namespace engram {
 
 namespace tc2 {
 
+using namespace tcg;
+
 constexpr int BMC = 128;                            // rows a CTA (M 256 a pair)
-constexpr int BN = 256, BK = 64, STAGES = 6;
+constexpr int BN = 256, STAGES = 6;
 constexpr int kThreads = 192;
 constexpr uint32_t kStageA = BMC * BK * 2;          // 16 KB
 constexpr uint32_t kStageB = (BN / 2) * BK * 2;     // 16 KB: this CTA's half of the wkv tile
@@ -80,22 +79,8 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
-// Shared-memory matrix descriptor, K-major with the 128-byte swizzle (as in gemm_tc.cu).
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)1u << 16;
-    d |= (uint64_t)(1024u >> 4) << 32;
-    d |= (uint64_t)1u << 46;
-    d |= (uint64_t)2u << 61;
-    return d;
-}
-
-// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, both
-// K-major, N = 256 (N >> 3 in bits 17..22), M = 256 for the pair (M >> 4 in
-// bits 24..28).
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(2 * BMC >> 4) << 24);
+// M 256 for the pair, N 256.
+constexpr uint32_t kIdesc = idesc_bf16(2 * BMC, BN);
 
 __device__ __forceinline__ void mma_pair(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
     asm volatile(
@@ -113,35 +98,6 @@ __device__ __forceinline__ void commit_both(uint32_t bar) {
         ::"r"(bar), "h"((uint16_t)0x3)
         : "memory");
 }
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tile_coords(int r, int m_tiles, int n_tiles, int group_m, int &mt, int &nt) {
-    const int per_group = group_m * n_tiles;
-    const int g = r / per_group, idx = r % per_group;
-    const int gsz = min(group_m, m_tiles - g * group_m);
-    mt = g * group_m + idx % gsz;
-    nt = idx / gsz;
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -300,10 +256,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace tc2
 
-namespace tc {
-bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_outer);
-}
-
 // L layers: x[l] [M, K] and wkv[l] [N, K] -> kv[l] [M, N], one persistent
 // launch of CTA pairs.
 cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
@@ -312,8 +264,8 @@ cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *con
     if (L < 1 || L > kMaxL || M < 1 || K < BK || K % BK || N < 8 || N % 8) return cudaErrorInvalidValue;
     Params p{};
     for (int l = 0; l < L; ++l) {
-        if (!tc::make_map(&p.ta[l], x[l], (uint64_t)K, (uint64_t)M, BMC)) return cudaErrorInvalidValue;
-        if (!tc::make_map(&p.tb[l], wkv[l], (uint64_t)K, (uint64_t)N, BN / 2)) return cudaErrorInvalidValue;
+        if (!make_map(&p.ta[l], x[l], (uint64_t)K, (uint64_t)M, BMC)) return cudaErrorInvalidValue;
+        if (!make_map(&p.tb[l], wkv[l], (uint64_t)K, (uint64_t)N, BN / 2)) return cudaErrorInvalidValue;
         p.kv[l] = kv[l];
     }
     p.L = L;
@@ -322,15 +274,7 @@ cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *con
     p.K = K;
     p.m_tiles = (M + 2 * BMC - 1) / (2 * BMC);
     p.n_tiles = (N + BN - 1) / BN;
-    // the group rule of gemm_tc.cu in 128-row tiles (all up to 32, else equal
-    // groups of about 24), halved for 256-row pair tiles
-    const int rows128 = 2 * p.m_tiles;
-    int g128 = rows128;
-    if (rows128 > 32) {
-        const int groups = (rows128 + 23) / 24;
-        g128 = (rows128 + groups - 1) / groups;
-    }
-    p.group_m = g128 / 2 > 0 ? g128 / 2 : 1;
+    p.group_m = group_rows128(2 * p.m_tiles) / 2 > 0 ? group_rows128(2 * p.m_tiles) / 2 : 1;   // in pair tiles
     p.err = err;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
