@@ -244,13 +244,15 @@ MAX_GEO = configs.TINY.with_(
 
 
 def test_forward_maximum_geometry(E):
-    """Four layers (the most the kernels take), 16-gram windows (C = 15), hc = 4."""
+    """Four layers (the most the kernels take), 16-gram windows (C = 15), hc = 4;
+    300 tokens take the CTA-pair GEMM with four layers in one launch, a
+    half-empty pair row tile and a 64-column partial column tile (N = 320)."""
     from deepseek_v4_engram_hash_gb300 import runner
     cfg = MAX_GEO
-    eng = runner.EngramSetup(cfg, batch=1, max_tokens=cfg.T)
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=300)
     ref = G.hash_state(cfg, 1)
     pos = 0
-    for T in (cfg.T, 1, 3):
+    for T in (cfg.T, 1, 3, 300):
         ids = eng.ids_for(f"max{pos}", T)
         d_h = _h_device(cfg, pos, T, True)
         _check_call(eng, ref, ids, pos, d_h, d_h.cpu().numpy(), np.arange(T), np.arange(cfg.N), pos)

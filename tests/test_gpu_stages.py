@@ -162,6 +162,32 @@ def test_project_vs_oracle(E, T, K, N):
     assert G.kv_rel_err(_u16(d_kv), want) <= G.KV_TOL
 
 
+@pytest.mark.parametrize("T,N", [(512, 20480), (300, 1040)])
+def test_project_cta_pairs_bit_identical_to_one_cta(E, T, N):
+    """From 256 tokens the projection runs on CTA pairs (256 x 256 tiles); its
+    kv equals, bit for bit, the one-CTA tensor-core GEMM's on the same rows
+    (computed here 250 rows at a time, each call below 256 tokens), and the
+    oracle's within tolerance on sampled rows."""
+    K = 6144
+    rng = np.random.default_rng(T + N)
+    x = synth.to_bf16_bits(rng.standard_normal((T, K)).astype(np.float32))
+    w = synth.to_bf16_bits(0.02 * rng.standard_normal((N, K)).astype(np.float32))
+    d_x = torch.from_numpy(x.view(np.int16)).cuda()
+    d_w = torch.from_numpy(w.view(np.int16)).cuda()
+    kv2 = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    E.engram_project(d_x, d_w, T, K, N, kv2)
+    kv1 = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, T, 250):
+        r1 = min(T, r0 + 250)
+        assert r1 - r0 > 8                           # stays on the GEMM, not the GEMV
+        E.engram_project(d_x[r0:r1].contiguous(), d_w, r1 - r0, K, N, kv1[r0:r1])
+    assert E.engram_check() == 0
+    assert torch.equal(kv1.view(torch.int16), kv2.view(torch.int16))
+    rows = np.unique(np.concatenate([np.arange(0, T, 37), [T - 1]]))
+    want = oracle.linear_bf16(x[rows], w)
+    assert G.kv_rel_err(_u16(kv2)[rows], want) <= G.KV_TOL
+
+
 # ---------------------------------------------------------------- gate ----
 
 @pytest.mark.parametrize("T,hc,D", [(16, 2, 128), (5, 4, 4096), (3, 1, 8), (2, 3, 16384), (7, 4, 1000)])
