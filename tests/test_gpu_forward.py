@@ -167,8 +167,14 @@ ODD_Q2K = configs.TINY.with_(
 # short last group, the GEMM's partial column tile).
 ODD_N = configs.TINY.with_(name="odd_n", dim=40, hc=2, batch=3, T=7, seed=7)
 
+# C = 15 x 20 = 300 columns: 8 tokens are 2400 row ids, more than a GEMV CTA
+# hashes itself, so the hash kernel runs first and the GEMV gathers from the
+# ids in the workspace (4 tokens stay fused); K = 300 x 16 = 4800.
+WIDE_C = configs.TINY.with_(name="wide_c", layer_ids=(3,), max_ngram=16, n_heads=20, prime_target=97,
+                            head_dim=16, scale_block=16, dim=64, hc=1, batch=4, T=12, seed=8)
 
-@pytest.mark.parametrize("cfg", [ODD_FP8, ODD_Q2K, ODD_N], ids=lambda c: c.name)
+
+@pytest.mark.parametrize("cfg", [ODD_FP8, ODD_Q2K, ODD_N, WIDE_C], ids=lambda c: c.name)
 def test_forward_odd_geometry_all_paths(E, cfg):
     """Three layers / pad id -1 / 5-grams / 64-wide scale blocks, Q2_K at
     C = 5, and N = 120 (a short last row group); the call sequence crosses
