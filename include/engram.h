@@ -140,7 +140,8 @@ int engram_rows_q2k(const uint8_t *d_blocks, int64_t R, const int64_t *d_row_ids
  * bf16_rne(sum_i d_x[t, i] * d_wkv[o, i]) with f32 accumulation.
  *   d_x [T, K] bf16, d_wkv [N, K] bf16, d_kv [T, N] bf16; all 16-byte aligned.
  * K % 64 == 0, N % 16 == 0.  T <= 8 with K <= 6144 runs the bandwidth-bound
- * GEMV, anything else the tcgen05 tensor-core GEMM. */
+ * GEMV; otherwise the tcgen05 tensor-core GEMM, on CTA pairs (256 x 256 tiles)
+ * from T = 256 and on single CTAs below, the two bit-identical. */
 int engram_project(const uint16_t *d_x, const uint16_t *d_wkv, int32_t T, int32_t K, int32_t N,
                    uint16_t *d_kv, uintptr_t stream);
 
