@@ -190,7 +190,10 @@ def test_project_cta_pairs_bit_identical_to_one_cta(E, T, N):
 
 # ---------------------------------------------------------------- gate ----
 
-@pytest.mark.parametrize("T,hc,D", [(16, 2, 128), (5, 4, 4096), (3, 1, 8), (2, 3, 16384), (7, 4, 1000)])
+# rows = T x hc: up to 512 the layer-pipelined variant, above it the
+# register-lean one (four CTAs an SM), D from 8 to 16384
+@pytest.mark.parametrize("T,hc,D", [(16, 2, 128), (5, 4, 4096), (3, 1, 8), (2, 3, 16384), (7, 4, 1000),
+                                   (200, 4, 4096), (300, 2, 1000), (129, 4, 16384)])
 def test_gate_vs_oracle(E, T, hc, D):
     rng = np.random.default_rng(T + hc + D)
     h = rng.standard_normal((T, hc, D)).astype(np.float32)
