@@ -26,9 +26,6 @@ __device__ __forceinline__ void set_err(int *err, int code) {
 // ---------------------------------------------------------------------------
 // Number formats
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
-    return __uint_as_float(bits16 << 16);
-}
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

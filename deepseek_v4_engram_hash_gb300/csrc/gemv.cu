@@ -481,9 +481,14 @@ static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
         if (!w || reinterpret_cast<uintptr_t>(w) % 16) return cudaErrorInvalidValue;
     }
     const size_t smem = ring_smem_bytes<WQ2K>();
-    cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<HASH, WQ2K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
+    static bool smem_set[64] = {};                   // per device, per instance
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!smem_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<HASH, WQ2K>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        smem_set[dev] = true;
+    }
     int ctas_per_layer = sms / a.L;
     const int groups = (a.N + 15) / 16;
     if (ctas_per_layer > groups) ctas_per_layer = groups;
