@@ -509,7 +509,7 @@ def main():
                             "peak": bf16_burst, "unit": "TFLOP/s",
                             "frac": gemm_flops(pc, pc.T) / (gemm_ms * 1e-3) / 1e12 / bf16_burst,
                             "peak_source": f"{peak_src} bf16 burst (GEMM timed in short back-to-back steps)",
-                            "kernel": "gemm_tc_kernel (tcgen05, both layers in one launch)"}}
+                            "kernel": "gemm_tc2_kernel (tcgen05 on CTA pairs, both layers in one launch)"}}
 
     others = None
     if rank == 0 and args.only is None and not args.no_others:
