@@ -426,6 +426,28 @@ def oracle_decode_rate(budget_s: float, wkv_host=None):
     return n / t_used, oracle.num_threads(), n
 
 
+def oracle_prefill_rate(n_tokens: int, wkv_host):
+    """Oracle prefill of the first n_tokens of the 4096-token workload on the
+    host cores: projection + gate of both layers timed (hash and row
+    regeneration untimed).  Returns (tokens/s, threads)."""
+    import oracle
+    from deepseek_v4_engram_hash_gb300 import configs, synth
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle_glue as G
+
+    cfg = configs.V41_PREFILL
+    qk = [synth.qk_weights(cfg, l) for l in range(cfg.n_layers)]
+    st = G.hash_state(cfg, 1)
+    rid = st.forward(synth.token_ids(cfg, "prefill.0", cfg.T)[None, :n_tokens], 0)[0]   # [n, L, C]
+    xs = [G.x_of(cfg, l, rid) for l in range(cfg.n_layers)]
+    h = synth.highway(cfg, np.arange(n_tokens))
+    t = time.perf_counter()
+    for l in range(cfg.n_layers):
+        kv = oracle.linear_bf16(xs[l], wkv_host[l])
+        h = oracle.gate(h, kv, qk[l][0], qk[l][1], cfg.hc, cfg.dim, cfg.eps)
+    return n_tokens / (time.perf_counter() - t), oracle.num_threads()
+
+
 def reference_arm(args, rank, world):
     if rank != 0:
         return
@@ -552,10 +574,14 @@ def main():
         oracle.set_num_threads(1)
         rate1, _, n1 = oracle_decode_rate(6.0, wkv_host)
         oracle.set_num_threads(threads)
+        prate, pthreads = oracle_prefill_rate(64, wkv_host)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{n} V4.1 decode steps (T=1) of the plain C oracle, projection + gate of both "
                          f"layers timed; hash and row regeneration untimed",
-               "single_thread": {"value": rate1, "unit": "tokens/s", "cores": 1, "steps": n1}}
+               "single_thread": {"value": rate1, "unit": "tokens/s", "cores": 1, "steps": n1},
+               "prefill": {"value": prate, "unit": "tokens/s", "cores": pthreads,
+                           "sample": "the first 64 tokens of the 4096-token prefill in one call, "
+                                     "projection + gate of both layers timed"}}
 
     if rank == 0:
         line = {
