@@ -180,8 +180,11 @@ typedef struct {
 } engram_layer;
 
 /* The whole forward for n_layers engram layers (in `layers` order) on one
- * highway: one hash launch for every layer (as `V41Runtime.step_hashes`
- * reuses it), then rows -> projection per layer, then the gates.
+ * highway, every layer hashed together (as `V41Runtime.step_hashes` reuses
+ * them).  Up to 8 tokens (batch * T) with C * head_dim <= 6144: one launch
+ * hashes, gathers and projects every layer, then one launch applies every
+ * layer's gate.  Larger calls: the hash launch, the row gather per layer, one
+ * tensor-core GEMM launch for every layer, then the gates.
  *   d_ids [batch, T] int32 at positions start_pos..; d_h [batch * T, hc, dim]
  *   f32 in/out; d_ws device workspace of at least
  *   engram_workspace_bytes(geom, batch * T) bytes, 256-byte aligned.
@@ -255,7 +258,8 @@ size_t engram_workspace_bytes(const engram_geom *geom, int64_t max_tokens);
 
 /* Byte offsets inside the workspace for `tokens` tokens: off[0] = row ids,
  * off[1 + l] = kv of layer l, off[1 + n_layers + l] = gathered rows x of
- * layer l (present only when tokens > 8), off[1 + 2 n_layers] = total bytes.
+ * layer l (present only when the projection runs as a GEMM: tokens > 8, or
+ * C * head_dim > 6144), off[1 + 2 n_layers] = total bytes.
  * off must hold 2 + 2 * n_layers entries. */
 int engram_workspace_layout(const engram_geom *geom, int64_t tokens, size_t *off);
 
