@@ -44,11 +44,41 @@ constexpr size_t kSmemBytes = 1024 + STAGES * kStageBytes + 256;
 struct Params {
     CUtensorMap ta[kMaxL];
     CUtensorMap tb[kMaxL];
+    CUtensorMap tbs[kMaxL];                         // wkv boxes of BN / (2 split) rows (tail sub-tiles)
     uint16_t *kv[kMaxL];
     int L, M, N, K;
     int m_tiles, n_tiles, group_m;                  // m_tiles: 256-row pair tiles
+    int full_per_pair;                              // whole tiles every pair takes first
+    int tail_tiles, split;                          // the last tiles, each cut into `split` column parts
     int *err;
 };
+
+// Work item k of a pair: its whole tiles first (tile pair + k P, P pairs),
+// then column parts u = pair + j P of the last tail_tiles tiles (split parts
+// of BN / split columns each), so the partial last wave is spread over every
+// pair.  A part keeps every output's K order, so results do not depend on it.
+struct Work {
+    int l, mt, nt, n0, width;                      // n0: first column of the item
+};
+__device__ __forceinline__ bool work_item(const Params &p, int pair, int n_pairs, int k, Work &w) {
+    const int tiles_per_layer = p.m_tiles * p.n_tiles;
+    int tile, part = 0;
+    w.width = BN;
+    if (k < p.full_per_pair) {
+        tile = pair + k * n_pairs;
+        if (tile >= tiles_per_layer * p.L) return false;
+    } else {
+        const int u = pair + (k - p.full_per_pair) * n_pairs;
+        if (u >= p.tail_tiles * p.split) return false;
+        tile = p.full_per_pair * n_pairs + u / p.split;
+        part = u % p.split;
+        w.width = BN / p.split;
+    }
+    w.l = tile / tiles_per_layer;
+    tile_coords(tile % tiles_per_layer, p.m_tiles, p.n_tiles, p.group_m, w.mt, w.nt);
+    w.n0 = w.nt * BN + part * w.width;
+    return true;
+}
 
 // 2D tile load into this CTA's shared memory whose bytes complete on an
 // mbarrier of either CTA of the pair (`bar`: a shared::cluster address).
@@ -79,15 +109,14 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
-// M 256 for the pair, N 256.
-constexpr uint32_t kIdesc = idesc_bf16(2 * BMC, BN);
-
-__device__ __forceinline__ void mma_pair(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
+// M 256 for the pair, N = the item's width (256, or a tail part's 128 / 64).
+__device__ __forceinline__ void mma_pair(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
+                                         uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(tmem_d), "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate)
+        ::"r"(tmem_d), "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrive once on the mbarrier at this offset in both CTAs of the pair when
@@ -141,26 +170,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int tiles_per_layer = p.m_tiles * p.n_tiles;
-    const int n_tiles_total = tiles_per_layer * p.L;
     const int kblocks = p.K / BK;
     const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    Work w;
 
     if (warp == 0) {
         if (lane == 0) {
             int it = 0;
-            for (int tile = pair; tile < n_tiles_total && !*abort_flag; tile += n_pairs) {
-                const int l = tile / tiles_per_layer, r = tile % tiles_per_layer;
-                int mt, nt;
-                tile_coords(r, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
-                const int m0 = mt * 2 * BMC + (int)rank * BMC, n0 = nt * BN + (int)rank * (BN / 2);
+            for (int k = 0; work_item(p, pair, n_pairs, k, w) && !*abort_flag; ++k) {
+                const int half = w.width / 2;                 // wkv rows this CTA stages
+                const int m0 = w.mt * 2 * BMC + (int)rank * BMC, n0 = w.n0 + (int)rank * half;
+                const CUtensorMap *mb = w.width == BN ? &p.tb[w.l] : &p.tbs[w.l];
+                const uint32_t bytes = kStageA + (uint32_t)half * BK * 2;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(empty(s), ((it / STAGES) & 1) ^ 1, abort_flag, p.err)) break;
-                    if (rank == 0) mbar_expect_tx(full(s), 2 * kStageBytes);
+                    if (rank == 0) mbar_expect_tx(full(s), 2 * bytes);
                     const uint32_t sa = base + s * kStageBytes, fb = mapa(full(s), 0);
-                    tma_load_2d_pair(sa, &p.ta[l], kb * BK, m0, fb);
-                    tma_load_2d_pair(sa + kStageA, &p.tb[l], kb * BK, n0, fb);
+                    tma_load_2d_pair(sa, &p.ta[w.l], kb * BK, m0, fb);
+                    tma_load_2d_pair(sa + kStageA, mb, kb * BK, n0, fb);
                 }
             }
             // Let the copies already issued land before the pair can leave (CTA 0's
@@ -176,11 +204,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             int it = 0, i = 0;
-            for (int tile = pair; tile < n_tiles_total && !*abort_flag; tile += n_pairs, ++i) {
+            for (int k = 0; work_item(p, pair, n_pairs, k, w) && !*abort_flag; ++k, ++i) {
                 const int acc = i % kAcc;
                 if (!mbar_wait(tempty(acc), ((i / kAcc) & 1) ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + acc * BN;
+                const uint32_t idesc = idesc_bf16(2 * BMC, w.width);
                 bool ok = true;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % STAGES;
@@ -189,8 +218,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t sa = base + s * kStageBytes;
                     const uint64_t da = sdesc(sa), db = sdesc(sa + kStageA);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)                 // +32 bytes = 2 in the address field
-                        mma_pair(d, da + 2u * k, db + 2u * k, (kb | k) != 0);
+                    for (int kk = 0; kk < BK / 16; ++kk)              // +32 bytes = 2 in the address field
+                        mma_pair(d, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
                     commit_both(empty(s));
                 }
                 if (!ok) break;
@@ -208,18 +237,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int row = (int)rank * BMC + 32 * q + lane;
         int i = 0;
-        for (int tile = pair; tile < n_tiles_total; tile += n_pairs, ++i) {
+        for (int k = 0; work_item(p, pair, n_pairs, k, w); ++k, ++i) {
             const int acc = i % kAcc;
             const bool ok = mbar_wait(tfull(acc), (i / kAcc) & 1, abort_flag, p.err);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;          // reconverge before .sync.aligned loads
             tc_fence_after();
-            const int l = tile / tiles_per_layer, r = tile % tiles_per_layer;
-            int mt, nt;
-            tile_coords(r, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
-            const int m = mt * 2 * BMC + row, n0 = nt * BN;
-            uint16_t *out = p.kv[l] + (size_t)m * p.N;
+            const int m = w.mt * 2 * BMC + row, n0 = w.n0;
+            uint16_t *out = p.kv[w.l] + (size_t)m * p.N;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = 0; c < w.width; c += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + acc * BN + c, v);
                 if (m < p.M) {
@@ -289,6 +315,31 @@ cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *con
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int tiles = p.m_tiles * p.n_tiles * L;
     const int pairs = tiles < sms / 2 ? tiles : sms / 2;
+    // The partial last wave: its R tiles cut into `split` column parts (2 or 4)
+    // when that shortens it.  A part still stages the whole 16 KB x tile every k
+    // step, so it is bound by staging, not by its MMA: a half part costs about
+    // 6/8 of a whole tile, a quarter part 5/8 (measured: quarter parts made the
+    // 4096-token GEMM's 52-tile tail slower, the 512-token one's faster).
+    const int R = tiles % pairs;
+    int split = 1, best = R > 0 ? 8 : 0;
+    for (int c = 2; c <= 4 && R > 0; c *= 2) {
+        const int cost = ((R * c + pairs - 1) / pairs) * (c == 2 ? 6 : 5);
+        if (cost < best) {
+            best = cost;
+            split = c;
+        }
+    }
+    p.split = split;
+    if (split > 1) {
+        p.full_per_pair = (tiles - R) / pairs;
+        p.tail_tiles = R;
+        for (int l = 0; l < L; ++l)
+            if (!make_map(&p.tbs[l], wkv[l], (uint64_t)K, (uint64_t)N, (uint32_t)(BN / (2 * split))))
+                return cudaErrorInvalidValue;
+    } else {
+        p.full_per_pair = (tiles + pairs - 1) / pairs;
+        p.tail_tiles = 0;
+    }
     gemm_tc2_kernel<<<2 * pairs, kThreads, kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }

@@ -31,7 +31,7 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
 // Instruction descriptor, kind::f16: f32 accumulator (bits 4..5 = 1), bf16 A
 // and B (bits 7..9 = 1, 10..12 = 1), both K-major, N >> 3 in bits 17..22,
 // M >> 4 in bits 24..28 (M of the whole CTA group).
-constexpr uint32_t idesc_bf16(int M, int N) {
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
