@@ -527,6 +527,8 @@ def main():
         pre = {"workload": pc.name, "tokens_per_step": pc.T, "ms_per_step": p["ms"],
                "value": pc.T / (p["ms"] * 1e-3), "unit": "tokens/s",
                "stage_ms": dict(zip(["hash", "gather", "gemm", "gate"], p["stage_ms"])),
+               "stage_note": "fp8 tables hash inside the row-gather launch: 'hash' is the empty interval "
+                             "before it and 'gather' covers hash and gather of both layers",
                "roofline": {"bound": "tensor", "achieved": gemm_flops(pc, pc.T) / (gemm_ms * 1e-3) / 1e12,
                             "peak": bf16_burst, "unit": "TFLOP/s",
                             "frac": gemm_flops(pc, pc.T) / (gemm_ms * 1e-3) / 1e12 / bf16_burst,

@@ -502,12 +502,21 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
     int64_t *ids = reinterpret_cast<int64_t *>(ws + off[0]);
 
     // Small steps hash inside the projection kernel (each CTA hashes the ids
-    // of its own layer); larger ones run the hash kernel first.
+    // of its own layer); larger fp8 steps hash inside the row gather (one
+    // launch for every layer); the rest run the hash kernel first.
     const bool small = gemv_fits((int)M, K);
     const bool fuse_hash = small && M * C <= kFusedHashMaxIds;
+    HashRowsArgs hr{};
+    hr.L = L;
+    hr.M = M;
+    for (int l = 0; l < L; ++l)
+        hr.layer[l] = RowsArgs{static_cast<const uint8_t *>(layers[l].table), layers[l].scales, layers[l].rows,
+                               hd, g.scale_block, ids + (int64_t)l * C, M, (int64_t)L * C, C,
+                               reinterpret_cast<uint16_t *>(ws + off[1 + L + l]), err, layers[l].fmt};
+    const bool hash_in_rows = !small && hash_rows_supported(hr);
     record(0, s);
     cudaError_t e = cudaSuccess;
-    if (!fuse_hash) {
+    if (!fuse_hash && !hash_in_rows) {
         e = launch_hash(hash_args(hs, d_ids, T, start_pos, ids, d_pos), s);
         if (e != cudaSuccess) return ENGRAM_E_CUDA;
     }
@@ -561,12 +570,15 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
         if ((use_q2k ? launch_gemv_q2k(a, s) : launch_gemv(a, s)) != cudaSuccess) return ENGRAM_E_CUDA;
         record(3, s);
     } else {
-        for (int l = 0; l < L; ++l) {
-            RowsArgs ra{static_cast<const uint8_t *>(layers[l].table), layers[l].scales, layers[l].rows,
-                        hd, g.scale_block, ids + (int64_t)l * C, M, (int64_t)L * C, C,
-                        reinterpret_cast<uint16_t *>(ws + off[1 + L + l]), err, layers[l].fmt};
-            e = layers[l].fmt == ENGRAM_FMT_Q2K ? launch_rows_q2k(ra, s) : launch_rows_fp8(ra, s);
+        if (hash_in_rows) {
+            e = launch_hash_rows(hr, hash_args(hs, d_ids, T, start_pos, ids, d_pos), s);
             if (e != cudaSuccess) return ENGRAM_E_CUDA;
+        } else {
+            for (int l = 0; l < L; ++l) {
+                const RowsArgs &ra = hr.layer[l];
+                e = layers[l].fmt == ENGRAM_FMT_Q2K ? launch_rows_q2k(ra, s) : launch_rows_fp8(ra, s);
+                if (e != cudaSuccess) return ENGRAM_E_CUDA;
+            }
         }
         record(2, s);
         const uint16_t *xs[kMaxLayers], *ws_[kMaxLayers];

@@ -260,6 +260,18 @@ struct RowsArgs {
 cudaError_t launch_rows_fp8(const RowsArgs &a, cudaStream_t s);
 cudaError_t launch_rows_q2k(const RowsArgs &a, cudaStream_t s);
 
+// Hash and fp8 row gather of every layer in one launch: the first thread of a
+// row computes its id (written to hash.out, the cache written as the hash
+// kernel does) and hands it to the row's other threads.  layer[l]: table,
+// scales, R, fmt and out (x of layer l); hd, blk and C from layer[0].
+struct HashRowsArgs {
+    RowsArgs layer[kMaxLayers];
+    int32_t L;
+    int64_t M;              // tokens (B * T)
+};
+bool hash_rows_supported(const HashRowsArgs &a);
+cudaError_t launch_hash_rows(const HashRowsArgs &a, const HashArgs &h, cudaStream_t s);
+
 // Small-T GEMV, optionally with the row gather fused into the x staging.
 struct GemvLayer {
     const uint16_t *wkv;    // [N, K]

@@ -71,6 +71,93 @@ __global__ void __launch_bounds__(256) rows_q2k_kernel(const RowsArgs a) {
     }
 }
 
+// Hash and fp8 gather of every layer in one launch (the larger steps; the
+// hash kernel above is then not launched).  Global row r = (m L + l) C + col,
+// the hash output's order.  A warp takes 32 consecutive rows: lane i hashes
+// row base + i with hash_one (all 32 lanes busy), writes the id and, for
+// (l, col) = (0, 0), the position's cache entry; then the warp gathers the 32
+// rows, 32 / lpr a pass, each thread taking its row's id, layer and x row
+// from the hashing lane by shuffles, the loads of kU passes issued before any
+// conversion.  A device position that does not fit the cache (ENGRAM_E_CAPACITY
+// already raised) reads as id -1: zero rows, no row error on top.
+// head_dim / 16 and scale_block are powers of two, head_dim <= 512.
+// Measured on two V4.1 layers at 4096 tokens (hash + both gathers, against
+// 8 + 2 x 16 us for the hash kernel and two gathers): kU = 2 at 40 registers
+// 36.5 - 38 us; kU = 4 (64 registers) 43 us; kU = 1 43 - 48 us; the row's
+// first thread hashing alone (2 of 32 lanes busy) 57 - 70 us; the rows staged
+// in shared memory by bulk copies, one or two 32-row buffers a warp, 39 - 54 us.
+template <int kU>
+__global__ void __launch_bounds__(256, 6) hash_rows_fp8_kernel(const __grid_constant__ HashRowsArgs r,
+                                                            const __grid_constant__ HashArgs h) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t C = (uint32_t)r.layer[0].C, LC = (uint32_t)r.L * C, T = (uint32_t)h.T;
+    const uint32_t n_rows = (uint32_t)r.M * LC;
+    const int32_t hd = r.layer[0].hd;
+    const int ls = __ffs(hd >> 4) - 1, bs = __ffs(r.layer[0].blk) - 1;
+    const uint32_t per = 32u >> ls;                          // rows a pass
+    const uint32_t sub = lane >> ls, part = lane & ((1u << ls) - 1);
+    const uint32_t sb = (part << 4) >> bs;                   // the thread's scale block in its row
+    const int64_t nblk = hd >> bs;
+    int *err = r.layer[0].err;
+    int64_t sp;
+    const bool ok = hash_start(h, sp);
+    const uint32_t warps = gridDim.x * (blockDim.x >> 5);
+    for (uint32_t base = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32; base < n_rows;
+         base += warps * 32) {
+        const uint32_t row = base + lane;
+        int64_t id = -1;
+        uint32_t li = 0, xrow = 0;
+        if (row < n_rows) {
+            const uint32_t m = row / LC, j = row - m * LC;
+            li = j / C;
+            const uint32_t col = j - li * C;
+            xrow = m * C + col;
+            if (ok) {
+                const uint32_t b = m / T, s = m - b * T;
+                id = hash_one(h, sp, (int)b, (int)s, (int)li, (int)col);
+                if (j == 0) h.cache[(int64_t)b * h.max_seq + sp + s] = hash_compress(h, (int)b, s);
+            }
+            h.out[row] = id;
+        }
+#pragma unroll 1
+        for (uint32_t p0 = 0; p0 < 32; p0 += per * kU) {
+            uint4 v[kU];
+            float sc[kU];
+            uint32_t pl[kU], px[kU];
+            bool live[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const uint32_t i = (p0 + u * per + sub) & 31;   // the row's hashing lane
+                const int64_t rid = __shfl_sync(0xFFFFFFFFu, id, i);
+                pl[u] = __shfl_sync(0xFFFFFFFFu, li, i);
+                px[u] = __shfl_sync(0xFFFFFFFFu, xrow, i);
+                live[u] = p0 + u * per < 32 && base + i < n_rows;
+                const RowsArgs &a = r.layer[pl[u]];
+                v[u] = make_uint4(0, 0, 0, 0);
+                sc[u] = 0.0f;
+                if (live[u] && rid >= 0 && rid < a.R) {
+                    v[u] = __ldg(reinterpret_cast<const uint4 *>(a.table + rid * hd) + part);
+                    sc[u] = fp8_row_scale(a.scales, a.fmt, rid * nblk + sb);
+                } else if (live[u] && ok) {
+                    set_err(err, ENGRAM_E_ROW);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                if (!live[u]) continue;
+                uint4 o0, o1;                                    // zero codes x zero scale: zero rows
+                e4m3x4_scaled_to_bf16(v[u].x, sc[u], o0.x, o0.y);
+                e4m3x4_scaled_to_bf16(v[u].y, sc[u], o0.z, o0.w);
+                e4m3x4_scaled_to_bf16(v[u].z, sc[u], o1.x, o1.y);
+                e4m3x4_scaled_to_bf16(v[u].w, sc[u], o1.z, o1.w);
+                uint4 *dst = reinterpret_cast<uint4 *>(r.layer[pl[u]].out + (size_t)px[u] * hd) + 2 * part;
+                dst[0] = o0;
+                dst[1] = o1;
+            }
+        }
+    }
+}
+
 static unsigned grid_for(int64_t threads_needed) {
     int64_t b = (threads_needed + 255) / 256;
     if (b > 152 * 64) b = 152 * 64;
@@ -104,6 +191,27 @@ static cudaError_t launch_split(const RowsArgs &a, int64_t threads_per_row, int 
 cudaError_t launch_rows_fp8(const RowsArgs &a, cudaStream_t s) {
     if (a.n_tok * a.C == 0) return cudaSuccess;
     return launch_split(a, a.hd >> 4, 1, rows_fp8_kernel, s);
+}
+
+bool hash_rows_supported(const HashRowsArgs &a) {
+    if (a.L < 1 || a.L > kMaxLayers || a.M < 1) return false;
+    const RowsArgs &r0 = a.layer[0];
+    const int lpr = r0.hd >> 4;
+    if (r0.hd % 16 || lpr < 1 || lpr > 32 || (lpr & (lpr - 1)) || r0.blk < 1 || (r0.blk & (r0.blk - 1)) ||
+        r0.hd % r0.blk || r0.C < 1)
+        return false;
+    if (a.M * a.L * (int64_t)r0.C >= ((int64_t)1 << 30)) return false;
+    for (int l = 0; l < a.L; ++l)
+        if (a.layer[l].fmt != ENGRAM_FMT_FP8 && a.layer[l].fmt != ENGRAM_FMT_FP8_E8M0) return false;
+    return true;
+}
+
+cudaError_t launch_hash_rows(const HashRowsArgs &a, const HashArgs &h, cudaStream_t s) {
+    if (!hash_rows_supported(a)) return cudaErrorInvalidValue;
+    const int64_t warps = (a.M * a.L * a.layer[0].C + 31) / 32;
+    const int64_t blocks = (warps + 7) / 8;
+    hash_rows_fp8_kernel<2><<<(unsigned)(blocks < 152 * 64 ? blocks : 152 * 64), 256, 0, s>>>(a, h);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_rows_q2k(const RowsArgs &a, cudaStream_t s) {

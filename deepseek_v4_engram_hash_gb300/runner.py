@@ -92,6 +92,13 @@ class EngramSetup:
         n = tokens * self.cfg.N * 2
         return self.ws[off:off + n].view(torch.bfloat16).view(tokens, self.cfg.N)
 
+    def x(self, tokens: int, layer: int) -> torch.Tensor:
+        """The gathered rows [tokens, K] bf16 of one layer (steps that run the
+        projection as a GEMM keep them in the workspace)."""
+        off = self.workspace_layout(tokens)[1 + self.cfg.n_layers + layer]
+        n = tokens * self.cfg.K * 2
+        return self.ws[off:off + n].view(torch.bfloat16).view(tokens, self.cfg.K)
+
     def forward(self, ids, start_pos: int, d_h, stream=None):
         """ids: [batch, T] int32 (numpy or CUDA tensor); d_h: [batch*T, hc, dim] f32 CUDA."""
         if isinstance(ids, np.ndarray):

@@ -41,9 +41,13 @@ def _check_call(eng, ref, ids, start_pos, d_h, h0_rows, tok_sample, out_sample, 
     got_ids = eng.row_ids(M).cpu().numpy()
     assert np.array_equal(got_ids, want_ids), "row ids"
     h = h0_rows.copy()
+    lay = eng.workspace_layout(M)
+    x_kept = lay[1 + 2 * cfg.n_layers] > lay[1 + cfg.n_layers]     # GEMM steps keep x in the workspace
     for l in range(cfg.n_layers):
         kv_gpu = _u16(eng.kv(M, l))[tok_sample]                     # [S, N]
         x = G.x_of(cfg, l, want_ids[tok_sample])
+        if x_kept:
+            assert np.array_equal(_u16(eng.x(M, l))[tok_sample], x), f"layer {l} x rows"
         want_kv = G.kv(cfg, l, x, out_sample)
         err = G.kv_rel_err(kv_gpu[:, out_sample], want_kv)
         assert err <= G.KV_TOL, f"layer {l} kv rel err {err}"

@@ -60,21 +60,22 @@ def test_graph_replay_bit_identical_to_eager(E, cfg, B, T):
     graph.close()
 
 
-def test_device_position_past_the_cache_is_reported(E):
+@pytest.mark.parametrize("T", [4, 16])      # hash inside the GEMV; hash inside the row gather
+def test_device_position_past_the_cache_is_reported(E, T):
     from deepseek_v4_engram_hash_gb300 import runner
-    cfg = configs.TINY.with_(prefix=0, T=4, decode_steps=0)
-    eng = runner.EngramSetup(cfg, batch=1, max_tokens=4)
+    cfg = configs.TINY.with_(prefix=0, T=T, decode_steps=0)
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=T)
     cache_len = cfg.max_seq
-    d_pos = torch.tensor([cache_len - 2], dtype=torch.int64, device="cuda")     # 2 + 4 > remaining
-    ids = torch.ones((1, 4), dtype=torch.int32, device="cuda")
-    d_h = torch.zeros((4, cfg.hc, cfg.dim), device="cuda")
-    E.engram_forward_dpos(eng.hasher, eng.layers, ids, 4, d_pos, d_h, cfg.eps, eng.ws, eng.ws_bytes)
+    d_pos = torch.tensor([cache_len - 2], dtype=torch.int64, device="cuda")     # 2 + T > remaining
+    ids = torch.ones((1, T), dtype=torch.int32, device="cuda")
+    d_h = torch.zeros((T, cfg.hc, cfg.dim), device="cuda")
+    E.engram_forward_dpos(eng.hasher, eng.layers, ids, T, d_pos, d_h, cfg.eps, eng.ws, eng.ws_bytes)
     assert E.engram_check() == -4
     # a valid call afterwards still hashes exactly (the failed step wrote nothing)
     d_pos.fill_(0)
-    E.engram_forward_dpos(eng.hasher, eng.layers, ids, 4, d_pos, d_h, cfg.eps, eng.ws, eng.ws_bytes)
+    E.engram_forward_dpos(eng.hasher, eng.layers, ids, T, d_pos, d_h, cfg.eps, eng.ws, eng.ws_bytes)
     assert E.engram_check() == 0
     ref = G.hash_state(cfg, 1)
-    assert np.array_equal(eng.row_ids(4).cpu().numpy(),
-                          ref.forward(ids.cpu().numpy(), 0).reshape(4, cfg.n_layers, cfg.cols))
-    assert d_pos.item() == 4
+    assert np.array_equal(eng.row_ids(T).cpu().numpy(),
+                          ref.forward(ids.cpu().numpy(), 0).reshape(T, cfg.n_layers, cfg.cols))
+    assert d_pos.item() == T
