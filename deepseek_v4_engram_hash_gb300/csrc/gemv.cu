@@ -364,7 +364,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     // the first stages need nothing computed: before the wait
     if (producer) issue_until(min(nstages, R::kPrefetch));
 
-    if (a.pdl) {
+    // Hashing here from a host position, the hash and the gather read only the
+    // inputs, the constant tables and the cache entries of earlier steps; the
+    // projection that wrote those had finished before the gate between it and
+    // this grid let this grid launch (every kernel of the step signals its
+    // dependents only after its own wait).  So they run before the wait, beside
+    // the previous step's gate, and only the kv stores (which that gate reads)
+    // wait for it.  A device position is advanced by that gate: wait first.
+    const bool early = HASH && a.hash.start_pos_dev == nullptr;
+    if (a.pdl && !early) {
         griddep_wait();
         griddep_launch();
     }
@@ -393,6 +401,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     uint4 xr[kMmaSubMax][kMmaJ];
     gather_x(a, ly, ids, id_stride, nsub, warp, g, q, xr);
     mma_warps_sync();                      // every warp has read the hashed ids: the partial buffer is free
+    if (a.pdl && early) {
+        griddep_wait();
+        griddep_launch();
+    }
 
     bool live = true;
     // wait for stage i: false (for the whole warp) once the CTA is aborting
