@@ -502,8 +502,9 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
     int64_t *ids = reinterpret_cast<int64_t *>(ws + off[0]);
 
     // Small steps hash inside the projection kernel (each CTA hashes the ids
-    // of its own layer); larger fp8 steps hash inside the row gather (one
-    // launch for every layer); the rest run the hash kernel first.
+    // of its own layer); larger steps hash inside the row gather (one launch
+    // for every layer); the rest (mixed table formats, odd head_dim) run the
+    // hash kernel first.
     const bool small = gemv_fits((int)M, K);
     const bool fuse_hash = small && M * C <= kFusedHashMaxIds;
     HashRowsArgs hr{};

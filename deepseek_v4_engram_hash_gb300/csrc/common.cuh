@@ -260,10 +260,11 @@ struct RowsArgs {
 cudaError_t launch_rows_fp8(const RowsArgs &a, cudaStream_t s);
 cudaError_t launch_rows_q2k(const RowsArgs &a, cudaStream_t s);
 
-// Hash and fp8 row gather of every layer in one launch: the first thread of a
-// row computes its id (written to hash.out, the cache written as the hash
-// kernel does) and hands it to the row's other threads.  layer[l]: table,
-// scales, R, fmt and out (x of layer l); hd, blk and C from layer[0].
+// Hash and row gather (fp8 or Q2_K, the same format in every layer) of every
+// layer in one launch: one lane hashes a row (its id written to hash.out, the
+// cache written as the hash kernel does) and hands the id to the threads that
+// gather the row.  layer[l]: table, scales, R, fmt and out (x of layer l);
+// hd, blk and C from layer[0].
 struct HashRowsArgs {
     RowsArgs layer[kMaxLayers];
     int32_t L;

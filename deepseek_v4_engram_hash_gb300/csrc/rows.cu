@@ -71,6 +71,33 @@ __global__ void __launch_bounds__(256) rows_q2k_kernel(const RowsArgs a) {
     }
 }
 
+// The id of global row `row` = (m L + l) C + col of a fused hash + gather
+// launch, hashed by one lane: writes it to the workspace and, for
+// (l, col) = (0, 0), the position's cache entry; li and xrow = m C + col give
+// the row's layer and its row in that layer's x.  A row past the end, or a
+// device position that does not fit the cache (ok false, ENGRAM_E_CAPACITY
+// already raised), reads as id -1.
+__device__ __forceinline__ int64_t fused_row_id(const HashRowsArgs &r, const HashArgs &h, bool ok, int64_t sp,
+                                                uint32_t row, uint32_t &li, uint32_t &xrow) {
+    const uint32_t C = (uint32_t)r.layer[0].C, LC = (uint32_t)r.L * C, T = (uint32_t)h.T;
+    int64_t id = -1;
+    li = 0;
+    xrow = 0;
+    if (row < (uint32_t)r.M * LC) {
+        const uint32_t m = row / LC, j = row - m * LC;
+        li = j / C;
+        const uint32_t col = j - li * C;
+        xrow = m * C + col;
+        if (ok) {
+            const uint32_t b = m / T, s = m - b * T;
+            id = hash_one(h, sp, (int)b, (int)s, (int)li, (int)col);
+            if (j == 0) h.cache[(int64_t)b * h.max_seq + sp + s] = hash_compress(h, (int)b, s);
+        }
+        h.out[row] = id;
+    }
+    return id;
+}
+
 // Hash and fp8 gather of every layer in one launch (the larger steps; the
 // hash kernel above is then not launched).  Global row r = (m L + l) C + col,
 // the hash output's order.  A warp takes 32 consecutive rows: lane i hashes
@@ -90,8 +117,7 @@ template <int kU>
 __global__ void __launch_bounds__(256, 6) hash_rows_fp8_kernel(const __grid_constant__ HashRowsArgs r,
                                                             const __grid_constant__ HashArgs h) {
     const uint32_t lane = threadIdx.x & 31;
-    const uint32_t C = (uint32_t)r.layer[0].C, LC = (uint32_t)r.L * C, T = (uint32_t)h.T;
-    const uint32_t n_rows = (uint32_t)r.M * LC;
+    const uint32_t n_rows = (uint32_t)r.M * (uint32_t)r.L * (uint32_t)r.layer[0].C;
     const int32_t hd = r.layer[0].hd;
     const int ls = __ffs(hd >> 4) - 1, bs = __ffs(r.layer[0].blk) - 1;
     const uint32_t per = 32u >> ls;                          // rows a pass
@@ -104,21 +130,8 @@ __global__ void __launch_bounds__(256, 6) hash_rows_fp8_kernel(const __grid_cons
     const uint32_t warps = gridDim.x * (blockDim.x >> 5);
     for (uint32_t base = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32; base < n_rows;
          base += warps * 32) {
-        const uint32_t row = base + lane;
-        int64_t id = -1;
-        uint32_t li = 0, xrow = 0;
-        if (row < n_rows) {
-            const uint32_t m = row / LC, j = row - m * LC;
-            li = j / C;
-            const uint32_t col = j - li * C;
-            xrow = m * C + col;
-            if (ok) {
-                const uint32_t b = m / T, s = m - b * T;
-                id = hash_one(h, sp, (int)b, (int)s, (int)li, (int)col);
-                if (j == 0) h.cache[(int64_t)b * h.max_seq + sp + s] = hash_compress(h, (int)b, s);
-            }
-            h.out[row] = id;
-        }
+        uint32_t li, xrow;
+        const int64_t id = fused_row_id(r, h, ok, sp, base + lane, li, xrow);
 #pragma unroll 1
         for (uint32_t p0 = 0; p0 < 32; p0 += per * kU) {
             uint4 v[kU];
@@ -153,6 +166,57 @@ __global__ void __launch_bounds__(256, 6) hash_rows_fp8_kernel(const __grid_cons
                 uint4 *dst = reinterpret_cast<uint4 *>(r.layer[pl[u]].out + (size_t)px[u] * hd) + 2 * part;
                 dst[0] = o0;
                 dst[1] = o1;
+            }
+        }
+    }
+}
+
+// Hash and Q2_K gather of every layer in one launch: a warp takes RB
+// consecutive rows (RB <= 32), lanes 0 .. RB-1 hash one each; then the warp
+// decodes the RB rows one at a time as rows_q2k_kernel does (lanes 0..20 hold
+// the block's words), the words of kU rows loaded before any decode.  With
+// 84-byte rows the gather moves little data, so fewer rows a warp (more
+// warps) hide more of the load latency.  Measured on two V4.1 layers at 512
+// tokens (hash + gathers 23 us as two kernels): RB = 8 with kU = 8 12.7 -
+// 13.0 us; RB 8, kU 4 13.6; RB 8, kU 2 14.1 - 14.7; RB 4 13.8; RB 16 16.6.
+template <int RB, int kU>
+__global__ void __launch_bounds__(256) hash_rows_q2k_kernel(const __grid_constant__ HashRowsArgs r,
+                                                            const __grid_constant__ HashArgs h) {
+    static_assert(RB % kU == 0 && RB <= 32, "RB rows in passes of kU");
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t n_rows = (uint32_t)r.M * (uint32_t)r.L * (uint32_t)r.layer[0].C;
+    int *err = r.layer[0].err;
+    int64_t sp;
+    const bool ok = hash_start(h, sp);
+    const uint32_t warps = gridDim.x * (blockDim.x >> 5);
+    for (uint32_t base = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RB; base < n_rows;
+         base += warps * RB) {
+        uint32_t li = 0, xrow = 0;
+        int64_t id = -1;
+        if (lane < (uint32_t)RB) id = fused_row_id(r, h, ok, sp, base + lane, li, xrow);
+#pragma unroll 1
+        for (int p0 = 0; p0 < RB; p0 += kU) {
+            uint32_t word[kU], px[kU], pl[kU];
+            bool live[kU], valid[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = p0 + u;                              // the row's hashing lane
+                const int64_t rid = __shfl_sync(0xFFFFFFFFu, id, i);
+                pl[u] = __shfl_sync(0xFFFFFFFFu, li, i);
+                px[u] = __shfl_sync(0xFFFFFFFFu, xrow, i);
+                live[u] = base + i < n_rows;
+                const RowsArgs &a = r.layer[pl[u]];
+                valid[u] = live[u] && rid >= 0 && rid < a.R;
+                if (live[u] && !valid[u] && ok && lane == 0) set_err(err, ENGRAM_E_ROW);
+                word[u] = valid[u] && lane < 21 ? __ldg(reinterpret_cast<const uint32_t *>(a.table + rid * 84) + lane)
+                                                : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                if (!live[u]) continue;                            // the same for the whole warp
+                uint4 o = q2k_lane_decode(word[u], (int)lane);
+                if (!valid[u]) o = make_uint4(0, 0, 0, 0);
+                reinterpret_cast<uint4 *>(r.layer[pl[u]].out + (size_t)px[u] * 256)[lane] = o;
             }
         }
     }
@@ -193,24 +257,34 @@ cudaError_t launch_rows_fp8(const RowsArgs &a, cudaStream_t s) {
     return launch_split(a, a.hd >> 4, 1, rows_fp8_kernel, s);
 }
 
+// fp8 (f32 or e8m0 scales) in every layer, head_dim / 16 and scale_block
+// powers of two, head_dim <= 512; or Q2_K (head_dim 256) in every layer.
 bool hash_rows_supported(const HashRowsArgs &a) {
     if (a.L < 1 || a.L > kMaxLayers || a.M < 1) return false;
     const RowsArgs &r0 = a.layer[0];
+    if (r0.C < 1 || a.M * a.L * (int64_t)r0.C >= ((int64_t)1 << 30)) return false;
+    bool fp8 = true, q2k = r0.hd == 256;
+    for (int l = 0; l < a.L; ++l) {
+        fp8 = fp8 && (a.layer[l].fmt == ENGRAM_FMT_FP8 || a.layer[l].fmt == ENGRAM_FMT_FP8_E8M0);
+        q2k = q2k && a.layer[l].fmt == ENGRAM_FMT_Q2K;
+    }
+    if (q2k) return true;
     const int lpr = r0.hd >> 4;
-    if (r0.hd % 16 || lpr < 1 || lpr > 32 || (lpr & (lpr - 1)) || r0.blk < 1 || (r0.blk & (r0.blk - 1)) ||
-        r0.hd % r0.blk || r0.C < 1)
-        return false;
-    if (a.M * a.L * (int64_t)r0.C >= ((int64_t)1 << 30)) return false;
-    for (int l = 0; l < a.L; ++l)
-        if (a.layer[l].fmt != ENGRAM_FMT_FP8 && a.layer[l].fmt != ENGRAM_FMT_FP8_E8M0) return false;
-    return true;
+    return fp8 && r0.hd % 16 == 0 && lpr >= 1 && lpr <= 32 && (lpr & (lpr - 1)) == 0 && r0.blk >= 1 &&
+           (r0.blk & (r0.blk - 1)) == 0 && r0.hd % r0.blk == 0;
 }
 
 cudaError_t launch_hash_rows(const HashRowsArgs &a, const HashArgs &h, cudaStream_t s) {
     if (!hash_rows_supported(a)) return cudaErrorInvalidValue;
-    const int64_t warps = (a.M * a.L * a.layer[0].C + 31) / 32;
-    const int64_t blocks = (warps + 7) / 8;
-    hash_rows_fp8_kernel<2><<<(unsigned)(blocks < 152 * 64 ? blocks : 152 * 64), 256, 0, s>>>(a, h);
+    const int64_t n_rows = a.M * a.L * a.layer[0].C;
+    auto grid = [](int64_t warps) {
+        const int64_t blocks = (warps + 7) / 8;
+        return (unsigned)(blocks < 152 * 64 ? blocks : 152 * 64);
+    };
+    if (a.layer[0].fmt == ENGRAM_FMT_Q2K)
+        hash_rows_q2k_kernel<8, 8><<<grid((n_rows + 7) / 8), 256, 0, s>>>(a, h);
+    else
+        hash_rows_fp8_kernel<2><<<grid((n_rows + 31) / 32), 256, 0, s>>>(a, h);
     return cudaGetLastError();
 }
 
