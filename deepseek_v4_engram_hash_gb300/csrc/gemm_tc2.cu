@@ -8,7 +8,9 @@
 // issues tcgen05.mma.cta_group::2 (M 256, N 256, K 16), which reads both
 // CTAs' halves and accumulates each CTA's 128 rows x 256 columns in that CTA's
 // tensor memory.  A CTA stages 32 KB a k step for the same 4.2 MFLOP a CTA
-// that gemm_tc.cu stages 48 KB for, so six stages fit where four did.
+// that gemm_tc.cu stages 48 KB for, so seven stages fit where four did
+// (seven against six: 1012 against 1017 us at 4096 tokens, 165 against 167 us
+// at 512).
 //
 // Roles (6 warps a CTA):
 //   warp 0      TMA producer of this CTA's halves; the copies of both CTAs
@@ -31,7 +33,7 @@ namespace tc2 {
 using namespace tcg;
 
 constexpr int BMC = 128;                            // rows a CTA (M 256 a pair)
-constexpr int BN = 256, STAGES = 6;
+constexpr int BN = 256, STAGES = 7;            // 7 x 32 KB ring: 230.7 KB of shared memory
 constexpr int kThreads = 192;
 constexpr uint32_t kStageA = BMC * BK * 2;          // 16 KB
 constexpr uint32_t kStageB = (BN / 2) * BK * 2;     // 16 KB: this CTA's half of the wkv tile
