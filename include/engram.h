@@ -183,8 +183,11 @@ typedef struct {
  * highway, every layer hashed together (as `V41Runtime.step_hashes` reuses
  * them).  Up to 8 tokens (batch * T) with C * head_dim <= 6144: one launch
  * hashes, gathers and projects every layer, then one launch applies every
- * layer's gate.  Larger calls: the hash launch, the row gather per layer, one
- * tensor-core GEMM launch for every layer, then the gates.
+ * layer's gate.  Larger calls: one launch hashes and gathers the rows of
+ * every layer (when every layer's table has the same format and, for fp8,
+ * head_dim / 16 and scale_block are powers of two; otherwise the hash launch
+ * and one row-gather launch per layer), one tensor-core GEMM launch for every
+ * layer, then the gates.
  *   d_ids [batch, T] int32 at positions start_pos..; d_h [batch * T, hc, dim]
  *   f32 in/out; d_ws device workspace of at least
  *   engram_workspace_bytes(geom, batch * T) bytes, 256-byte aligned.
