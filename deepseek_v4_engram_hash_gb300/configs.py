@@ -37,6 +37,11 @@ class EngramConfig:
     eps: float = 1e-6
     decode_steps: int = 0        # single-token steps after the prefill
     wkv_fmt: str = "bf16"        # "q2k": wkv also held as Q2_K blocks (its bf16 form is their dequantisation)
+    layer_fmts: tuple = ()       # per-layer table formats overriding `fmt` (mixed-format tests)
+
+    def fmt_of(self, layer: int) -> str:
+        """The table format of layer `layer`."""
+        return self.layer_fmts[layer] if self.layer_fmts else self.fmt
 
     @property
     def n_layers(self) -> int:

@@ -35,13 +35,14 @@ class EngramSetup:
             for l in range(cfg.n_layers):
                 R = t["rows_per_layer"][l]
                 d = {"rows": R}
-                if cfg.fmt in ("fp8", "fp8_e8m0"):
+                fmt = cfg.fmt_of(l)
+                if fmt in ("fp8", "fp8_e8m0"):
                     d["table"] = torch.empty((R, cfg.head_dim), dtype=torch.uint8, device=self.device)
                     d["scales"] = torch.empty((R, cfg.head_dim // cfg.scale_block), dtype=torch.float32,
                                               device=self.device)
                     synth.fill_table_fp8_cuda(cfg, l, d["table"], d["scales"])
                     d["fmt"] = E.ENGRAM_FMT_FP8
-                    if cfg.fmt == "fp8_e8m0":
+                    if fmt == "fp8_e8m0":
                         # the scales are exact powers of two: store their biased exponent bytes
                         d["scales"] = ((d["scales"].view(torch.int32) >> 23) & 0xFF).to(torch.uint8)
                         d["fmt"] = E.ENGRAM_FMT_FP8_E8M0

@@ -22,10 +22,11 @@ def rows(cfg, layer, ids) -> np.ndarray:
     """Dequantised rows [len(ids), hd] (bf16 bits) of layer `layer` for row ids `ids`."""
     ids = np.asarray(ids, dtype=np.int64).ravel()
     uniq, inv = np.unique(ids, return_inverse=True)
-    if cfg.fmt == "fp8":
+    fmt = cfg.fmt_of(layer)
+    if fmt == "fp8":
         codes, scales = synth.table_fp8_rows(cfg, layer, uniq)
         return oracle.rows_fp8(codes, scales, cfg.head_dim, cfg.scale_block, inv)
-    if cfg.fmt == "fp8_e8m0":
+    if fmt == "fp8_e8m0":
         codes, scales = synth.table_fp8_rows(cfg, layer, uniq)
         e8 = ((scales.view(np.int32) >> 23) & 0xFF).astype(np.uint8)      # exact powers of two
         return oracle.rows_fp8_e8m0(codes, e8, cfg.head_dim, cfg.scale_block, inv)

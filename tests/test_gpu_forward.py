@@ -178,12 +178,21 @@ WIDE_C = configs.TINY.with_(name="wide_c", layer_ids=(3,), max_ngram=16, n_heads
                             head_dim=16, scale_block=16, dim=64, hc=1, batch=4, T=12, seed=8)
 
 
-@pytest.mark.parametrize("cfg", [ODD_FP8, ODD_Q2K, ODD_N, WIDE_C], ids=lambda c: c.name)
+# Table formats differing between layers: fp8, Q2_K and e8m0 layers (the
+# larger steps then hash in their own launch and gather layer by layer), and
+# f32 beside e8m0 scales (one fused hash + gather launch reading both).
+MIXED_Q2K = configs.TINY.with_(name="mixed_q2k", layer_ids=(1, 4, 7), head_dim=256, scale_block=32,
+                               layer_fmts=("fp8", "q2k", "fp8_e8m0"), batch=2, T=11, seed=9)
+MIXED_E8M0 = configs.TINY.with_(name="mixed_e8m0", layer_ids=(2, 5), head_dim=128, scale_block=16,
+                                layer_fmts=("fp8_e8m0", "fp8"), batch=2, T=13, seed=10)
+
+
+@pytest.mark.parametrize("cfg", [ODD_FP8, ODD_Q2K, ODD_N, WIDE_C, MIXED_Q2K, MIXED_E8M0], ids=lambda c: c.name)
 def test_forward_odd_geometry_all_paths(E, cfg):
     """Three layers / pad id -1 / 5-grams / 64-wide scale blocks, Q2_K at
-    C = 5, and N = 120 (a short last row group); the call sequence crosses
-    both projection paths (GEMM above 8 tokens, fused GEMV at or below) and
-    checks every output."""
+    C = 5, N = 120 (a short last row group), and table formats that differ
+    between layers; the call sequence crosses both projection paths (GEMM
+    above 8 tokens, fused GEMV at or below) and checks every output."""
     from deepseek_v4_engram_hash_gb300 import runner
     B = cfg.batch
     eng = runner.EngramSetup(cfg, batch=B, max_tokens=B * cfg.T)
