@@ -1,4 +1,6 @@
-// rows.cu -- table row gather and dequantisation (stage 2), standalone.
+// rows.cu -- table row gather and dequantisation (stage 2): the standalone
+// row kernels (engram_rows_*), and the prefill kernels that hash (stage 1)
+// and gather every layer's rows in one launch.
 //
 // fp8: `regen_table` + `embed_rows` on metrale_model_arch/deepseek_v41_ref/engram.rs:
 //   row(id)[d] = bf16_rne(e4m3(table[id, d]) * scales[id, d / blk]).
