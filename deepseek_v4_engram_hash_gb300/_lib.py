@@ -37,7 +37,8 @@ class engram_geom(ctypes.Structure):
 class engram_layer(ctypes.Structure):
     _fields_ = [("table", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("fmt", ctypes.c_int32),
-                ("wkv", ctypes.c_void_p), ("qk", ctypes.c_void_p), ("wkv_q2k", ctypes.c_void_p)]
+                ("wkv", ctypes.c_void_p), ("qk", ctypes.c_void_p), ("wkv_q2k", ctypes.c_void_p),
+                ("wkv_tiled", ctypes.c_void_p)]
 
 
 _lib = None
@@ -66,6 +67,8 @@ def lib() -> ctypes.CDLL:
             "engram_project": ([P, P, i32, i32, i32, P, st], ctypes.c_int),
             "engram_gate": ([P, P, P, i32, i32, i32, ctypes.c_float, st], ctypes.c_int),
             "engram_project_q2k": ([P, P, i32, i32, P, st], ctypes.c_int),
+            "engram_tiled_wkv_bytes": ([i32, i32], ctypes.c_size_t),
+            "engram_tile_wkv": ([P, i32, i32, P, st], ctypes.c_int),
             "engram_forward": ([P, ctypes.POINTER(engram_layer), P, i32, i64, P, ctypes.c_float,
                                 P, sz, st], ctypes.c_int),
             "engram_forward_host": ([P, ctypes.POINTER(engram_layer), P, P, i32, i64, P, P,
@@ -212,6 +215,14 @@ def engram_project_q2k(d_x, d_wkv_q2k, K, N, d_kv, stream=None):
         "engram_project_q2k")
 
 
+def engram_tiled_wkv_bytes(N, K) -> int:
+    return int(lib().engram_tiled_wkv_bytes(int(N), int(K)))
+
+
+def engram_tile_wkv(d_wkv, N, K, d_tiled, stream=None):
+    _ok(lib().engram_tile_wkv(_ptr(d_wkv), int(N), int(K), _ptr(d_tiled), _stream(stream)), "engram_tile_wkv")
+
+
 def engram_gate(d_h, d_kv, d_qk, T, hc, dim, eps, stream=None):
     _ok(lib().engram_gate(_ptr(d_h), _ptr(d_kv), _ptr(d_qk), int(T), int(hc), int(dim), float(eps),
                           _stream(stream)), "engram_gate")
@@ -223,7 +234,7 @@ def layers_array(layers) -> ctypes.Array:
     for i, ly in enumerate(layers):
         arr[i] = engram_layer(_ptr(ly["table"]).value, _ptr(ly.get("scales")).value, int(ly["rows"]),
                               int(ly["fmt"]), _ptr(ly.get("wkv")).value, _ptr(ly["qk"]).value,
-                              _ptr(ly.get("wkv_q2k")).value)
+                              _ptr(ly.get("wkv_q2k")).value, _ptr(ly.get("wkv_tiled")).value)
     return arr
 
 

@@ -401,6 +401,22 @@ int engram_project_q2k(const uint16_t *d_x, const uint8_t *d_wkv_q2k, int32_t K,
     return cuda_rc(launch_gemv_q2k(a, S(stream)));
 }
 
+size_t engram_tiled_wkv_bytes(int32_t N, int32_t K) {
+    if (N < 1 || K < 8 || K % 8) return 0;
+    const size_t groups = ((size_t)N + kTileRows - 1) / kTileRows, chunks = ((size_t)K + kTileCols - 1) / kTileCols;
+    return groups * chunks * kTileRows * kTileCols * sizeof(uint16_t);
+}
+
+int engram_tile_wkv(const uint16_t *d_wkv, int32_t N, int32_t K, uint16_t *d_tiled, uintptr_t stream) {
+    if (!d_wkv || !d_tiled) return ENGRAM_E_NULL;
+    if (N < 1 || K < 8 || K % 8) return ENGRAM_E_INVALID;
+    if (!aligned(d_wkv, 16) || !aligned(d_tiled, 16)) return ENGRAM_E_ALIGN;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(d_wkv), a1 = a0 + (size_t)N * K * 2;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(d_tiled), b1 = b0 + engram_tiled_wkv_bytes(N, K);
+    if (a0 < b1 && b0 < a1) return ENGRAM_E_INVALID;        // overlapping buffers
+    return cuda_rc(launch_tile_wkv(d_wkv, N, K, d_tiled, S(stream)));
+}
+
 int engram_gate(float *d_h, const uint16_t *d_kv, const float *d_qk, int32_t T, int32_t hc, int32_t dim,
                 float eps, uintptr_t stream) {
     if (!d_h || !d_kv || !d_qk) return ENGRAM_E_NULL;
@@ -476,6 +492,7 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
         if (!ly.table || !ly.qk) return ENGRAM_E_NULL;
         if (!ly.wkv && !use_q2k) return all_q2k && M >= 1 && M <= kSmallT ? ENGRAM_E_UNSUPPORTED : ENGRAM_E_NULL;
         if (ly.wkv_q2k && !aligned(ly.wkv_q2k, 16)) return ENGRAM_E_ALIGN;
+        if (ly.wkv_tiled && !aligned(ly.wkv_tiled, 16)) return ENGRAM_E_ALIGN;
         if (ly.rows < 1) return ENGRAM_E_INVALID;
         if (ly.fmt == ENGRAM_FMT_FP8 || ly.fmt == ENGRAM_FMT_FP8_E8M0) {
             if (!ly.scales) return ENGRAM_E_NULL;
@@ -545,6 +562,7 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
         GemvArgs a{};
         for (int l = 0; l < L; ++l) {
             a.layer[l].wkv = layers[l].wkv;
+            a.layer[l].wkv_tiled = layers[l].wkv_tiled;
             a.layer[l].wkv_q2k = layers[l].wkv_q2k;
             a.layer[l].kv = reinterpret_cast<uint16_t *>(ws + off[1 + l]);
             a.layer[l].table = static_cast<const uint8_t *>(layers[l].table);

@@ -276,6 +276,7 @@ cudaError_t launch_hash_rows(const HashRowsArgs &a, const HashArgs &h, cudaStrea
 // Small-T GEMV, optionally with the row gather fused into the x staging.
 struct GemvLayer {
     const uint16_t *wkv;    // [N, K]
+    const uint16_t *wkv_tiled;  // the same in 16 x 2048 tiles (engram_tile_wkv), or null
     const uint8_t *wkv_q2k; // [N, K / 256] Q2_K blocks (the q2k launch reads these instead)
     uint16_t *kv;           // [T, N]
     const uint16_t *x;      // plain x [T, K] (gather == 0)
@@ -301,6 +302,9 @@ constexpr int kGemvMaxK = 6144;         // widest x the 1..8-token GEMV holds in
 cudaError_t launch_gemv(const GemvArgs &a, cudaStream_t s);
 cudaError_t launch_gemv_q2k(const GemvArgs &a, cudaStream_t s);   // one token, Q2_K wkv
 size_t gemv_smem_bytes(int T, int K);
+// wkv [N, K] -> 16-row x 2048-column tiles, g-major (the engram_tile_wkv layout).
+constexpr int kTileRows = 16, kTileCols = 2048;
+cudaError_t launch_tile_wkv(const uint16_t *wkv, int N, int K, uint16_t *tiled, cudaStream_t s);
 
 // GEMM: kv [M, N] = bf16(x [M, K] . wkv [N, K]^T).
 cudaError_t launch_gemm(const uint16_t *x, const uint16_t *wkv, uint16_t *kv, int M, int N, int K,

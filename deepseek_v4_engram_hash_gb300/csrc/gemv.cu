@@ -358,8 +358,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
                 const int r0 = grp * 16, nrows = min(16, N - r0);
                 if (lane == 0) mbar_expect_tx(full(b), bytes * (uint32_t)nrows);
                 __syncwarp();
-                if (lane < nrows)
-                    bulk_load(dst + lane * kRowBytes, ly.wkv + (size_t)(r0 + lane) * K + kb0 * 32, bytes, full(b), pol);
+                // row r0 + lane, columns kb0 * 32 ..: from the tiled copy (the group's
+                // piece is one contiguous 64 KB tile) or from row-major wkv
+                const uint16_t *src =
+                    ly.wkv_tiled ? ly.wkv_tiled + ((size_t)(grp * nsub + i % nsub) * kTileRows + lane) * kTileCols
+                                 : ly.wkv + (size_t)(r0 + lane) * K + kb0 * 32;
+                if (lane < nrows) bulk_load(dst + lane * kRowBytes, src, bytes, full(b), pol);
             }
         }
     };
@@ -518,6 +522,37 @@ static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<HASH, WQ2K>, a);
+}
+
+static_assert(kStageKb * 32 == kTileCols && kTileRows == 16, "a bf16 ring stage is one tile of engram_tile_wkv");
+
+// The engram_tile_wkv layout: one thread a 16-byte piece of the output, read
+// from the row-major weights (K % 8 == 0), zero past the last row or column.
+__global__ void __launch_bounds__(256) tile_wkv_kernel(const uint16_t *__restrict__ wkv, int N, int K,
+                                                       uint16_t *__restrict__ tiled, int64_t pieces) {
+    const int nchunks = (K + kTileCols - 1) / kTileCols;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < pieces;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int j8 = (int)(e % (kTileCols / 8));
+        const int64_t row_of_tiles = e / (kTileCols / 8);       // (g * nchunks + c) * 16 + r
+        const int r = (int)(row_of_tiles % kTileRows);
+        const int64_t gc = row_of_tiles / kTileRows;
+        const int c = (int)(gc % nchunks);
+        const int64_t n = (gc / nchunks) * kTileRows + r;
+        const int k = c * kTileCols + 8 * j8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (n < N && k < K) v = *reinterpret_cast<const uint4 *>(wkv + n * K + k);
+        reinterpret_cast<uint4 *>(tiled)[e] = v;
+    }
+}
+
+cudaError_t launch_tile_wkv(const uint16_t *wkv, int N, int K, uint16_t *tiled, cudaStream_t s) {
+    const int64_t groups = (N + kTileRows - 1) / kTileRows, nchunks = (K + kTileCols - 1) / kTileCols;
+    const int64_t pieces = groups * nchunks * kTileRows * (kTileCols / 8);
+    if (pieces == 0) return cudaSuccess;
+    const int64_t blocks = (pieces + 255) / 256;
+    tile_wkv_kernel<<<(unsigned)(blocks < 152 * 32 ? blocks : 152 * 32), 256, 0, s>>>(wkv, N, K, tiled, pieces);
+    return cudaGetLastError();
 }
 
 size_t gemv_smem_bytes(int T, int K) {

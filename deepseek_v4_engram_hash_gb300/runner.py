@@ -16,9 +16,11 @@ from . import synth
 
 class EngramSetup:
     def __init__(self, cfg, device="cuda", batch: int | None = None, max_tokens: int | None = None,
-                 tables_on_host: bool = False):
+                 tables_on_host: bool = False, tiled_wkv: bool = True):
         """tables_on_host: keep the per-layer tables in page-locked host memory,
-        read row by row in place by the kernels (tables larger than HBM)."""
+        read row by row in place by the kernels (tables larger than HBM).
+        tiled_wkv: also hold each layer's wkv in the engram_tile_wkv layout,
+        which the 1..8-token projection then reads."""
         self.cfg = cfg
         self.tables_on_host = tables_on_host
         self.device = torch.device(device)
@@ -61,6 +63,10 @@ class EngramSetup:
                     E.engram_rows_q2k(d["wkv_q2k"], nb, ids, nb, 1, 1, d["wkv"])
                 else:
                     synth.fill_wkv_cuda(cfg, l, d["wkv"])
+                if tiled_wkv:
+                    d["wkv_tiled"] = torch.empty(E.engram_tiled_wkv_bytes(cfg.N, cfg.K) // 2, dtype=torch.bfloat16,
+                                                 device=self.device)
+                    E.engram_tile_wkv(d["wkv"], cfg.N, cfg.K, d["wkv_tiled"])
                 if tables_on_host:
                     for key in ("table", "scales"):
                         if d.get(key) is not None:

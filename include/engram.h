@@ -163,6 +163,19 @@ int engram_gate(float *d_h, const uint16_t *d_kv, const float *d_qk, int32_t T, 
 int engram_project_q2k(const uint16_t *d_x, const uint8_t *d_wkv_q2k, int32_t K, int32_t N,
                        uint16_t *d_kv, uintptr_t stream);
 
+/* wkv tiled for the 1..8-token projection (a layout of the same weights,
+ * made once when the weights are loaded; not a step of the method).  Tile
+ * (g, c) holds rows 16 g .. 16 g + 15 and columns 2048 c .. 2048 c + 2047 of
+ * wkv [N, K] bf16, row after row, 64 KB contiguous; tiles are ordered g-major:
+ *   tiled[((g * ceil(K / 2048) + c) * 16 + r) * 2048 + j] = wkv[16 g + r, 2048 c + j],
+ * zero where 16 g + r >= N or 2048 c + j >= K.  The projection then streams
+ * each 16-row group's pieces from one contiguous range instead of 16 rows
+ * 2 K apart.  engram_tiled_wkv_bytes gives the size; engram_tile_wkv writes
+ * it (d_wkv and d_tiled device memory, 16-byte aligned, not overlapping;
+ * stream-ordered, no host sync). */
+size_t engram_tiled_wkv_bytes(int32_t N, int32_t K);
+int engram_tile_wkv(const uint16_t *d_wkv, int32_t N, int32_t K, uint16_t *d_tiled, uintptr_t stream);
+
 /* One engram layer for engram_forward. */
 typedef struct {
     const void *table;      /* FP8, FP8_E8M0: e4m3 [rows, head_dim]; Q2K: blocks [rows, 84] */
@@ -177,6 +190,10 @@ typedef struct {
                                16-byte aligned: when every layer has it and C * head_dim
                                <= 6144, calls of 1..8 tokens (batch * T) project from it,
                                bit-identical to the bf16 path on the dequantised blocks */
+    const uint16_t *wkv_tiled; /* optional engram_tile_wkv(wkv), 16-byte aligned: calls of
+                               1..8 tokens that project from bf16 read the layer's weights
+                               from it instead of wkv, with bit-identical results; wkv is
+                               still required (the larger calls read it) */
 } engram_layer;
 
 /* The whole forward for n_layers engram layers (in `layers` order) on one

@@ -156,6 +156,35 @@ def test_forward_fused_gemv_matches_staged_calls(E):
         assert torch.equal(kv.view(torch.int16), eng.kv(1, l).view(torch.int16))
 
 
+@pytest.mark.parametrize("name", ["v41", "odd_n", "wide_c"])
+def test_forward_tiled_wkv_bit_identical(E, name):
+    """The 1..8-token projection reading the tiled wkv gives the same kv and
+    highway bits as reading row-major wkv (V4.1 at 1, 2 and 8 tokens; N = 120
+    with a short last row group; K = 4800 with a part-filled last tile)."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = {"v41": configs.V41_DECODE.with_(batch=1, T=8), "odd_n": ODD_N, "wide_c": WIDE_C}[name]
+    B = 1 if name == "v41" else cfg.batch
+    engs = [runner.EngramSetup(cfg, batch=B, max_tokens=8 * B, tiled_wkv=t) for t in (True, False)]
+    assert "wkv_tiled" in engs[0].layer_data[0] and "wkv_tiled" not in engs[1].layer_data[0]
+    pos, first = 0, 0
+    for T in (1, 2, 8, 1):
+        M = B * T
+        if M > 8:
+            continue
+        ids = engs[0].ids_for(f"tiled{pos}", T)
+        outs = []
+        for eng in engs:
+            d_h = _h_device(cfg, first, M, True)
+            eng.forward(ids, pos, d_h)
+            assert E.engram_check() == 0
+            outs.append((d_h.clone(), [eng.kv(M, l).clone() for l in range(cfg.n_layers)]))
+        assert torch.equal(outs[0][0].view(torch.int32), outs[1][0].view(torch.int32)), "highway"
+        for l in range(cfg.n_layers):
+            assert torch.equal(outs[0][1][l].view(torch.int16), outs[1][1][l].view(torch.int16)), f"kv {l}"
+        pos += T
+        first += M
+
+
 ODD_FP8 = configs.TINY.with_(
     name="odd_fp8", vocab=5000, n_compressed=3000, unmapped_5pct=True, pad_token_id=7,
     pad_compressed=-1, layer_ids=(2, 9, 30), max_ngram=5, n_heads=3, prime_target=1000,

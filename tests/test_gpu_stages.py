@@ -192,6 +192,25 @@ def test_project_cta_pairs_bit_identical_to_one_cta(E, T, N):
 
 # rows = T x hc: up to 512 the layer-pipelined variant, above it the
 # register-lean one (four CTAs an SM), D from 8 to 16384
+@pytest.mark.parametrize("N,K", [(120, 4800), (1040, 6144), (7, 16), (20480, 2056)])
+def test_tile_wkv_layout(E, N, K):
+    """engram_tile_wkv against the layout written out in numpy: 16-row x
+    2048-column tiles, g-major, zero past the last row and column."""
+    g = torch.Generator(device="cpu").manual_seed(N * 7 + K)
+    w = torch.randint(-32768, 32767, (N, K), generator=g, dtype=torch.int32).to(torch.int16)
+    d_w = w.cuda().view(torch.bfloat16)
+    nbytes = E.engram_tiled_wkv_bytes(N, K)
+    G, C = -(-N // 16), -(-K // 2048)
+    assert nbytes == G * C * 16 * 2048 * 2
+    d_t = torch.full((nbytes // 2,), -1, dtype=torch.int16, device="cuda")   # poison: every slot written
+    E.engram_tile_wkv(d_w, N, K, d_t.view(torch.bfloat16))
+    torch.cuda.synchronize()
+    want = np.zeros((G * 16, C * 2048), dtype=np.int16)
+    want[:N, :K] = w.numpy()
+    want = want.reshape(G, 16, C, 2048).transpose(0, 2, 1, 3).ravel()
+    assert np.array_equal(d_t.cpu().numpy(), want)
+
+
 @pytest.mark.parametrize("T,hc,D", [(16, 2, 128), (5, 4, 4096), (3, 1, 8), (2, 3, 16384), (7, 4, 1000),
                                    (200, 4, 4096), (300, 2, 1000), (129, 4, 16384)])
 def test_gate_vs_oracle(E, T, hc, D):
