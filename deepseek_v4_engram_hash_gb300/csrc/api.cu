@@ -24,6 +24,7 @@ struct engram_hasher {
     int32_t batch;
     int64_t max_seq;
     int64_t *cache;
+    int *sched;             // the projection's work counters, 2 a layer, zero between launches
     int device;
     // engram_forward_host: the highway upload runs on `aux` while the
     // projection streams wkv on the caller's stream; only the gate waits.
@@ -202,7 +203,9 @@ int engram_hasher_create(const engram_tables *t, int32_t batch, int64_t max_seq,
     h->max_seq = max_seq;
     cudaGetDevice(&h->device);
     const size_t bytes = (size_t)batch * max_seq * sizeof(int64_t);
+    const size_t sched_bytes = 2 * kMaxLayers * sizeof(int);
     if (cudaMalloc(&h->cache, bytes) != cudaSuccess || cudaMemset(h->cache, 0, bytes) != cudaSuccess ||
+        cudaMalloc(&h->sched, sched_bytes) != cudaSuccess || cudaMemset(h->sched, 0, sched_bytes) != cudaSuccess ||
         cudaStreamCreateWithFlags(&h->aux, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_main, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_h, cudaEventDisableTiming) != cudaSuccess) {
@@ -219,12 +222,14 @@ int engram_hasher_create(const engram_tables *t, int32_t batch, int64_t max_seq,
 
 int engram_hasher_reset(engram_hasher *hs, uintptr_t stream) {
     if (!hs) return ENGRAM_E_NULL;
+    if (cudaMemsetAsync(hs->sched, 0, 2 * kMaxLayers * sizeof(int), S(stream)) != cudaSuccess) return ENGRAM_E_CUDA;
     return cuda_rc(cudaMemsetAsync(hs->cache, 0, (size_t)hs->batch * hs->max_seq * sizeof(int64_t), S(stream)));
 }
 
 void engram_hasher_destroy(engram_hasher *hs) {
     if (!hs) return;
     cudaFree(hs->cache);
+    cudaFree(hs->sched);
     if (hs->ev_h) cudaEventDestroy(hs->ev_h);
     if (hs->ev_main) cudaEventDestroy(hs->ev_main);
     if (hs->aux) cudaStreamDestroy(hs->aux);
@@ -583,6 +588,7 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
         a.fuse_hash = fuse_hash ? 1 : 0;
         a.hash = hash_args(hs, d_ids, T, start_pos, ids, d_pos);
         a.pdl = 1;
+        a.sched = hs->sched;
         a.err = err;
         ga.pdl = 1;
         record(2, s);

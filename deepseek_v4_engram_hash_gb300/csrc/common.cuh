@@ -295,6 +295,7 @@ struct GemvArgs {
     int32_t fuse_hash;      // compute the row ids in-kernel (hash below), write them to ids_out
     HashArgs hash;          // hash.out = row ids [T, L, C] in the workspace
     int32_t pdl;            // launched as a programmatic dependent
+    int *sched;             // per layer: next 16-row group, copy warps done (zero between launches), or null
     int *err;
 };
 constexpr int kFusedHashMaxIds = 2048;  // T * C row ids a CTA may hash for its layer

@@ -94,7 +94,9 @@ struct Ring<true> {
 };
 template <bool WQ2K>
 constexpr size_t ring_smem_bytes() {
-    return (size_t)Ring<WQ2K>::kStages * Ring<WQ2K>::kStageBytes + kRedBytes + 2 * Ring<WQ2K>::kStages * 8 + 16;
+    // ring, partials, full/empty barriers, then the abort flag and each slot's group
+    return (size_t)Ring<WQ2K>::kStages * Ring<WQ2K>::kStageBytes + kRedBytes + 2 * Ring<WQ2K>::kStages * 8 + 16 +
+           4 * Ring<WQ2K>::kStages;
 }
 static_assert(ring_smem_bytes<false>() <= 227 * 1024 && ring_smem_bytes<true>() <= 227 * 1024, "shared memory");
 
@@ -134,6 +136,20 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 // The 16 MMA warps only (the copy warp does not take part).
 __device__ __forceinline__ void mma_warps_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(kMmaWarps * 32) : "memory");
+}
+// The same barrier, returning whether any MMA thread passed p: a decision that
+// every MMA warp takes alike.
+__device__ __forceinline__ bool mma_warps_any(bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)p), "r"(kMmaWarps * 32)
+        : "memory");
+    return r != 0;
 }
 
 // Small non-negative integer -> f32 without the quarter-rate conversion unit:
@@ -296,6 +312,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     int64_t *s_ids = reinterpret_cast<int64_t *>(red);                                   // until x is gathered
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::kStages * R::kStageBytes + kRedBytes);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * R::kStages);
+    volatile int *stage_grp = abort_flag + 1;   // [kStages]: the group of the stage in the slot, -1 at the end
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int b) { return bar0 + 8u * b; };
     auto empty = [&](int b) { return bar0 + 8u * (R::kStages + b); };
@@ -310,11 +327,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     const int nsub = (kblocks + kStageKb - 1) / kStageKb;                // <= kMmaSubMax (host-checked)
     const uint32_t q2k_row = (uint32_t)(K >> 8) * 84u;                  // bytes of a Q2_K row
     const int groups_total = (N + 15) / 16;
-    // the CTA's groups: cta, cta + P, cta + 2P, ... (P CTAs a layer)
-    const int ngroups = cta < groups_total ? (groups_total - cta + ctas_per_layer - 1) / ctas_per_layer : 0;
-    auto group_of = [&](int gi) { return cta + gi * ctas_per_layer; };
     const int spg = WQ2K ? 1 : nsub;                                     // stages a group
-    const int nstages = ngroups * spg;
     const bool producer = warp == kMmaWarps;
 
     if (threadIdx.x == 0) {
@@ -329,46 +342,78 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     __syncthreads();
 
     const uint64_t pol = l2_evict_first();
-    int issued = 0;
-    // Copy warp: stage i into slot i % kStages once the MMA warps have released it.
-    auto issue_until = [&](int stop) {
-        for (; issued < stop; ++issued) {
-            const int i = issued, b = i % R::kStages;
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(empty(b), ((i / R::kStages) & 1) ^ 1, abort_flag, a.err);
-            if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
-            const uint32_t dst = ring + b * R::kStageBytes;
-            if (WQ2K) {
-                // the group's rows are contiguous: one copy of the 16-byte multiple,
-                // the last 4..12 bytes (a short last group only) by plain stores
-                const int r0 = group_of(i) * 16, nrows = min(16, N - r0);
-                const uint32_t total = (uint32_t)nrows * q2k_row, bulk = total & ~15u;
-                const uint8_t *src = ly.wkv_q2k + (size_t)r0 * q2k_row;
-                if (lane < (int)(total - bulk) / 4)
-                    reinterpret_cast<uint32_t *>(smem_raw + b * R::kStageBytes + bulk)[lane] =
-                        __ldg(reinterpret_cast<const uint32_t *>(src + bulk) + lane);
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_expect_tx(full(b), bulk);
-                    if (bulk) bulk_load(dst, src, bulk, full(b), pol);
-                }
-            } else {
-                const int grp = group_of(i / nsub), kb0 = (i % nsub) * kStageKb;
-                const uint32_t bytes = (uint32_t)min(kStageKb, kblocks - kb0) * 64u;
-                const int r0 = grp * 16, nrows = min(16, N - r0);
-                if (lane == 0) mbar_expect_tx(full(b), bytes * (uint32_t)nrows);
-                __syncwarp();
-                // row r0 + lane, columns kb0 * 32 ..: from the tiled copy (the group's
-                // piece is one contiguous 64 KB tile) or from row-major wkv
-                const uint16_t *src =
-                    ly.wkv_tiled ? ly.wkv_tiled + ((size_t)(grp * nsub + i % nsub) * kTileRows + lane) * kTileCols
-                                 : ly.wkv + (size_t)(r0 + lane) * K + kb0 * 32;
-                if (lane < nrows) bulk_load(dst + lane * kRowBytes, src, bytes, full(b), pol);
-            }
+    // The CTA's 16-row groups.  With a.sched, a per-layer counter hands them
+    // out as the copy warps ask (CTAs whose copies land sooner take more: the
+    // SMs of one launch stream at unequal rates, 11 us apart at the end of a
+    // single-token step with a fixed share each); else cta, cta + P, cta + 2P, ...
+    int issued = 0, cur = -1, grabs = 0;
+    bool ended = false;
+    auto next_group = [&]() {
+        if (a.sched) return atomicAdd(a.sched + 2 * li, 1);
+        return cta + (grabs++) * ctas_per_layer;
+    };
+    // Copy warp: stage `issued` into slot issued % kStages once the MMA warps
+    // have released it, the slot's group written beside it.  Past the last
+    // group the stage is an end marker (group -1, no bytes).  False once the
+    // end marker is out or the CTA is aborting.
+    auto issue_one = [&]() -> bool {
+        const int i = issued, b = i % R::kStages;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(empty(b), ((i / R::kStages) & 1) ^ 1, abort_flag, a.err);
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+            ended = true;
+            return false;
         }
+        const int sub = WQ2K ? 0 : i % nsub;
+        if (sub == 0) {
+            int gnext = 0;
+            if (lane == 0) gnext = next_group();
+            cur = __shfl_sync(0xFFFFFFFFu, gnext, 0);
+        }
+        ++issued;
+        if (cur >= groups_total) {
+            if (lane == 0) {
+                stage_grp[b] = -1;
+                mbar_arrive(full(b));                  // completes the phase: no bytes
+            }
+            ended = true;
+            return false;
+        }
+        if (lane == 0) stage_grp[b] = cur;             // published by the arrival below
+        const uint32_t dst = ring + b * R::kStageBytes;
+        if (WQ2K) {
+            // the group's rows are contiguous: one copy of the 16-byte multiple,
+            // the last 4..12 bytes (a short last group only) by plain stores
+            const int r0 = cur * 16, nrows = min(16, N - r0);
+            const uint32_t total = (uint32_t)nrows * q2k_row, bulk = total & ~15u;
+            const uint8_t *src = ly.wkv_q2k + (size_t)r0 * q2k_row;
+            if (lane < (int)(total - bulk) / 4)
+                reinterpret_cast<uint32_t *>(smem_raw + b * R::kStageBytes + bulk)[lane] =
+                    __ldg(reinterpret_cast<const uint32_t *>(src + bulk) + lane);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_expect_tx(full(b), bulk);
+                if (bulk) bulk_load(dst, src, bulk, full(b), pol);
+            }
+        } else {
+            const int kb0 = sub * kStageKb;
+            const uint32_t bytes = (uint32_t)min(kStageKb, kblocks - kb0) * 64u;
+            const int r0 = cur * 16, nrows = min(16, N - r0);
+            if (lane == 0) mbar_expect_tx(full(b), bytes * (uint32_t)nrows);
+            __syncwarp();
+            // row r0 + lane, columns kb0 * 32 ..: from the tiled copy (the group's
+            // piece is one contiguous 64 KB tile) or from row-major wkv
+            const uint16_t *src =
+                ly.wkv_tiled ? ly.wkv_tiled + ((size_t)(cur * nsub + sub) * kTileRows + lane) * kTileCols
+                             : ly.wkv + (size_t)(r0 + lane) * K + kb0 * 32;
+            if (lane < nrows) bulk_load(dst + lane * kRowBytes, src, bytes, full(b), pol);
+        }
+        return true;
     };
     // the first stages need nothing computed: before the wait
-    if (producer) issue_until(min(nstages, R::kPrefetch));
+    if (producer)
+        for (int k = 0; k < R::kPrefetch && issue_one(); ++k) {
+        }
 
     // Hashing here from a host position, the hash and the gather read only the
     // inputs, the constant tables and the cache entries of earlier steps; the
@@ -392,7 +437,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     }
 
     if (producer) {
-        issue_until(nstages);
+        while (!ended && issue_one()) {
+        }
         // Let every copy already issued land before the CTA can leave.
         if (lane == 0)
             for (int d = 1; d <= R::kStages && issued - d >= 0; ++d) {
@@ -401,6 +447,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
                 while (!mbar_try(full(i % R::kStages), (i / R::kStages) & 1) && now_ns() - t0 < 10000000ull) {
                 }
             }
+        // The last of the layer's copy warps to finish resets its counters for
+        // the next launch (launches of this kernel never overlap: the next one
+        // starts after the gate that waits for this one).
+        if (lane == 0 && a.sched) {
+            __threadfence();
+            if (atomicAdd(a.sched + 2 * li + 1, 1) == ctas_per_layer - 1) {
+                atomicExch(a.sched + 2 * li, 0);
+                atomicExch(a.sched + 2 * li + 1, 0);
+            }
+        }
         return;
     }
 
@@ -424,36 +480,39 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
         if (lane == 0) mbar_arrive(empty(i % R::kStages));
     };
     const uint32_t a_off = g * kRowBytes + (warp * kMmaJ) * 64 + 16 * q;
-    for (int gi = 0; gi < ngroups; ++gi) {
+    for (int gi = 0;; ++gi) {
+        // the group's first stage names the group; every MMA warp leaves at the
+        // end marker, or when any of them finds the CTA aborting
+        const int i0 = gi * spg;
+        const int grp = acquire(i0) ? stage_grp[i0 % R::kStages] : -1;
+        if (mma_warps_any(grp < 0)) break;
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         if (WQ2K) {
-            if (acquire(gi)) {
-                // this warp's blocks 8 s + w/2, half w % 2, of rows g and g + 8
-                const uint8_t *row_lo = smem_raw + (gi % R::kStages) * R::kStageBytes + g * q2k_row +
-                                        (warp >> 1) * 84;
-                const uint8_t *row_hi = row_lo + 8 * q2k_row;
+            // this warp's blocks 8 s + w/2, half w % 2, of rows g and g + 8
+            const uint8_t *row_lo = smem_raw + (gi % R::kStages) * R::kStageBytes + g * q2k_row +
+                                    (warp >> 1) * 84;
+            const uint8_t *row_hi = row_lo + 8 * q2k_row;
 #pragma unroll
-                for (int sub = 0; sub < kMmaSubMax; ++sub) {
-                    if (sub < nsub && sub * kStageKb + warp * kMmaJ < kblocks) {
-                        const Q2kHalf hl = q2k_half(row_lo + sub * 8 * 84, warp & 1, q);
-                        const Q2kHalf hh = q2k_half(row_hi + sub * 8 * 84, warp & 1, q);
+            for (int sub = 0; sub < kMmaSubMax; ++sub) {
+                if (sub < nsub && sub * kStageKb + warp * kMmaJ < kblocks) {
+                    const Q2kHalf hl = q2k_half(row_lo + sub * 8 * 84, warp & 1, q);
+                    const Q2kHalf hh = q2k_half(row_hi + sub * 8 * 84, warp & 1, q);
 #pragma unroll
-                        for (int jj = 0; jj < kMmaJ; ++jj) {
-                            const uint4 lo = q2k_frag(hl, jj, q), hi = q2k_frag(hh, jj, q);
-                            const uint4 xb = xr[sub][jj];
-                            mma_16816(c, lo.x, hi.x, lo.y, hi.y, xb.x, xb.y);
-                            mma_16816(c, lo.z, hi.z, lo.w, hi.w, xb.z, xb.w);
-                        }
+                    for (int jj = 0; jj < kMmaJ; ++jj) {
+                        const uint4 lo = q2k_frag(hl, jj, q), hi = q2k_frag(hh, jj, q);
+                        const uint4 xb = xr[sub][jj];
+                        mma_16816(c, lo.x, hi.x, lo.y, hi.y, xb.x, xb.y);
+                        mma_16816(c, lo.z, hi.z, lo.w, hi.w, xb.z, xb.w);
                     }
                 }
-                release(gi);
             }
+            release(gi);
         } else {
 #pragma unroll
             for (int sub = 0; sub < kMmaSubMax; ++sub) {
                 if (sub < nsub) {
-                    const int i = gi * nsub + sub;
-                    if (acquire(i)) {
+                    const int i = i0 + sub;
+                    if (sub == 0 || acquire(i)) {
                         const uint32_t sa = ring + (i % R::kStages) * R::kStageBytes + a_off;
 #pragma unroll
                         for (int jj = 0; jj < kMmaJ; ++jj) {
@@ -481,7 +540,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
 #pragma unroll
             for (int w = 0; w < kMmaWarps; ++w) v += rb[(w * 32 + l) * 4 + j];
             const int gg = l >> 2, qq = l & 3;
-            const int r = group_of(gi) * 16 + gg + ((j & 2) ? 8 : 0), t = 2 * qq + (j & 1);
+            const int r = grp * 16 + gg + ((j & 2) ? 8 : 0), t = 2 * qq + (j & 1);
             if (r < N && t < T) ly.kv[(size_t)t * N + r] = (uint16_t)f32_to_bf16_bits(v);
         }
     }

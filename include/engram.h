@@ -97,10 +97,13 @@ void engram_tables_destroy(engram_tables *t);
 
 /* Look-back cache [batch, max_seq] of compressed ids, zero-filled like
  * `EngramHasher::new` / `NgramHashState::new`, so decode steps see the
- * prefill's ids.  The hasher borrows `t`, which must outlive it. */
+ * prefill's ids.  The hasher borrows `t`, which must outlive it.  It also
+ * holds the work counters of the 1..8-token projection (zero between
+ * calls; one forward at a time on a hasher). */
 int engram_hasher_create(const engram_tables *t, int32_t batch, int64_t max_seq,
                          engram_hasher **out);
-/* `EngramHasher::reset`: the cache returns to zeros (enqueued on `stream`). */
+/* `EngramHasher::reset`: the cache returns to zeros (enqueued on `stream`);
+ * the projection's work counters too (after ENGRAM_E_TIMEOUT they may not be). */
 int engram_hasher_reset(engram_hasher *hs, uintptr_t stream);
 void engram_hasher_destroy(engram_hasher *hs);
 
