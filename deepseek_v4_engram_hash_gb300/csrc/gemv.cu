@@ -7,13 +7,14 @@
 // so this kernel is shaped for HBM bandwidth, as the pages choose a GEMV over
 // a tiled GEMM at m = 1 (spark_model/layers/attn_v41.rs, `Kernels.gemv`).
 //
-// Grid: the layers' CTAs side by side, one an SM; each CTA owns a contiguous
-// run of 16-row groups of one layer's wkv.  Prologue: the CTA gathers that
-// layer's T * C table rows (fp8 codes x pow2 scale, or Q2_K blocks) straight
-// into x [T, K] bf16 in shared memory -- the [T * C, head_dim] rows never
-// touch HBM.  Main loop: a copy warp streams the CTA's wkv rows into a
-// shared-memory ring with bulk copies; 16 MMA warps multiply them by x on
-// mma.sync m16n8k16 (bf16 in, f32 accumulate).  wkv may also be held as Q2_K
+// Grid: the layers' CTAs side by side, one an SM; the CTAs of a layer share
+// its 16-row groups of wkv (handed out by a counter).  Prologue: the CTA
+// hashes the step's ids for its layer and each MMA lane gathers its x
+// fragments straight from the table rows (fp8 codes x scale, or Q2_K blocks)
+// into registers -- the [T * C, head_dim] rows never touch HBM.  Main loop: a
+// copy warp streams the groups' wkv rows into a shared-memory ring with bulk
+// copies; 16 MMA warps multiply them by x on mma.sync m16n8k16 (bf16 in, f32
+// accumulate).  wkv may also be held as Q2_K
 // blocks (`wkv_q2k` on spark_model/layers/engram_v41.rs, 6x fewer bytes): the
 // same kernel then copies the blocks and decodes each lane's weights into its
 // mma fragments, in the same order, so kv is bit-identical to the bf16 path on
@@ -293,9 +294,11 @@ __device__ __forceinline__ void gather_x(const GemvArgs &a, const GemvLayer &ly,
     }
 }
 
-// One CTA per SM; CTA c of the P that serve a layer takes its 16-row groups
-// c, c + P, c + 2P, ... (all CTAs sweep the layer's wkv together: 78.1
-// against 78.9 us for contiguous runs of groups, both layers at one token).
+// One CTA per SM.  The P CTAs that serve a layer take its 16-row groups from
+// a counter (a.sched) in the order they ask, or else CTA c takes c, c + P,
+// c + 2P, ...; either way the CTAs sweep the layer's wkv together (78.1
+// against 78.9 us for contiguous runs of groups a CTA, both layers at one
+// token; the counter 73.3 against 74.1 us a step).
 // MMA warp w takes k blocks 64 s + 4w + j (s = 0 .. nsub-1, j = 0..3) of
 // every row group, in that order -- for Q2_K weights the four shifts of half
 // w % 2 of block 8 s + w / 2 -- and the 16 partial 16 x 8 tiles of a group are
