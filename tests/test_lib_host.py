@@ -109,3 +109,24 @@ def test_compute_calls_refuse_before_launch(E):
     assert L.engram_project_q2k(a16, a16, 6400, 16, a16, None) == -11
     assert L.engram_hash(None, a16, 1, 0, a16, None) == -2
     assert L.engram_set_profile_events(a16, 3) == -1
+
+
+def test_tiled_wkv_size_and_refusals(E):
+    """engram_tiled_wkv_bytes: 16-row x 2048-column tiles, ragged edges padded;
+    engram_tile_wkv refuses null, misaligned and overlapping buffers and bad
+    shapes before it launches anything."""
+    L = E.lib()
+    L.engram_tiled_wkv_bytes.restype = ctypes.c_size_t
+    assert L.engram_tiled_wkv_bytes(20480, 6144) == 1280 * 3 * 16 * 2048 * 2   # = wkv bytes, no padding
+    assert L.engram_tiled_wkv_bytes(120, 4800) == 8 * 3 * 16 * 2048 * 2
+    assert L.engram_tiled_wkv_bytes(1, 8) == 16 * 2048 * 2
+    assert L.engram_tiled_wkv_bytes(0, 64) == 0 and L.engram_tiled_wkv_bytes(16, 12) == 0
+    P = ctypes.c_void_p
+    w, t = P(1 << 30), P(1 << 34)      # far apart, aligned, never dereferenced
+    assert L.engram_tile_wkv(None, 16, 64, t, None) == -2
+    assert L.engram_tile_wkv(w, 16, 64, None, None) == -2
+    assert L.engram_tile_wkv(w, 0, 64, t, None) == -1
+    assert L.engram_tile_wkv(w, 16, 60, t, None) == -1
+    assert L.engram_tile_wkv(P((1 << 30) + 8), 16, 64, t, None) == -3
+    assert L.engram_tile_wkv(w, 16, 64, P((1 << 34) + 2), None) == -3
+    assert L.engram_tile_wkv(w, 16, 64, P((1 << 30) + 1024), None) == -1    # overlaps wkv
