@@ -311,11 +311,14 @@ cudaError_t launch_tile_wkv(const uint16_t *wkv, int N, int K, uint16_t *tiled, 
 cudaError_t launch_gemm(const uint16_t *x, const uint16_t *wkv, uint16_t *kv, int M, int N, int K,
                         int *err, cudaStream_t s);
 bool gemm_tc_supported(int M, int N, int K);
+// pdl: launched as a programmatic dependent of the kernel before it (which
+// writes x); the GEMM waits for it after its set-up (TMEM, barriers).  Pair
+// kernel only (256 tokens and up).
 cudaError_t launch_gemm_tc(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
-                           int M, int N, int K, int *err, cudaStream_t s);
+                           int M, int N, int K, int *err, cudaStream_t s, bool pdl = false);
 // The same on CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles).
 cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
-                           int M, int N, int K, int *err, cudaStream_t s);
+                           int M, int N, int K, int *err, cudaStream_t s, bool pdl = false);
 cudaError_t launch_gemm_simt(const uint16_t *x, const uint16_t *wkv, uint16_t *kv, int M, int N,
                              int K, cudaStream_t s);
 

@@ -52,6 +52,7 @@ struct Params {
     int m_tiles, n_tiles, group_m;                  // m_tiles: 256-row pair tiles
     int full_per_pair;                              // whole tiles every pair takes first
     int tail_tiles, split;                          // the last tiles, each cut into `split` column parts
+    int pdl;                                        // wait for the previous kernel after the set-up
     int *err;
 };
 
@@ -171,6 +172,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();                                     // both CTAs' barriers exist before any remote arrival
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched early (programmatic dependent of the row gather): the set-up
+    // above ran beside the gather's last CTAs; x is read only after this.
+    // (The gate after the GEMM stays a plain launch: launched early, its CTAs
+    // beside the GEMM's made the 512-token step 2 % slower.)
+    if (p.pdl) griddep_wait();
 
     const int kblocks = p.K / BK;
     const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
@@ -287,7 +293,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // L layers: x[l] [M, K] and wkv[l] [N, K] -> kv[l] [M, N], one persistent
 // launch of CTA pairs.
 cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
-                            int M, int N, int K, int *err, cudaStream_t s) {
+                            int M, int N, int K, int *err, cudaStream_t s, bool pdl) {
     using namespace tc2;
     if (L < 1 || L > kMaxL || M < 1 || K < BK || K % BK || N < 8 || N % 8) return cudaErrorInvalidValue;
     Params p{};
@@ -342,8 +348,18 @@ cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *con
         p.full_per_pair = (tiles + pairs - 1) / pairs;
         p.tail_tiles = 0;
     }
-    gemm_tc2_kernel<<<2 * pairs, kThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    p.pdl = pdl ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, p);
 }
 
 }  // namespace engram

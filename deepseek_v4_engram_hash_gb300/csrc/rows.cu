@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(256, 6) hash_rows_fp8_kernel(const __grid_cons
     const uint32_t sb = (part << 4) >> bs;                   // the thread's scale block in its row
     const int64_t nblk = hd >> bs;
     int *err = r.layer[0].err;
+    griddep_launch();                 // the GEMM after this may start its set-up; it waits for x
     int64_t sp;
     const bool ok = hash_start(h, sp);
     const uint32_t warps = gridDim.x * (blockDim.x >> 5);
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(256) hash_rows_q2k_kernel(const __grid_constan
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t n_rows = (uint32_t)r.M * (uint32_t)r.L * (uint32_t)r.layer[0].C;
     int *err = r.layer[0].err;
+    griddep_launch();                 // the GEMM after this may start its set-up; it waits for x
     int64_t sp;
     const bool ok = hash_start(h, sp);
     const uint32_t warps = gridDim.x * (blockDim.x >> 5);
