@@ -173,7 +173,7 @@ int engram_project_q2k(const uint16_t *d_x, const uint8_t *d_wkv_q2k, int32_t K,
  *   tiled[((g * ceil(K / 2048) + c) * 16 + r) * 2048 + j] = wkv[16 g + r, 2048 c + j],
  * zero where 16 g + r >= N or 2048 c + j >= K.  The projection then streams
  * each 16-row group's pieces from one contiguous range instead of 16 rows
- * 2 K apart.  engram_tiled_wkv_bytes gives the size; engram_tile_wkv writes
+ * 2 K bytes apart.  engram_tiled_wkv_bytes gives the size; engram_tile_wkv writes
  * it (d_wkv and d_tiled device memory, 16-byte aligned, not overlapping;
  * stream-ordered, no host sync). */
 size_t engram_tiled_wkv_bytes(int32_t N, int32_t K);
@@ -287,9 +287,11 @@ size_t engram_workspace_bytes(const engram_geom *geom, int64_t max_tokens);
 int engram_workspace_layout(const engram_geom *geom, int64_t tokens, size_t *off);
 
 /* Optional stage timing: when set, engram_forward records on its stream
- * events[0] before the hash, [1] after it, [2] after the row gather (== [1]
- * where the gather is fused into the projection), [3] after the projection
- * and [4] after the gate.  events holds 5 cudaEvent_t as uintptr_t; the
+ * events[0] before the hash, [1] after it (== [0] where the hash runs inside
+ * the next launch), [2] after the row gather (== [1] where the gather is
+ * fused into the projection), [3] after the projection and [4] after the
+ * gate.  The events sit between the launches, so a profiled step loses the
+ * overlap of programmatic launches.  events holds 5 cudaEvent_t as uintptr_t; the
  * library keeps the pointer (the array must stay alive) until it is set to
  * NULL.  Process-wide; not thread-safe. */
 int engram_set_profile_events(const uintptr_t *events, int32_t n);
