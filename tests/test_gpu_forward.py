@@ -185,6 +185,28 @@ def test_forward_tiled_wkv_bit_identical(E, name):
         first += M
 
 
+def test_hasher_reset_clears_the_lookback(E):
+    """engram_hasher_reset returns the look-back cache to zeros (and the
+    projection's work counters): a decode step after a prefill and a reset
+    hashes its window over zeros, as a fresh oracle state does, and every
+    output of that step checks."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = configs.TINY
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=cfg.T)
+    pre = eng.ids_for("reset-prefill", cfg.T)
+    eng.forward(pre, 0, _h_device(cfg, 0, cfg.T, True))
+    assert E.engram_check() == 0
+    E.engram_hasher_reset(eng.hasher)
+    ids = eng.ids_for("reset-step", 2)
+    kept = G.hash_state(cfg, 1)
+    kept.forward(pre, 0)
+    fresh = G.hash_state(cfg, 1)
+    assert not np.array_equal(kept.forward(ids, cfg.T), G.hash_state(cfg, 1).forward(ids, cfg.T)), \
+        "the windows must reach into the prefill for the reset to show"
+    d_h = _h_device(cfg, cfg.T, 2, True)
+    _check_call(eng, fresh, ids, cfg.T, d_h, d_h.cpu().numpy(), np.arange(2), np.arange(cfg.N), cfg.T)
+
+
 ODD_FP8 = configs.TINY.with_(
     name="odd_fp8", vocab=5000, n_compressed=3000, unmapped_5pct=True, pad_token_id=7,
     pad_compressed=-1, layer_ids=(2, 9, 30), max_ngram=5, n_heads=3, prime_target=1000,
