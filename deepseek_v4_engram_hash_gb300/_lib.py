@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
             "engram_gate": ([P, P, P, i32, i32, i32, ctypes.c_float, st], ctypes.c_int),
             "engram_project_q2k": ([P, P, i32, i32, P, st], ctypes.c_int),
             "engram_tiled_wkv_bytes": ([i32, i32], ctypes.c_size_t),
+            "engram_selftest_wait_timeout": ([i32, st], ctypes.c_int),
             "engram_tile_wkv": ([P, i32, i32, P, st], ctypes.c_int),
             "engram_forward": ([P, ctypes.POINTER(engram_layer), P, i32, i64, P, ctypes.c_float,
                                 P, sz, st], ctypes.c_int),
@@ -213,6 +214,10 @@ def engram_project(d_x, d_wkv, T, K, N, d_kv, stream=None):
 def engram_project_q2k(d_x, d_wkv_q2k, K, N, d_kv, stream=None):
     _ok(lib().engram_project_q2k(_ptr(d_x), _ptr(d_wkv_q2k), int(K), int(N), _ptr(d_kv), _stream(stream)),
         "engram_project_q2k")
+
+
+def engram_selftest_wait_timeout(limit_us, stream=None):
+    _ok(lib().engram_selftest_wait_timeout(int(limit_us), _stream(stream)), "engram_selftest_wait_timeout")
 
 
 def engram_tiled_wkv_bytes(N, K) -> int:

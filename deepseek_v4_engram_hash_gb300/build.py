@@ -21,7 +21,7 @@ FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                 "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]
 
 ENGRAM_SRCS = ["api.cu", "hash.cu", "rows.cu", "gemv.cu", "gemm.cu", "gemm_simt.cu", "gemm_tc.cu", "gemm_tc2.cu",
-               "gate.cu", "noalloc.cu"]
+               "gate.cu", "noalloc.cu", "selftest.cu"]
 SYNTH_SRCS = ["synth.cu"]
 
 LIBENGRAM = os.path.join(PKG, "libengram.so")

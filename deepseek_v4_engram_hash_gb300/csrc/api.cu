@@ -406,6 +406,13 @@ int engram_project_q2k(const uint16_t *d_x, const uint8_t *d_wkv_q2k, int32_t K,
     return cuda_rc(launch_gemv_q2k(a, S(stream)));
 }
 
+int engram_selftest_wait_timeout(int32_t limit_us, uintptr_t stream) {
+    if (limit_us < 1 || limit_us > 1000000) return ENGRAM_E_INVALID;
+    int *err = err_ptr();
+    if (!err) return ENGRAM_E_CUDA;
+    return cuda_rc(launch_wait_timeout(err, (uint64_t)limit_us * 1000ull, S(stream)));
+}
+
 size_t engram_tiled_wkv_bytes(int32_t N, int32_t K) {
     if (N < 1 || K < 8 || K % 8) return 0;
     const size_t groups = ((size_t)N + kTileRows - 1) / kTileRows, chunks = ((size_t)K + kTileCols - 1) / kTileCols;

@@ -227,11 +227,11 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // Bounded wait: false if the CTA is aborting or the wait ran out (then it
 // raises the abort flag and the device error word).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int *err) {
+                                          int *err, uint64_t limit_ns = kWaitNs) {
     const uint64_t t0 = now_ns();
     while (!mbar_try(bar, parity)) {
         if (*abort_flag) return false;
-        if (now_ns() - t0 > kWaitNs) {
+        if (now_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             set_err(err, ENGRAM_E_TIMEOUT);
             return false;
@@ -334,5 +334,8 @@ struct GateArgs {
     int32_t pdl;            // launched as a programmatic dependent of the projection
 };
 cudaError_t launch_gate(const GateArgs &a, cudaStream_t s);
+
+// Self-test of the bounded wait (selftest.cu): one wait that must run out.
+cudaError_t launch_wait_timeout(int *err, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace engram

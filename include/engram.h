@@ -300,6 +300,14 @@ int engram_set_profile_events(const uintptr_t *events, int32_t n);
  * sticky error word (ENGRAM_OK if none). */
 int engram_check(uintptr_t stream);
 
+/* Self-test of failure detection (not a step of the method): enqueues one
+ * kernel whose thread waits, through the same bounded mbarrier wait that
+ * every copy ring and GEMM here uses, on a barrier nothing arrives at, for
+ * limit_us microseconds (1 .. 1e6); the wait gives up, the kernel raises
+ * ENGRAM_E_TIMEOUT in the error word (read by engram_check) and returns, and
+ * the device stays usable.  ENGRAM_E_INVALID for a limit out of range. */
+int engram_selftest_wait_timeout(int32_t limit_us, uintptr_t stream);
+
 const char *engram_strerror(int code);
 
 #ifdef __cplusplus

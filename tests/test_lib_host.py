@@ -111,6 +111,12 @@ def test_compute_calls_refuse_before_launch(E):
     assert L.engram_set_profile_events(a16, 3) == -1
 
 
+def test_selftest_wait_timeout_refuses_bad_limits(E):
+    L = E.lib()
+    assert L.engram_selftest_wait_timeout(0, None) == -1
+    assert L.engram_selftest_wait_timeout(2000000, None) == -1
+
+
 def test_tiled_wkv_size_and_refusals(E):
     """engram_tiled_wkv_bytes: 16-row x 2048-column tiles, ragged edges padded;
     engram_tile_wkv refuses null, misaligned and overlapping buffers and bad
