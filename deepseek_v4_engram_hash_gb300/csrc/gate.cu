@@ -77,17 +77,6 @@ __device__ __forceinline__ void load_kv(const GateArgs &a, int l, int t, int c, 
     }
 }
 
-// Per-thread asynchronous copies (cp.async) into this thread's own shared-
-// memory slots: no registers held while they land, no barrier to read them.
-__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // NV = float4 chunks per thread (D <= kGateThreads * 4 * NV).  PIPE: the next
 // layer's operands load while this layer reduces -- the latency choice for a
 // handful of rows (one token); without it the kernel stays under 64
@@ -95,14 +84,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 template <int NV, bool PIPE>
 __global__ void __launch_bounds__(kGateThreads, PIPE ? 1 : 4) gate_kernel(const __grid_constant__ GateArgs a) {
     constexpr bool kPipe = PIPE && NV <= 4;
-    // Many rows (register-lean, four CTAs an SM): the next layer's key, value
-    // and q*k go to shared memory by per-thread asynchronous copies while this
-    // layer reduces, so its loads no longer wait behind this layer's barriers.
-    constexpr bool kStage = !PIPE && NV <= 4;
-    constexpr int SNV = kStage ? NV : 1;
     __shared__ float red[3 * kGateThreads / 32];
-    __shared__ uint2 s_kb[SNV][kGateThreads], s_vb[SNV][kGateThreads];
-    __shared__ float4 s_q[SNV][kGateThreads];
     const int row = blockIdx.x;                       // (t, c)
     const int t = row / a.hc, c = row % a.hc;
     const int D = a.D, D4 = D >> 2;
@@ -116,33 +98,6 @@ __global__ void __launch_bounds__(kGateThreads, PIPE ? 1 : 4) gate_kernel(const 
         h[v] = i < D4 ? hrow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     GateChunk<NV> cur, nxt;
-    auto prefetch = [&](int l) {                      // layer l's operands into this thread's slots
-        const size_t N = (size_t)D * (a.hc + 1);
-        const uint16_t *kvt = a.kv[l] + (size_t)t * N;
-        const uint2 *key = reinterpret_cast<const uint2 *>(kvt + (size_t)c * D);
-        const uint2 *val = reinterpret_cast<const uint2 *>(kvt + (size_t)a.hc * D);
-        const float4 *qk = reinterpret_cast<const float4 *>(a.qk[l] + (size_t)c * D);
-#pragma unroll
-        for (int v = 0; v < SNV; ++v) {
-            const int i = threadIdx.x + v * kGateThreads;
-            if (i < D4) {
-                cp_async8(&s_kb[v][threadIdx.x], key + i);
-                cp_async8(&s_vb[v][threadIdx.x], val + i);
-                cp_async16(&s_q[v][threadIdx.x], qk + i);
-            }
-        }
-        cp_async_commit();
-    };
-    auto take = [&](GateChunk<NV> &g) {               // the prefetched layer, into registers
-        cp_async_wait_all();
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int i = threadIdx.x + v * kGateThreads, sv = v < SNV ? v : 0;
-            g.kb[v] = i < D4 ? s_kb[sv][threadIdx.x] : make_uint2(0, 0);
-            g.vb[v] = i < D4 ? s_vb[sv][threadIdx.x] : make_uint2(0, 0);
-            g.q[v] = i < D4 ? s_q[sv][threadIdx.x] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
     load_qk(a, 0, c, cur);
     if (a.pdl) {
         griddep_wait();
@@ -151,7 +106,6 @@ __global__ void __launch_bounds__(kGateThreads, PIPE ? 1 : 4) gate_kernel(const 
     if (a.advance_pos && blockIdx.x == 0 && threadIdx.x == 0)
         *a.advance_pos += a.advance_by;     // every read of the position happened in the projection
     load_kv(a, 0, t, c, cur);
-    if (kStage && a.L > 1) prefetch(1);
     for (int l = 0; l < a.L; ++l) {
         if (kPipe && l + 1 < a.L) {
             load_qk(a, l + 1, c, nxt);
@@ -184,9 +138,6 @@ __global__ void __launch_bounds__(kGateThreads, PIPE ? 1 : 4) gate_kernel(const 
         if (l + 1 < a.L) {
             if (kPipe) {
                 cur = nxt;
-            } else if (kStage) {
-                take(cur);
-                if (l + 2 < a.L) prefetch(l + 2);
             } else {
                 load_qk(a, l + 1, c, cur);
                 load_kv(a, l + 1, t, c, cur);
