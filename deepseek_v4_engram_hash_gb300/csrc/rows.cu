@@ -102,20 +102,21 @@ __device__ __forceinline__ int64_t fused_row_id(const HashRowsArgs &r, const Has
 
 // Hash and fp8 gather of every layer in one launch (the larger steps; the
 // hash kernel above is then not launched).  Global row r = (m L + l) C + col,
-// the hash output's order.  A warp takes 32 consecutive rows: lane i hashes
-// row base + i with hash_one (all 32 lanes busy), writes the id and, for
-// (l, col) = (0, 0), the position's cache entry; then the warp gathers the 32
+// the hash output's order.  A warp takes RB consecutive rows (RB <= 32): lane
+// i < RB hashes row base + i with hash_one, writes the id and, for
+// (l, col) = (0, 0), the position's cache entry; then the warp gathers the RB
 // rows, 32 / lpr a pass, each thread taking its row's id, layer and x row
 // from the hashing lane by shuffles, the loads of kU passes issued before any
 // conversion.  A device position that does not fit the cache (ENGRAM_E_CAPACITY
 // already raised) reads as id -1: zero rows, no row error on top.
 // head_dim / 16 and scale_block are powers of two, head_dim <= 512.
 // Measured on two V4.1 layers at 4096 tokens (hash + both gathers, against
-// 8 + 2 x 16 us for the hash kernel and two gathers): kU = 2 at 40 registers
-// 36.5 - 38 us; kU = 4 (64 registers) 43 us; kU = 1 43 - 48 us; the row's
-// first thread hashing alone (2 of 32 lanes busy) 57 - 70 us; the rows staged
-// in shared memory by bulk copies, one or two 32-row buffers a warp, 39 - 54 us.
-template <int kU>
+// 8 + 2 x 16 us for the hash kernel and two gathers): RB = 16, kU = 2 34.5 -
+// 35.1 us; RB = 8 34.7 - 35.4; RB = 32 36.5 - 39.7 (kU = 4 43, kU = 1 43 - 48);
+// RB = 16 with kU = 1 38, kU = 4 42; the row's first thread hashing alone
+// (2 of 32 lanes busy) 57 - 70 us; the rows staged in shared memory by bulk
+// copies, one or two 32-row buffers a warp, 39 - 54 us.
+template <int kU, int RB>
 __global__ void __launch_bounds__(256, 6) hash_rows_fp8_kernel(const __grid_constant__ HashRowsArgs r,
                                                             const __grid_constant__ HashArgs h) {
     const uint32_t lane = threadIdx.x & 31;
@@ -131,23 +132,24 @@ __global__ void __launch_bounds__(256, 6) hash_rows_fp8_kernel(const __grid_cons
     int64_t sp;
     const bool ok = hash_start(h, sp);
     const uint32_t warps = gridDim.x * (blockDim.x >> 5);
-    for (uint32_t base = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32; base < n_rows;
-         base += warps * 32) {
-        uint32_t li, xrow;
-        const int64_t id = fused_row_id(r, h, ok, sp, base + lane, li, xrow);
+    for (uint32_t base = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RB; base < n_rows;
+         base += warps * RB) {
+        uint32_t li = 0, xrow = 0;
+        int64_t id = -1;
+        if (lane < (uint32_t)RB) id = fused_row_id(r, h, ok, sp, base + lane, li, xrow);
 #pragma unroll 1
-        for (uint32_t p0 = 0; p0 < 32; p0 += per * kU) {
+        for (uint32_t p0 = 0; p0 < (uint32_t)RB; p0 += per * kU) {
             uint4 v[kU];
             float sc[kU];
             uint32_t pl[kU], px[kU];
             bool live[kU];
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
-                const uint32_t i = (p0 + u * per + sub) & 31;   // the row's hashing lane
+                const uint32_t i = (p0 + u * per + sub) & 31;   // the row's hashing lane (< RB when live)
                 const int64_t rid = __shfl_sync(0xFFFFFFFFu, id, i);
                 pl[u] = __shfl_sync(0xFFFFFFFFu, li, i);
                 px[u] = __shfl_sync(0xFFFFFFFFu, xrow, i);
-                live[u] = p0 + u * per < 32 && base + i < n_rows;
+                live[u] = p0 + u * per + sub < (uint32_t)RB && base + i < n_rows;
                 const RowsArgs &a = r.layer[pl[u]];
                 v[u] = make_uint4(0, 0, 0, 0);
                 sc[u] = 0.0f;
@@ -288,7 +290,7 @@ cudaError_t launch_hash_rows(const HashRowsArgs &a, const HashArgs &h, cudaStrea
     if (a.layer[0].fmt == ENGRAM_FMT_Q2K)
         hash_rows_q2k_kernel<8, 8><<<grid((n_rows + 7) / 8), 256, 0, s>>>(a, h);
     else
-        hash_rows_fp8_kernel<2><<<grid((n_rows + 31) / 32), 256, 0, s>>>(a, h);
+        hash_rows_fp8_kernel<2, 16><<<grid((n_rows + 15) / 16), 256, 0, s>>>(a, h);
     return cudaGetLastError();
 }
 
