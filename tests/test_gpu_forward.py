@@ -353,6 +353,14 @@ def test_long_decode_carries_lookback(E):
     for k in range(512):
         want = ref.forward(steps[:, k:k + 1], cfg.T + k).reshape(B, cfg.n_layers, cfg.cols)
         assert np.array_equal(got[k].cpu().numpy(), want), f"step {k}"
+    # the last step's projection, one output row from every 16-row group of both
+    # layers: after 512 launches the groups still all get computed
+    last = got[-1].cpu().numpy()
+    rows = np.arange(0, cfg.N, 16) + np.arange(cfg.N // 16) % 16
+    for l in range(cfg.n_layers):
+        kv_gpu = _u16(eng.kv(B, l))[:, rows]
+        want_kv = G.kv(cfg, l, G.x_of(cfg, l, last), rows)
+        assert G.kv_rel_err(kv_gpu, want_kv) <= G.KV_TOL, f"layer {l} kv after 512 steps"
 
 
 @pytest.mark.parametrize("name,T", [("v41_decode_T1", 1), ("tiny", 16), ("v41_prefill_T4096", 4096)])
