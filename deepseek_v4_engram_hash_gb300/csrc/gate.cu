@@ -8,7 +8,7 @@
 //   g  = copysign(sqrt(max(|s|, 1e-6)), s)
 //   h += sigmoid(g) * value.
 //
-// One CTA per (token, stream) row of D values.  The row stays in registers
+// One CTA per (token, stream) row of D values (128 or 256 threads).  The row stays in registers
 // across the layers: layer l+1's norms and dot are taken on the highway that
 // layer l just updated, so the highway is read and written once for all
 // layers.  Reductions: per-thread f32 sums, a warp butterfly, then the
@@ -19,6 +19,7 @@ namespace engram {
 
 constexpr int kGateThreads = 256;
 
+template <int TH>
 __device__ __forceinline__ void block_sum3(float &a, float &b, float &c, float *red) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -36,7 +37,7 @@ __device__ __forceinline__ void block_sum3(float &a, float &b, float &c, float *
     __syncthreads();
     a = b = c = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kGateThreads / 32; ++w) {
+    for (int w = 0; w < TH / 32; ++w) {
         a += red[3 * w + 0];
         b += red[3 * w + 1];
         c += red[3 * w + 2];
@@ -51,18 +52,18 @@ struct GateChunk {
     float4 q[NV];
 };
 
-template <int NV>
+template <int NV, int TH>
 __device__ __forceinline__ void load_qk(const GateArgs &a, int l, int c, GateChunk<NV> &g) {
     const int D4 = a.D >> 2;
     const float4 *qk = reinterpret_cast<const float4 *>(a.qk[l] + (size_t)c * a.D);
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-        const int i = threadIdx.x + v * kGateThreads;
+        const int i = threadIdx.x + v * TH;
         g.q[v] = i < D4 ? __ldg(qk + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
-template <int NV>
+template <int NV, int TH>
 __device__ __forceinline__ void load_kv(const GateArgs &a, int l, int t, int c, GateChunk<NV> &g) {
     const int D4 = a.D >> 2;
     const size_t N = (size_t)a.D * (a.hc + 1);
@@ -71,20 +72,21 @@ __device__ __forceinline__ void load_kv(const GateArgs &a, int l, int t, int c, 
     const uint2 *val = reinterpret_cast<const uint2 *>(kvt + (size_t)a.hc * a.D);
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-        const int i = threadIdx.x + v * kGateThreads;
+        const int i = threadIdx.x + v * TH;
         g.kb[v] = i < D4 ? key[i] : make_uint2(0, 0);
         g.vb[v] = i < D4 ? val[i] : make_uint2(0, 0);
     }
 }
 
-// NV = float4 chunks per thread (D <= kGateThreads * 4 * NV).  PIPE: the next
+// NV = float4 chunks per thread (D <= TH * 4 * NV, TH threads a CTA).  PIPE: the next
 // layer's operands load while this layer reduces -- the latency choice for a
-// handful of rows (one token); without it the kernel stays under 64
-// registers, so four CTAs share an SM -- the throughput choice for many rows.
-template <int NV, bool PIPE>
-__global__ void __launch_bounds__(kGateThreads, PIPE ? 1 : 4) gate_kernel(const __grid_constant__ GateArgs a) {
+// handful of rows (one token).  Without it four CTAs share an SM -- the
+// throughput choice for many rows, at 128 threads and 128 registers (32
+// values a thread) up to D = 4096, at 256 threads and 64 registers beyond.
+template <int NV, bool PIPE, int TH = kGateThreads>
+__global__ void __launch_bounds__(TH, PIPE ? 1 : 4) gate_kernel(const __grid_constant__ GateArgs a) {
     constexpr bool kPipe = PIPE && NV <= 4;
-    __shared__ float red[3 * kGateThreads / 32];
+    __shared__ float red[3 * TH / 32];
     const int row = blockIdx.x;                       // (t, c)
     const int t = row / a.hc, c = row % a.hc;
     const int D = a.D, D4 = D >> 2;
@@ -94,22 +96,22 @@ __global__ void __launch_bounds__(kGateThreads, PIPE ? 1 : 4) gate_kernel(const 
     float4 h[NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-        const int i = threadIdx.x + v * kGateThreads;
+        const int i = threadIdx.x + v * TH;
         h[v] = i < D4 ? hrow[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     GateChunk<NV> cur, nxt;
-    load_qk(a, 0, c, cur);
+    load_qk<NV, TH>(a, 0, c, cur);
     if (a.pdl) {
         griddep_wait();
         griddep_launch();
     }
     if (a.advance_pos && blockIdx.x == 0 && threadIdx.x == 0)
         *a.advance_pos += a.advance_by;     // every read of the position happened in the projection
-    load_kv(a, 0, t, c, cur);
+    load_kv<NV, TH>(a, 0, t, c, cur);
     for (int l = 0; l < a.L; ++l) {
         if (kPipe && l + 1 < a.L) {
-            load_qk(a, l + 1, c, nxt);
-            load_kv(a, l + 1, t, c, nxt);
+            load_qk<NV, TH>(a, l + 1, c, nxt);
+            load_kv<NV, TH>(a, l + 1, t, c, nxt);
         }
         float hh = 0.f, kk = 0.f, dot = 0.f;
 #pragma unroll
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kGateThreads, PIPE ? 1 : 4) gate_kernel(const 
             dot = fmaf(h[v].x * cur.q[v].x, k0, dot); dot = fmaf(h[v].y * cur.q[v].y, k1, dot);
             dot = fmaf(h[v].z * cur.q[v].z, k2, dot); dot = fmaf(h[v].w * cur.q[v].w, k3, dot);
         }
-        block_sum3(hh, kk, dot, red);
+        block_sum3<TH>(hh, kk, dot, red);
         const float rstd = (1.0f / sqrtf(hh / (float)D + a.eps)) * (1.0f / sqrtf(kk / (float)D + a.eps));
         const float s = dot * rstd * a.inv_sqrt_dim;
         const float g = copysignf(sqrtf(fmaxf(fabsf(s), 1e-6f)), s);
@@ -139,30 +141,30 @@ __global__ void __launch_bounds__(kGateThreads, PIPE ? 1 : 4) gate_kernel(const 
             if (kPipe) {
                 cur = nxt;
             } else {
-                load_qk(a, l + 1, c, cur);
-                load_kv(a, l + 1, t, c, cur);
+                load_qk<NV, TH>(a, l + 1, c, cur);
+                load_kv<NV, TH>(a, l + 1, t, c, cur);
             }
         }
     }
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-        const int i = threadIdx.x + v * kGateThreads;
+        const int i = threadIdx.x + v * TH;
         if (i < D4) hrow[i] = h[v];
     }
 }
 
-template <int NV, bool PIPE>
+template <int NV, bool PIPE, int TH = kGateThreads>
 static cudaError_t launch_nv(const GateArgs &a, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.M * a.hc);
-    cfg.blockDim = dim3(kGateThreads);
+    cfg.blockDim = dim3(TH);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gate_kernel<NV, PIPE>, a);
+    return cudaLaunchKernelEx(&cfg, gate_kernel<NV, PIPE, TH>, a);
 }
 
 template <bool PIPE>
@@ -178,8 +180,17 @@ static cudaError_t launch_p(const GateArgs &a, cudaStream_t s) {
 
 cudaError_t launch_gate(const GateArgs &a, cudaStream_t s) {
     if (a.M == 0) return cudaSuccess;
-    // one CTA per (token, stream): pipeline the layers when there are few rows
-    return (int64_t)a.M * a.hc <= 512 ? launch_p<true>(a, s) : launch_p<false>(a, s);
+    // One CTA per (token, stream).  Few rows: 256 threads, the layers pipelined.
+    // Many rows up to dim 4096: 128 threads, 8 float4 a thread in 128 registers,
+    // four CTAs an SM (4096 tokens: 140.8 us against 148.7 with 256 threads at
+    // 64 registers; 161 at 96 registers, which spill; 247 with 512 threads).
+    if ((int64_t)a.M * a.hc <= 512) return launch_p<true>(a, s);
+    constexpr int per = 128 * 4;
+    if (a.D <= per) return launch_nv<1, false, 128>(a, s);
+    if (a.D <= 2 * per) return launch_nv<2, false, 128>(a, s);
+    if (a.D <= 4 * per) return launch_nv<4, false, 128>(a, s);
+    if (a.D <= 8 * per) return launch_nv<8, false, 128>(a, s);
+    return launch_p<false>(a, s);
 }
 
 }  // namespace engram
