@@ -166,9 +166,10 @@ __device__ __forceinline__ float small_u2f(uint32_t n) {
 // being (byte >> 2j) & 3.  A value is y = d*sc*q - dmin*m rounded once (d*sc*q
 // and dmin*m are exact in f32, so fma(d*sc, q, -dmin*m) is that), then bf16:
 // with one sub-block the lane's eight values take one of four, v[q].  v[0..3]
-// are built once and each pair (v[q_e], v[q_e+1]) is one byte permute of them,
-// its selector nibbles 2q_e, 2q_e + 1, 2q_e+1, 2q_e+1 + 1 = h * 0x22 + 0x1010
-// for the two quant bytes h = q_e + 256 q_e+1.
+// are built once (q2k_table) and each pair (v[q_e], v[q_e+1]) is one byte
+// permute of them, its selector nibbles 2q_e, 2q_e + 1, 2q_e+1, 2q_e+1 + 1: for
+// four quants t, one a byte, t * 0x22 + 0x10101010 holds the selectors of
+// pairs (0, 1) and, 16 bits up, (2, 3) (a permute reads the low 16 bits).
 struct Q2kHalf {                  // what a lane needs of one half-block
     uint32_t q0, q1;              // its 8 quant bytes
     uint32_t sc01, sc23;          // the scale words of shifts 0,1 and 2,3
@@ -186,22 +187,31 @@ __device__ __forceinline__ Q2kHalf q2k_half(const uint8_t *blk, int half, int q)
     h.dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
     return h;
 }
+// v[0..3] as bf16 pairs (v0 v1, v2 v3) for the sub-block scale byte sc
+__device__ __forceinline__ uint2 q2k_table(uint32_t sc, float d, float dmin) {
+    const float dl = __fmul_rn(d, small_u2f(sc & 15u));
+    const float nml = -__fmul_rn(dmin, small_u2f(sc >> 4));
+    return make_uint2(pack_bf16x2(__fmaf_rn(dl, 0.0f, nml), __fmaf_rn(dl, 1.0f, nml)),
+                      pack_bf16x2(__fmaf_rn(dl, 2.0f, nml), __fmaf_rn(dl, 3.0f, nml)));
+}
+// four values v[t_0..3] as bf16 pairs, quants t one a byte
+__device__ __forceinline__ uint2 q2k_pick4(uint2 v, uint32_t t) {
+    const uint32_t s = t * 0x22u + 0x10101010u;
+    return make_uint2(__byte_perm(v.x, v.y, s), __byte_perm(v.x, v.y, s >> 16));
+}
 __device__ __forceinline__ uint4 q2k_frag(const Q2kHalf &h, int j, int q) {
     // sub-block 8 half + 2j + q/2: byte 2 (j % 2) + q/2 of scale word j / 2
     const uint32_t sc = ((j < 2 ? h.sc01 : h.sc23) >> (8 * (2 * (j & 1) + (q >> 1)))) & 0xFFu;
-    const float dl = __fmul_rn(h.d, small_u2f(sc & 15u));
-    const float nml = -__fmul_rn(h.dmin, small_u2f(sc >> 4));
-    const uint32_t v01 = pack_bf16x2(__fmaf_rn(dl, 0.0f, nml), __fmaf_rn(dl, 1.0f, nml));
-    const uint32_t v23 = pack_bf16x2(__fmaf_rn(dl, 2.0f, nml), __fmaf_rn(dl, 3.0f, nml));
-    const uint32_t t0 = (h.q0 >> (2 * j)) & 0x03030303u, t1 = (h.q1 >> (2 * j)) & 0x03030303u;
-    return make_uint4(__byte_perm(v01, v23, t0 * 0x22u + 0x1010u),
-                      __byte_perm(v01, v23, (t0 >> 16) * 0x22u + 0x1010u),
-                      __byte_perm(v01, v23, t1 * 0x22u + 0x1010u),
-                      __byte_perm(v01, v23, (t1 >> 16) * 0x22u + 0x1010u));
+    const uint2 v = q2k_table(sc, h.d, h.dmin);
+    const uint2 a = q2k_pick4(v, (h.q0 >> (2 * j)) & 0x03030303u), b = q2k_pick4(v, (h.q1 >> (2 * j)) & 0x03030303u);
+    return make_uint4(a.x, a.y, b.x, b.y);
 }
 
-// This lane's x fragments: token g, 32-wide k blocks kb = 64 s + 4w + j of
-// its warp w, values x[g, 32 kb + 8q .. +7] as bf16 pairs -- from the plain x,
+// This lane's x fragments: token g, 32-wide k blocks kb = 64 s + 4w + (jj ^ q%2)
+// of its warp w (jj = 0..3: lanes q and q ^ 1 take the blocks of a pair in
+// opposite order, so that at Q2_K weights each builds one of the pair's two
+// value tables and swaps it with the other), values x[g, 32 kb + 8q .. +7] as
+// bf16 pairs -- from the plain x,
 // or gathered from the layer's table rows ids[g * id_stride + c] (fp8 codes x
 // their block's scale, or a Q2_K block) exactly as the row kernels dequantise
 // them.  Ids first, then every load (an invalid id reads row 0 and gives
@@ -218,7 +228,7 @@ __device__ __forceinline__ void gather_x(const GemvArgs &a, const GemvLayer &ly,
     bool need[NF];
 #pragma unroll
     for (int f = 0; f < NF; ++f) {
-        const int sub = f / kMmaJ, kb = sub * kStageKb + warp * kMmaJ + f % kMmaJ;
+        const int sub = f / kMmaJ, kb = sub * kStageKb + warp * kMmaJ + ((f % kMmaJ) ^ (q & 1));
         need[f] = tok && sub < nsub && kb < kblocks;
         k0[f] = (need[f] ? kb : 0) * 32 + 8 * q;
     }
@@ -267,7 +277,7 @@ __device__ __forceinline__ void gather_x(const GemvArgs &a, const GemvLayer &ly,
             h[sub] = q2k_half(ly.table + id[sub * kMmaJ] * 84, warp & 1, q);
 #pragma unroll
         for (int f = 0; f < NF; ++f)
-            xr[f / kMmaJ][f % kMmaJ] = ok[f] ? q2k_frag(h[f / kMmaJ], f % kMmaJ, q) : make_uint4(0, 0, 0, 0);
+            xr[f / kMmaJ][f % kMmaJ] = ok[f] ? q2k_frag(h[f / kMmaJ], (f % kMmaJ) ^ (q & 1), q) : make_uint4(0, 0, 0, 0);
         return;
     }
     const int nblk = a.hd / a.blk;
@@ -300,11 +310,14 @@ __device__ __forceinline__ void gather_x(const GemvArgs &a, const GemvLayer &ly,
 // against 78.9 us for contiguous runs of groups a CTA, both layers at one
 // token; the counter 73.3 against 74.1 us a step).
 // MMA warp w takes k blocks 64 s + 4w + j (s = 0 .. nsub-1, j = 0..3) of
-// every row group, in that order -- for Q2_K weights the four shifts of half
-// w % 2 of block 8 s + w / 2 -- and the 16 partial 16 x 8 tiles of a group are
-// summed in warp order through shared memory; both weight formats follow
-// this order exactly.  bf16: stage i is the CTA's group i / nsub, k blocks
-// 64 (i % nsub) .. +63.  Q2_K: stage i is its group i.
+// every row group -- for Q2_K weights the four shifts of half w % 2 of block
+// 8 s + w / 2 -- lane q in the order j = 0 ^ q%2, 1 ^ q%2, 2 ^ q%2, 3 ^ q%2
+// (K is a multiple of 64 on every path, so a warp's blocks in a stage are
+// all valid, the first pair only, or none, alike for every lane), and the 16
+// partial 16 x 8 tiles of a group are summed in warp order through shared
+// memory; both weight formats follow this order exactly.  bf16: stage i is
+// the CTA's group i / nsub, k blocks 64 (i % nsub) .. +63.  Q2_K: stage i is
+// its group i.
 template <bool HASH, bool WQ2K>
 __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_constant__ GemvArgs a) {
     using R = Ring<WQ2K>;
@@ -483,6 +496,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
         if (lane == 0) mbar_arrive(empty(i % R::kStages));
     };
     const uint32_t a_off = g * kRowBytes + (warp * kMmaJ) * 64 + 16 * q;
+    // Q2_K: this lane's scale byte in a scale word, and the quant shifts 2j of blocks jj = 0, 1
+    const uint32_t sc_sh = 8u * (2u * (q & 1) + (q >> 1));
+    const uint32_t q_sh0 = 2u * (q & 1), q_sh1 = 2u - q_sh0;
     for (int gi = 0;; ++gi) {
         // the group's first stage names the group; every MMA warp leaves at the
         // end marker, or when any of them finds the CTA aborting
@@ -500,12 +516,33 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
                 if (sub < nsub && sub * kStageKb + warp * kMmaJ < kblocks) {
                     const Q2kHalf hl = q2k_half(row_lo + sub * 8 * 84, warp & 1, q);
                     const Q2kHalf hh = q2k_half(row_hi + sub * 8 * 84, warp & 1, q);
+                    // Block jj of the lane is shift j = jj ^ q%2.  At jj = 0, 2 the lane
+                    // builds the value table of its sub-block (scale byte 2 (q%2) + q/2 of
+                    // word jj/2); at jj = 1, 3 it needs shift j ^ 1 of the same pair,
+                    // whose table lane q ^ 1 (same row, same sub-block) built at jj - 1.
+                    uint2 vl[kMmaJ], vh[kMmaJ];
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        vl[2 * p] = q2k_table(((p ? hl.sc23 : hl.sc01) >> sc_sh) & 0xFFu, hl.d, hl.dmin);
+                        vh[2 * p] = q2k_table(((p ? hh.sc23 : hh.sc01) >> sc_sh) & 0xFFu, hh.d, hh.dmin);
+                    }
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        vl[2 * p + 1] = make_uint2(__shfl_xor_sync(0xFFFFFFFFu, vl[2 * p].x, 1),
+                                                   __shfl_xor_sync(0xFFFFFFFFu, vl[2 * p].y, 1));
+                        vh[2 * p + 1] = make_uint2(__shfl_xor_sync(0xFFFFFFFFu, vh[2 * p].x, 1),
+                                                   __shfl_xor_sync(0xFFFFFFFFu, vh[2 * p].y, 1));
+                    }
 #pragma unroll
                     for (int jj = 0; jj < kMmaJ; ++jj) {
-                        const uint4 lo = q2k_frag(hl, jj, q), hi = q2k_frag(hh, jj, q);
+                        const uint32_t sh = ((jj & 1) ? q_sh1 : q_sh0) + ((jj & 2) ? 4u : 0u);    // 2j
+                        const uint2 l0 = q2k_pick4(vl[jj], (hl.q0 >> sh) & 0x03030303u);
+                        const uint2 l1 = q2k_pick4(vl[jj], (hl.q1 >> sh) & 0x03030303u);
+                        const uint2 h0 = q2k_pick4(vh[jj], (hh.q0 >> sh) & 0x03030303u);
+                        const uint2 h1 = q2k_pick4(vh[jj], (hh.q1 >> sh) & 0x03030303u);
                         const uint4 xb = xr[sub][jj];
-                        mma_16816(c, lo.x, hi.x, lo.y, hi.y, xb.x, xb.y);
-                        mma_16816(c, lo.z, hi.z, lo.w, hi.w, xb.z, xb.w);
+                        mma_16816(c, l0.x, h0.x, l0.y, h0.y, xb.x, xb.y);
+                        mma_16816(c, l1.x, h1.x, l1.y, h1.y, xb.z, xb.w);
                     }
                 }
             }
@@ -520,7 +557,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
 #pragma unroll
                         for (int jj = 0; jj < kMmaJ; ++jj) {
                             if (sub * kStageKb + warp * kMmaJ + jj < kblocks) {
-                                const uint4 lo = lds128(sa + jj * 64), hi = lds128(sa + 8 * kRowBytes + jj * 64);
+                                const uint32_t sj = sa + (uint32_t)((jj ^ (q & 1)) * 64);
+                                const uint4 lo = lds128(sj), hi = lds128(sj + 8 * kRowBytes);
                                 const uint4 xb = xr[sub][jj];
                                 mma_16816(c, lo.x, hi.x, lo.y, hi.y, xb.x, xb.y);
                                 mma_16816(c, lo.z, hi.z, lo.w, hi.w, xb.z, xb.w);
@@ -554,7 +592,7 @@ static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (a.T < 1 || a.T > kMmaT || a.K % (WQ2K ? 256 : 32) || a.K > kGemvMaxK) return cudaErrorInvalidValue;
+    if (a.T < 1 || a.T > kMmaT || a.K % (WQ2K ? 256 : 64) || a.K > kGemvMaxK) return cudaErrorInvalidValue;
     if (HASH && (size_t)a.T * a.C > (size_t)kFusedHashMaxIds) return cudaErrorInvalidValue;
     for (int l = 0; l < a.L; ++l) {
         const void *w = WQ2K ? static_cast<const void *>(a.layer[l].wkv_q2k) : static_cast<const void *>(a.layer[l].wkv);
