@@ -212,7 +212,8 @@ def test_tile_wkv_layout(E, N, K):
 
 
 @pytest.mark.parametrize("T,hc,D", [(16, 2, 128), (5, 4, 4096), (3, 1, 8), (2, 3, 16384), (7, 4, 1000),
-                                   (200, 4, 4096), (300, 2, 1000), (129, 4, 16384)])
+                                   (200, 4, 4096), (300, 2, 1000), (129, 4, 16384), (700, 4, 4096),
+                                   (150, 4, 3000)])
 def test_gate_vs_oracle(E, T, hc, D):
     rng = np.random.default_rng(T + hc + D)
     h = rng.standard_normal((T, hc, D)).astype(np.float32)
