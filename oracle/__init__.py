@@ -32,19 +32,64 @@ E_ROW = -3
 E_PRIME = -4
 
 
-def build(force: bool = False) -> str:
-    """Compile ``oracle.c`` into ``liboracle.so`` with gcc (OpenMP if available)."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
-        return _LIB
-    tmp = _LIB + f".{os.getpid()}.tmp"
+def compile_source(src: str, out: str) -> str:
+    """Compile the C source `src` into the shared library `out` with gcc
+    (OpenMP if available), with the flags the oracle is built with."""
+    tmp = out + f".{os.getpid()}.tmp"
     base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-            "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+            "-fno-fast-math", src, "-o", tmp, "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
     except subprocess.CalledProcessError:
         subprocess.run(base, check=True, capture_output=True)
-    os.replace(tmp, _LIB)
-    return _LIB
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so``."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    return compile_source(_SRC, _LIB)
+
+
+def load(path: str) -> ctypes.CDLL:
+    """The library at `path` (built from ``oracle.c`` or a copy of it) with
+    the signatures of its functions declared."""
+    L = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    i32 = ctypes.c_int
+    L.orc_num_threads.restype = i32
+    L.orc_set_num_threads.argtypes = [i32]
+    L.orc_set_num_threads.restype = None
+    L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+    L.orc_f32_to_bf16.restype = ctypes.c_uint16
+    L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    L.orc_bf16_to_f32.restype = ctypes.c_float
+    L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+    L.orc_f16_to_f32.restype = ctypes.c_float
+    L.orc_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    L.orc_e4m3_to_f32.restype = ctypes.c_float
+    L.orc_f32_to_e4m3.argtypes = [ctypes.c_float]
+    L.orc_f32_to_e4m3.restype = ctypes.c_uint8
+    L.orc_f32_to_e8m0.argtypes = [ctypes.c_float]
+    L.orc_f32_to_e8m0.restype = ctypes.c_float
+    L.orc_e8m0_to_f32.argtypes = [ctypes.c_uint8]
+    L.orc_e8m0_to_f32.restype = ctypes.c_float
+    L.orc_rows_fp8_e8m0.argtypes = [P, P, i64, i32, i32, P, i64, P]
+    L.orc_rows_fp8_e8m0.restype = i32
+    L.orc_hash.argtypes = [P, i64, i64, P, P, P, i32, i32, i32, P, i32, i64, P, i32, i64, P]
+    L.orc_hash.restype = i32
+    L.orc_rows_fp8.argtypes = [P, P, i64, i32, i32, P, i64, P]
+    L.orc_rows_fp8.restype = i32
+    L.orc_rows_q2k.argtypes = [P, i64, P, i64, P]
+    L.orc_rows_q2k.restype = i32
+    L.orc_linear_bf16.argtypes = [P, i64, i64, P, i64, P, P]
+    L.orc_linear_bf16.restype = None
+    L.orc_gate.argtypes = [P, P, P, P, i64, i32, i32, ctypes.c_float, i32, P]
+    L.orc_gate.restype = None
+    return L
 
 
 def lib() -> ctypes.CDLL:
@@ -52,40 +97,7 @@ def lib() -> ctypes.CDLL:
     with _lock:
         if _lib is None:
             build()
-            L = ctypes.CDLL(_LIB)
-            P = ctypes.c_void_p
-            i64 = ctypes.c_int64
-            i32 = ctypes.c_int
-            L.orc_num_threads.restype = i32
-            L.orc_set_num_threads.argtypes = [i32]
-            L.orc_set_num_threads.restype = None
-            L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
-            L.orc_f32_to_bf16.restype = ctypes.c_uint16
-            L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
-            L.orc_bf16_to_f32.restype = ctypes.c_float
-            L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
-            L.orc_f16_to_f32.restype = ctypes.c_float
-            L.orc_e4m3_to_f32.argtypes = [ctypes.c_uint8]
-            L.orc_e4m3_to_f32.restype = ctypes.c_float
-            L.orc_f32_to_e4m3.argtypes = [ctypes.c_float]
-            L.orc_f32_to_e4m3.restype = ctypes.c_uint8
-            L.orc_f32_to_e8m0.argtypes = [ctypes.c_float]
-            L.orc_f32_to_e8m0.restype = ctypes.c_float
-            L.orc_e8m0_to_f32.argtypes = [ctypes.c_uint8]
-            L.orc_e8m0_to_f32.restype = ctypes.c_float
-            L.orc_rows_fp8_e8m0.argtypes = [P, P, i64, i32, i32, P, i64, P]
-            L.orc_rows_fp8_e8m0.restype = i32
-            L.orc_hash.argtypes = [P, i64, i64, P, P, P, i32, i32, i32, P, i32, i64, P, i32, i64, P]
-            L.orc_hash.restype = i32
-            L.orc_rows_fp8.argtypes = [P, P, i64, i32, i32, P, i64, P]
-            L.orc_rows_fp8.restype = i32
-            L.orc_rows_q2k.argtypes = [P, i64, P, i64, P]
-            L.orc_rows_q2k.restype = i32
-            L.orc_linear_bf16.argtypes = [P, i64, i64, P, i64, P, P]
-            L.orc_linear_bf16.restype = None
-            L.orc_gate.argtypes = [P, P, P, P, i64, i32, i32, ctypes.c_float, i32, P]
-            L.orc_gate.restype = None
-            _lib = L
+            _lib = load(_LIB)
     return _lib
 
 
