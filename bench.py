@@ -396,9 +396,10 @@ def rank_seed(rank: int) -> int:
 # CPU oracle (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_decode_rate(budget_s: float, wkv_host=None):
-    """Oracle decode steps on the host cores for about budget_s seconds.
-    Returns (tokens/s, threads, steps)."""
+def oracle_decode_rate(budget_s: float, wkv_host=None, steps=None, warm=0):
+    """Oracle decode steps (T = 1) on the host cores: for about budget_s
+    seconds, or -- with `steps` -- `warm` untimed steps and then exactly
+    `steps` timed ones.  Returns (tokens/s, threads, timed steps)."""
     import oracle
     from deepseek_v4_engram_hash_gb300 import configs, synth
     sys.path.insert(0, os.path.join(ROOT, "tests"))
@@ -408,22 +409,25 @@ def oracle_decode_rate(budget_s: float, wkv_host=None):
     if wkv_host is None:       # regenerate wkv on the host (input preparation, untimed)
         wkv_host = [synth.wkv_rows(cfg, l, np.arange(cfg.N)) for l in range(cfg.n_layers)]
     qk = [synth.qk_weights(cfg, l) for l in range(cfg.n_layers)]
-    st = G.hash_state(cfg, 1)
+    total = 4096 if steps is None else warm + steps
+    st = G.hash_state(cfg, 1, cfg.prefix + total + 16)
     st.forward(synth.token_ids(cfg, "prefix.0", cfg.prefix)[None], 0)
     h = synth.highway(cfg, [cfg.prefix])
-    ids = synth.token_ids(cfg, "decode.0", 4096)
+    ids = synth.token_ids(cfg, "decode.0", total)
     pos, n, t_used = cfg.prefix, 0, 0.0
-    while t_used < budget_s and n < 4096:
+    while n < total and (steps is not None or t_used < budget_s):
         rid = st.forward(ids[n:n + 1][None], pos)[0]          # hash [1, L, C]
         rows = [G.rows(cfg, l, rid[:, l, :]) for l in range(cfg.n_layers)]   # includes table regen
         t = time.perf_counter()
         for l in range(cfg.n_layers):
             kv = oracle.linear_bf16(rows[l].reshape(1, cfg.K), wkv_host[l])
             h = oracle.gate(h, kv, qk[l][0], qk[l][1], cfg.hc, cfg.dim, cfg.eps)
-        t_used += time.perf_counter() - t
+        if n >= warm:
+            t_used += time.perf_counter() - t
         pos += 1
         n += 1
-    return n / t_used, oracle.num_threads(), n
+    timed = n - warm
+    return timed / t_used, oracle.num_threads(), timed
 
 
 def oracle_prefill_rate(n_tokens: int, wkv_host):
@@ -451,15 +455,17 @@ def oracle_prefill_rate(n_tokens: int, wkv_host):
 def reference_arm(args, rank, world):
     if rank != 0:
         return
-    rate, threads, n = oracle_decode_rate(max(10.0, 0.5 * args.steps * 0.1))
+    # W untimed and K timed oracle decode steps, each one token of the
+    # single-token workload (about 21 ms a step on the 16 host cores)
+    rate, threads, n = oracle_decode_rate(0.0, steps=args.steps, warm=args.warmup)
     line = {"metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 / rate, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "impl": "reference",
             "config": {"workload": "v41_decode_T1", "tokens_per_step": 1},
             "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{n} decode steps of the plain C oracle (projection + gate of both "
-                                       f"layers; hash and row gather untimed)"},
+                             "sample": f"{n} timed decode steps (after {args.warmup} untimed) of the plain C "
+                                       f"oracle (projection + gate of both layers; hash and row gather untimed)"},
             "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
