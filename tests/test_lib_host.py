@@ -136,3 +136,14 @@ def test_tiled_wkv_size_and_refusals(E):
     assert L.engram_tile_wkv(P((1 << 30) + 8), 16, 64, t, None) == -3
     assert L.engram_tile_wkv(w, 16, 64, P((1 << 34) + 2), None) == -3
     assert L.engram_tile_wkv(w, 16, 64, P((1 << 30) + 1024), None) == -1    # overlaps wkv
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    """Without libengram.so the binding raises; nothing falls back to the CPU."""
+    from deepseek_v4_engram_hash_gb300 import _lib
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", _lib.LIB_PATH + ".absent")
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _lib.lib()
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _lib.strerror(0)
