@@ -60,6 +60,12 @@ def test_bf16_matches_library(orc):
     ref = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     got = np.array([orc.f32_to_bf16(float(x)) for x in xs], dtype=np.uint16)
     assert np.array_equal(got, ref)
+    # a NaN stays a NaN whatever its sign and payload (IEEE 754 conversion); the
+    # library returns one canonical NaN, so only NaN-ness is compared
+    nans = np.array([0x7FC00000, 0x7FFFFFFF, 0xFFFFFFFF, 0xFFC00001, 0x7FC0FFFF], dtype=np.uint32).view(np.float32)
+    for x in nans:
+        b = orc.f32_to_bf16(float(x))
+        assert (b & 0x7F80) == 0x7F80 and (b & 0x007F) != 0, hex(b)
 
 
 def test_f16_decode_all_codes(orc):

@@ -71,6 +71,21 @@ MUTANTS = [
      "const int q = (qs[l] >> (2 * j)) & 3;", [FORMATS]),
     ("q2k: one sub-block per 32 values", "const int s = sc[8 * half + 2 * j + l / 16];",
      "const int s = sc[8 * half + 2 * j];", [FORMATS]),
+    ("e4m3 encode: truncation", "int mant = (int)round_ties_even((a * ldexp(1.0, -e) - 1.0) * 8.0);",
+     "int mant = (int)((a * ldexp(1.0, -e) - 1.0) * 8.0);", [FORMATS]),
+    ("e4m3 encode: subnormal threshold", "if (e < -6) return sign | (uint8_t)round_ties_even(a * 512.0);",
+     "if (e < -7) return sign | (uint8_t)round_ties_even(a * 512.0);", [FORMATS]),
+    ("e4m3 encode: mantissa carry dropped", "if (mant == 8) { e += 1; mant = 0; }", "", [FORMATS]),
+    ("rounding: ties up", "return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;", "return f + 1.0;", [FORMATS]),
+    ("f16: normal exponent bias", "else v = ldexpf((float)(1024 + m), e - 25);",
+     "else v = ldexpf((float)(1024 + m), e - 24);", [FORMATS]),
+    ("bf16: NaN not kept quiet", "if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x0040u);",
+     "", [FORMATS]),
+    ("e8m0 decode: code 255 not NaN", "if (code == 255) return NAN;", "", [FORMATS]),
+    ("hash: token range off by one", "if (ids[i] < 0 || ids[i] >= vocab) return ORC_E_TOKEN;",
+     "if (ids[i] < 0 || ids[i] > vocab) return ORC_E_TOKEN;", [HASH]),
+    ("hash: capacity off by one", "if (start_pos < 0 || start_pos + T > max_seq) return ORC_E_CAPACITY;",
+     "if (start_pos < 0 || start_pos + T > max_seq + 1) return ORC_E_CAPACITY;", [HASH]),
     # stage 3: the projection
     ("linear: w transposed", "sum += orc_bf16_to_f32(xr[i]) * orc_bf16_to_f32(wr[i]);",
      "sum += orc_bf16_to_f32(xr[i]) * orc_bf16_to_f32(w[i * out_f + o]);", [LINGATE]),
@@ -143,7 +158,7 @@ def test_pins_catch_mutant(idx, tmp_path, monkeypatch):
     for pin, call in _pin_calls(modules):
         try:
             call()
-        except (AssertionError, ValueError, IndexError):
+        except (AssertionError, ValueError, IndexError, pytest.fail.Exception):
             caught.append(pin)
     assert caught, f"no pin catches the planted mistake: {name}"
 
@@ -160,7 +175,7 @@ def test_unmutated_copy_passes_every_pin(tmp_path, monkeypatch):
     for pin, call in _pin_calls([HASH, FORMATS, LINGATE]):
         try:
             call()
-        except Exception as e:                                  # noqa: BLE001 -- any failure counts
+        except (Exception, pytest.fail.Exception) as e:         # noqa: BLE001 -- any failure counts
             failed.append(f"{pin}: {type(e).__name__}")
     assert not failed, failed
     assert len(_pin_calls([HASH, FORMATS, LINGATE])) >= 25
