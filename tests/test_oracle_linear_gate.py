@@ -34,6 +34,19 @@ def test_linear_matches_f64_product(orc):
     assert np.array_equal(y, _bf16(acc))
 
 
+def test_linear_accumulates_in_f32_in_index_order(orc):
+    """x = (1, 2^-24, 2^-24), w = (1, 1, 1): in f32 from the left each 2^-24 is
+    half an ulp of 1 and rounds away (ties to even), so the sum is exactly 1;
+    the exact sum, a wider accumulator or a pairwise order give 1 + 2^-23."""
+    x = _bf16(np.array([[1.0, 2.0 ** -24, 2.0 ** -24]]))
+    w = _bf16(np.ones((1, 3)))
+    _, acc = orc.linear_bf16(x, w, return_acc=True)
+    assert acc[0, 0] == np.float32(1.0)
+    x2 = _bf16(np.array([[2.0 ** -24, 2.0 ** -24, 1.0]]))      # small terms first: they add up
+    _, acc2 = orc.linear_bf16(x2, w, return_acc=True)
+    assert acc2[0, 0] == np.float32(1.0 + 2.0 ** -23)
+
+
 def test_linear_picks_rows_of_w(orc):
     in_f = 64
     x = _bf16(np.eye(3, in_f))                              # x_r = e_r

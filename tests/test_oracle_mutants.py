@@ -91,6 +91,10 @@ MUTANTS = [
      "sum += orc_bf16_to_f32(xr[i]) * orc_bf16_to_f32(w[i * out_f + o]);", [LINGATE]),
     ("linear: last term dropped", "for (int64_t i = 0; i < in_f; ++i)",
      "for (int64_t i = 0; i + 1 < in_f; ++i)", [LINGATE]),
+    ("linear: accumulated in double", "float sum = 0.0f;\n            for (int64_t i = 0; i < in_f; ++i)",
+     "double sum = 0.0;\n            for (int64_t i = 0; i < in_f; ++i)", [LINGATE]),
+    ("linear: summed from the last term", "sum += orc_bf16_to_f32(xr[i]) * orc_bf16_to_f32(wr[i]);",
+     "sum += orc_bf16_to_f32(xr[in_f - 1 - i]) * orc_bf16_to_f32(wr[in_f - 1 - i]);", [LINGATE]),
     ("linear: output truncated to bf16", "y[r * out_f + o] = orc_f32_to_bf16(sum);",
      "y[r * out_f + o] = (uint16_t)(f2u(sum) >> 16);", [LINGATE]),
     # stage 4: the gate
