@@ -115,6 +115,12 @@ MUTANTS = [
      "const uint16_t *key = kv + t * kv_w;", [LINGATE]),
     ("gate: value from the key columns", "const uint16_t *value = kv + t * kv_w + (int64_t)hc * D;",
      "const uint16_t *value = kv + t * kv_w;", [LINGATE]),
+    ("gate: kk from the highway", "kk += kd * kd;", "kk += hr[d] * hr[d];", [LINGATE]),
+    ("gate: key norm dropped", "(1.0f / sqrtf(kk / (float)D + eps));", "1.0f;", [LINGATE]),
+    ("gate: key added instead of the value", "float o = hr[d] + gate * orc_bf16_to_f32(value[d]);",
+     "float o = hr[d] + gate * orc_bf16_to_f32(key[d]);", [LINGATE]),
+    ("gate: every stream updates stream 0", "float *hr = h + (t * hc + c) * D;", "float *hr = h + t * hc * D;",
+     [LINGATE]),
     ("gate: sigmoid of -g", "const float gate = 1.0f / (1.0f + expf(-g));",
      "const float gate = 1.0f / (1.0f + expf(g));", [LINGATE]),
     ("gate: highway rounded to bf16 always", "if (bf16_out) o = orc_bf16_to_f32(orc_f32_to_bf16(o));",
