@@ -36,6 +36,10 @@ MUTANTS = [
      "rolling ^= wrapping_mul(tokens[i], mult[(int64_t)i * L + li]);", [HASH]),
     ("hash: columns head-major", "const int col = (i - 1) * H + h;",
      "const int col = h * (ng - 1) + (i - 1);", [HASH]),
+    ("hash: roll starts from zero", "int64_t rolling = wrapping_mul(tokens[0], m[0]);", "int64_t rolling = 0;",
+     [HASH]),
+    ("hash: unsigned remainder", "int64_t r = rolling % p;",
+     "int64_t r = (int64_t)((uint64_t)rolling % (uint64_t)p);", [HASH]),
     ("hash: new positions never enter the cache",
      "cache[(int64_t)b * max_seq + start_pos + s] = token_map[ids[(int64_t)b * T + s]];", "(void)0;", [HASH]),
     # number formats and table rows
@@ -50,6 +54,7 @@ MUTANTS = [
      "if (a > 448.0) return sign | 0x7F;", [FORMATS]),
     ("f16: subnormals off by a factor two", "if (e == 0) v = ldexpf((float)m, -24);",
      "if (e == 0) v = ldexpf((float)m, -25);", [FORMATS]),
+    ("e8m0: rounds down", "if (m > 0x400000u || (m == 0x400000u && (e & 1u) == 1u)) e += 1;", "", [FORMATS]),
     ("e8m0: ties to the odd code", "(m == 0x400000u && (e & 1u) == 1u)",
      "(m == 0x400000u && (e & 1u) == 0u)", [FORMATS]),
     ("fp8 rows: scale block d % nblk", "const float s = scales[id * nblk + d / blk];",
