@@ -145,6 +145,8 @@ float orc_e8m0_to_f32(uint8_t code) {
 /* Stage 1: the n-gram hash                                             */
 /* ------------------------------------------------------------------ */
 
+/* Two's-complement wrapping product: the exact product reduced mod 2^64,
+ * read back as a signed value. */
 static int64_t wrapping_mul(int64_t a, int64_t b) {
     return (int64_t)((uint64_t)a * (uint64_t)b);
 }
@@ -152,21 +154,47 @@ static int64_t wrapping_add(int64_t a, int64_t b) {
     return (int64_t)((uint64_t)a + (uint64_t)b);
 }
 
-/* engram.rs (CPU reference), `NgramHashState::forward`; the same steps as
- * `EngramHasher::hash` on spark_model/layers/engram_v41.rs, with a batch.
+/* The Euclidean remainder of x by P > 0: the one r in [0, P) with
+ * x - r divisible by P, taken from the exact 128-bit quotient. */
+static int64_t euclid_mod(int64_t x, int64_t P) {
+    __int128 r = (__int128)x % (__int128)P;   /* sign of x, |r| < P */
+    if (r < 0) r += P;
+    return (int64_t)r;
+}
+
+/* How many leading window slots of position p are real ids: the first shift
+ * j (0 <= j < ng) that reaches before position 0 or lands on an unmapped
+ * (-1) id, or ng if none does.  Slot j < cut holds cache[p - j]; slot
+ * j >= cut holds the pad (a blocked slot blocks every larger shift). */
+static int window_cut(const int64_t *seq_cache, int64_t p, int ng) {
+    for (int j = 0; j < ng; ++j)
+        if (j > p || seq_cache[p - j] == -1) return j;
+    return ng;
+}
+
+/* The n-gram hash of the CPU reference page
+ * "metrale_model_arch/deepseek_v41_ref/engram.rs" (module doc, item 1: the
+ * compressed token map, the n-gram window with pad, the look-back cache
+ * carried across the prefill/decode split, a multiplier per look-back slot,
+ * the products XOR-combined, then % prime per (n-gram size, head) plus that
+ * slot's offset), for a batch of sequences.  Written as equations:
+ *
+ *   cache[b][start_pos + s] = token_map[ids[b][s]]          (all s, first)
+ *   w_j(p) = cache[b][p - j]   if j < cut(p),   pad_id otherwise
+ *   for n-gram size g = 2 .. ng and head h, column c = (g - 2) H + h:
+ *     X_g(p)        = XOR_{j = 0 .. g-1} ( w_j(p) *wrap mult[l][j] )
+ *     id[b][s][l][c] = euclid_mod(X_g(p), primes[l][c]) + offsets[l][c]
  *
  *   token_map [vocab]          compressed id per token, -1 = unmapped
  *   pad_id                     token_map[pad token]
- *   mult    [L * ng]           multipliers[layer][lookback]
- *   primes  [L * C]            primes[layer][(ngram - 2) * H + head]
- *   offsets [L * C]            offsets[layer][(ngram - 2) * H + head]
+ *   mult    [L * ng]           multiplier of look-back slot j in layer l
+ *   primes  [L * C]            prime of column c = (g - 2) H + h in layer l
+ *   offsets [L * C]            row offset of that column in layer l's table
  *   cache   [B * max_seq]      compressed ids of every position seen (in/out)
  *   ids     [B * T]            input token ids at positions start_pos ..
  *   out     [B * T * L * C]    row ids
  *
- * All hash arithmetic is i64 with two's-complement wrap; `% prime` is the
- * Euclidean (non-negative) remainder.  Column (n - 1) * H + h holds the
- * (n + 1)-gram of head h.  Inputs are checked before the cache is touched. */
+ * Inputs are checked before the cache is touched. */
 int orc_hash(const int64_t *token_map, int64_t vocab, int64_t pad_id,
              const int64_t *mult, const int64_t *primes, const int64_t *offsets,
              int L, int ng, int H, int64_t *cache, int B, int64_t max_seq,
@@ -179,36 +207,28 @@ int orc_hash(const int64_t *token_map, int64_t vocab, int64_t pad_id,
     for (int64_t i = 0; i < (int64_t)B * T; ++i)
         if (ids[i] < 0 || ids[i] >= vocab) return ORC_E_TOKEN;
 
-    /* The new positions enter the cache before any window is formed. */
+    /* Every new position enters the cache before any window is formed. */
     for (int b = 0; b < B; ++b)
         for (int s = 0; s < T; ++s)
             cache[(int64_t)b * max_seq + start_pos + s] = token_map[ids[(int64_t)b * T + s]];
 
-    int64_t tokens[64];
     for (int b = 0; b < B; ++b) {
+        const int64_t *seq_cache = cache + (int64_t)b * max_seq;
         for (int s = 0; s < T; ++s) {
-            const int64_t pos = start_pos + s;
-            /* Once a shift reaches before position 0 or an unmapped (-1) id,
-             * it and every larger shift take the pad. */
-            int blocked = 0;
-            for (int shift = 0; shift < ng; ++shift) {
-                const int64_t src_pos = pos >= shift ? pos - shift : 0;
-                const int64_t src = cache[(int64_t)b * max_seq + src_pos];
-                blocked = blocked || pos < shift || src == -1;
-                tokens[shift] = blocked ? pad_id : src;
-            }
-            for (int li = 0; li < L; ++li) {
-                const int64_t *m = mult + (int64_t)li * ng;
-                int64_t rolling = wrapping_mul(tokens[0], m[0]);
-                for (int i = 1; i < ng; ++i) {
-                    rolling ^= wrapping_mul(tokens[i], m[i]);
+            const int64_t p = start_pos + s;
+            const int cut = window_cut(seq_cache, p, ng);
+            for (int l = 0; l < L; ++l) {
+                for (int g = 2; g <= ng; ++g) {
+                    /* X_g: the g-slot window, each slot times its multiplier */
+                    int64_t X = 0;
+                    for (int j = 0; j < g; ++j) {
+                        const int64_t w = j < cut ? seq_cache[p - j] : pad_id;
+                        X ^= wrapping_mul(w, mult[(int64_t)l * ng + j]);
+                    }
                     for (int h = 0; h < H; ++h) {
-                        const int col = (i - 1) * H + h;
-                        const int64_t p = primes[(int64_t)li * C + col];
-                        int64_t r = rolling % p;
-                        if (r < 0) r += p;
-                        out[(((int64_t)b * T + s) * L + li) * C + col] =
-                            wrapping_add(r, offsets[(int64_t)li * C + col]);
+                        const int c = (g - 2) * H + h;
+                        out[(((int64_t)b * T + s) * L + l) * C + c] =
+                            wrapping_add(euclid_mod(X, primes[(int64_t)l * C + c]), offsets[(int64_t)l * C + c]);
                     }
                 }
             }

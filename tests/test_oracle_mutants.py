@@ -21,25 +21,29 @@ HASH, FORMATS, LINGATE = pins_hash, pins_formats, pins_linear_gate
 # (name, text in oracle.c, replacement, pin modules that must catch it)
 MUTANTS = [
     # stage 1: the hash
-    ("hash: XOR roll dropped", "rolling ^= wrapping_mul(tokens[i], m[i]);",
-     "rolling = wrapping_mul(tokens[i], m[i]);", [HASH]),
-    ("hash: truncated remainder", "if (r < 0) r += p;", "", [HASH]),
-    ("hash: window shifted by one", "const int64_t src_pos = pos >= shift ? pos - shift : 0;",
-     "const int64_t src_pos = pos >= shift + 1 ? pos - shift - 1 : 0;", [HASH]),
-    ("hash: blocking not carried to larger shifts", "blocked = blocked || pos < shift || src == -1;",
-     "blocked = pos < shift || src == -1;", [HASH]),
-    ("hash: unmapped id not blocked", "blocked = blocked || pos < shift || src == -1;",
-     "blocked = blocked || pos < shift;", [HASH]),
-    ("hash: first layer's offsets for every layer", "wrapping_add(r, offsets[(int64_t)li * C + col]);",
-     "wrapping_add(r, offsets[col]);", [HASH]),
-    ("hash: multipliers indexed [shift][layer]", "rolling ^= wrapping_mul(tokens[i], m[i]);",
-     "rolling ^= wrapping_mul(tokens[i], mult[(int64_t)i * L + li]);", [HASH]),
-    ("hash: columns head-major", "const int col = (i - 1) * H + h;",
-     "const int col = h * (ng - 1) + (i - 1);", [HASH]),
-    ("hash: roll starts from zero", "int64_t rolling = wrapping_mul(tokens[0], m[0]);", "int64_t rolling = 0;",
-     [HASH]),
-    ("hash: unsigned remainder", "int64_t r = rolling % p;",
-     "int64_t r = (int64_t)((uint64_t)rolling % (uint64_t)p);", [HASH]),
+    ("hash: XOR combine dropped (last slot only)", "X ^= wrapping_mul(w, mult[(int64_t)l * ng + j]);",
+     "X = wrapping_mul(w, mult[(int64_t)l * ng + j]);", [HASH]),
+    ("hash: products added instead of XOR-combined", "X ^= wrapping_mul(w, mult[(int64_t)l * ng + j]);",
+     "X = wrapping_add(X, wrapping_mul(w, mult[(int64_t)l * ng + j]));", [HASH]),
+    ("hash: truncated remainder", "if (r < 0) r += P;", "", [HASH]),
+    ("hash: unsigned remainder", "__int128 r = (__int128)x % (__int128)P;",
+     "__int128 r = (__int128)((uint64_t)x % (uint64_t)P);", [HASH]),
+    ("hash: window shifted by one", "const int64_t w = j < cut ? seq_cache[p - j] : pad_id;",
+     "const int64_t w = j < cut && p > j ? seq_cache[p - j - 1] : pad_id;", [HASH]),
+    ("hash: blocking not carried to larger shifts", "const int64_t w = j < cut ? seq_cache[p - j] : pad_id;",
+     "const int64_t w = j <= p && seq_cache[p - j] != -1 ? seq_cache[p - j] : pad_id;", [HASH]),
+    ("hash: unmapped id not blocked", "if (j > p || seq_cache[p - j] == -1) return j;",
+     "if (j > p) return j;", [HASH]),
+    ("hash: first layer's offsets for every layer", "offsets[(int64_t)l * C + c]);",
+     "offsets[c]);", [HASH]),
+    ("hash: multipliers indexed [shift][layer]", "X ^= wrapping_mul(w, mult[(int64_t)l * ng + j]);",
+     "X ^= wrapping_mul(w, mult[(int64_t)j * L + l]);", [HASH]),
+    ("hash: columns head-major", "const int c = (g - 2) * H + h;",
+     "const int c = h * (ng - 1) + (g - 2);", [HASH]),
+    ("hash: the window's first slot left out", "for (int j = 0; j < g; ++j) {",
+     "for (int j = 1; j < g; ++j) {", [HASH]),
+    ("hash: the (n+1)-gram one slot short", "for (int j = 0; j < g; ++j) {",
+     "for (int j = 0; j < g - 1; ++j) {", [HASH]),
     ("hash: new positions never enter the cache",
      "cache[(int64_t)b * max_seq + start_pos + s] = token_map[ids[(int64_t)b * T + s]];", "(void)0;", [HASH]),
     # number formats and table rows
