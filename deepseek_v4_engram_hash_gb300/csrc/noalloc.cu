@@ -30,6 +30,9 @@ extern "C" int engram_forward_noalloc(engram_hasher *hs, const engram_layer *lay
     int batch = 0;
     if (!engram::hasher_geometry(hs, &g, &batch)) return ENGRAM_E_NULL;
     if (T < 0) return ENGRAM_E_INVALID;
+    // No tokens: the same checks and the same no-op as engram_forward; no
+    // scratch is touched.
+    if ((int64_t)batch * T == 0) return engram_forward(hs, layers, d_ids, T, start_pos, d_h, eps, nullptr, 0, stream);
     const size_t need = engram_workspace_bytes(&g, (int64_t)batch * T);
     if (need == 0) return ENGRAM_E_INVALID;
     if (need > kNoAllocScratchBytes) return ENGRAM_E_NOALLOC_LIMIT;

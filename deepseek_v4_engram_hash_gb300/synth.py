@@ -202,17 +202,33 @@ def table_q2k_rows(cfg, layer: int, rows, tag: str = "q2k") -> np.ndarray:
     return out
 
 
+def _chunked(n: int, step: int, fn) -> None:
+    """fn(a, b) over [0, n) in chunks of `step`, on a few threads when there
+    are several chunks (numpy and torch release the GIL on large arrays; each
+    chunk writes its own slice, so the result does not depend on the order)."""
+    starts = list(range(0, n, step))
+    if len(starts) <= 1:
+        for a in starts:
+            fn(a, min(n, a + step))
+        return
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=min(len(starts), os.cpu_count() or 1, 16)) as ex:
+        list(ex.map(lambda a: fn(a, min(n, a + step)), starts))
+
+
 def wkv_rows(cfg, layer: int, rows, sigma: float = 0.02) -> np.ndarray:
     """Rows of wkv [N, K] as bf16 bits, N(0, sigma^2)."""
     rows = np.atleast_1d(np.asarray(rows, dtype=np.uint64)).ravel()
     K = cfg.K
     key = stream_key(cfg.seed, f"wkv.{layer}")
     out = np.empty((rows.size, K), dtype=np.uint16)
-    step = max(1, (1 << 22) // K)
-    for a in range(0, rows.size, step):
-        r = rows[a:a + step]
+
+    def fill(a, b):
+        r = rows[a:b]
         idx = r[:, None] * np.uint64(K) + np.arange(K, dtype=np.uint64)[None, :]
-        out[a:a + step] = to_bf16_bits(normal_f32(key, idx, sigma)).reshape(r.size, K)
+        out[a:b] = to_bf16_bits(normal_f32(key, idx, sigma)).reshape(r.size, K)
+
+    _chunked(rows.size, max(1, (1 << 20) // K), fill)
     return out
 
 

@@ -53,11 +53,63 @@ def wkv(cfg, layer, out_rows) -> np.ndarray:
     return synth.wkv_rows(cfg, layer, out_rows)
 
 
+_WKV_FULL = {}
+
+
+def wkv_full(cfg, layer) -> np.ndarray:
+    """All N rows of wkv (bf16 bits), regenerated on the CPU once per
+    (seed, layer, shape, format) and kept for the session."""
+    key = (cfg.seed, layer, cfg.N, cfg.K, getattr(cfg, "wkv_fmt", "bf16"))
+    w = _WKV_FULL.get(key)
+    if w is None:
+        if len(_WKV_FULL) >= 4:
+            _WKV_FULL.clear()
+        w = wkv(cfg, layer, np.arange(cfg.N))
+        _WKV_FULL[key] = w
+    return w
+
+
 def kv(cfg, layer, x_bits, out_rows=None) -> np.ndarray:
     """kv [M, len(out_rows)] bf16 bits; out_rows defaults to all N outputs."""
     if out_rows is None:
-        out_rows = np.arange(cfg.N)
+        return oracle.linear_bf16(x_bits, wkv_full(cfg, layer))
     return oracle.linear_bf16(x_bits, wkv(cfg, layer, out_rows))
+
+
+def e2e_highway(cfg, h0, kv_gpu, kv_orc, h_gpu):
+    """The end-to-end highway check: the oracle's gates run on the oracle's
+    own kv (kv_orc, one [M, N] bf16 array a layer) from h0, and the GPU's
+    highway h_gpu is compared with that result against the bound the
+    projection's rounding allows.  With the stage-wise chain s (the oracle's
+    gates on the GPU's kv, kv_gpu) and the end-to-end chain o, layer l adds
+    sigma_s v_s - sigma_o v_o = sigma_s (v_s - v_o) + (sigma_s - sigma_o) v_o
+    to the difference of the two chains, so
+
+      |h_gpu - h_o| <= |h_gpu - h_s| + sum_l (sigma_s |dv| + |dsigma| |v_o|) + rounding
+
+    with |h_gpu - h_s| <= H_TOL (the stage-wise bar) and the rounding of the
+    two chains' f32 updates (a half-ulp of each product sigma v and of each
+    sum, per chain and layer).  Returns (max |h_gpu - h_o|, the smallest bound - |h_gpu - h_o|)."""
+    q_k = [synth.qk_weights(cfg, l) for l in range(cfg.n_layers)]
+    hs = np.array(h0, dtype=np.float32, copy=True)
+    ho = hs.copy()
+    D, hc = cfg.dim, cfg.hc
+    bound = np.full(hs.shape, H_TOL, dtype=np.float64)
+    for l in range(cfg.n_layers):
+        q, k = q_k[l]
+        hs_n, gs = oracle.gate(hs, kv_gpu[l], q, k, hc, D, cfg.eps, return_gate=True)
+        ho_n, go = oracle.gate(ho, kv_orc[l], q, k, hc, D, cfg.eps, return_gate=True)
+        vs = oracle.bf16_bits_to_f32(np.asarray(kv_gpu[l])[:, hc * D:]).astype(np.float64)
+        vo = oracle.bf16_bits_to_f32(np.asarray(kv_orc[l])[:, hc * D:]).astype(np.float64)
+        gs64, go64 = gs.astype(np.float64), go.astype(np.float64)
+        bound += (gs64[:, :, None] * np.abs(vs - vo)[:, None, :]
+                  + np.abs(gs64 - go64)[:, :, None] * np.abs(vo)[:, None, :]
+                  + 2.0 ** -24 * (np.abs(hs_n) + np.abs(ho_n)
+                                  + gs64[:, :, None] * np.abs(vs)[:, None, :]
+                                  + go64[:, :, None] * np.abs(vo)[:, None, :]))
+        hs, ho = hs_n, ho_n
+    dh = np.abs(np.asarray(h_gpu, dtype=np.float64) - ho)
+    return float(dh.max()), float((bound - dh).min())
 
 
 def gate(cfg, layer, h, kv_bits):

@@ -1,0 +1,206 @@
+"""Parity of the decode loop exactly as the benchmark times it.
+
+The benchmark calls engram_forward step after step on one carried highway,
+with the ids already on the device and nothing enqueued between the calls.
+In that mode the launches overlap across steps: a step's hash, row gather and
+first wkv copies run before its dependency wait, beside the previous step's
+gate, and only its kv stores wait for that gate.  These tests run that mode
+and check it three ways:
+
+1. The same steps run again with a device synchronisation after every call
+   (nothing overlaps) give the same bits: the final highway, the last step's
+   kv of every layer and its row ids.
+2. The synchronised run is checked against the oracle step by step: row ids
+   exact for every sequence, kv within 2e-2 on sampled outputs and the
+   highway within 1e-3 stage-wise for the checked sequences, and the highway
+   end to end (the oracle's own kv) against the derived bound on some steps.
+3. One further call after the overlapped chain hashes over the look-back
+   cache that the overlapped steps wrote: its row ids equal the oracle's.
+   (The CPU reference page, "metrale_model_arch/deepseek_v41_ref/engram.rs",
+   module doc item 1: the cache carries the look-back across the
+   prefill/decode split, and each call's positions enter it before any of
+   its windows is formed.)
+
+Workloads: the single-token V4.1-Flash step (bf16 wkv; Q2_K-quantised wkv;
+one-byte e8m0 table scales), eight sequences a step on the same tables, the
+large-table workload (1536-token prefill of eight sequences on 2^20-prime
+tables, then 512 single-token steps of all eight, sequences 0 and 7 checked
+at every step), and the 4096-token prefill followed at once by decode steps.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_glue as G
+from deepseek_v4_engram_hash_gb300 import configs, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def E():
+    import __graft_entry__
+    __graft_entry__.build()
+    from deepseek_v4_engram_hash_gb300 import _lib
+    return _lib
+
+
+def _u16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# name: (config, sequences, decode steps, prefill tokens a sequence, checked sequences, end-to-end every)
+CASES = {
+    "v41_decode_T1": (configs.V41_DECODE, 1, 64, 0, (0,), 4),
+    "v41_decode_T1_wkv_q2k": (configs.V41_DECODE_WKVQ2K, 1, 64, 0, (0,), 4),
+    "v41_decode_T1_e8m0": (configs.V41_DECODE_E8M0, 1, 64, 0, (0,), 4),
+    "v41_decode_B8": (configs.V41_DECODE, 8, 64, 0, (0, 7), 16),
+    "large_table_stress": (configs.STRESS, 8, 512, 1536, (0, 7), 64),
+    "v41_prefill_then_decode": (configs.V41_PREFILL, 1, 64, 4096, (0,), 16),
+}
+
+
+class Chain:
+    """One workload's inputs and the two ways of running its steps."""
+
+    def __init__(self, E, name):
+        from deepseek_v4_engram_hash_gb300 import runner
+        cfg, B, steps, prefill, checked, e2e_every = CASES[name]
+        cfg = cfg.with_(decode_steps=steps + 8)
+        self.E, self.cfg, self.B, self.steps, self.prefill = E, cfg, B, steps, prefill
+        self.checked, self.e2e_every = checked, e2e_every
+        self.eng = runner.EngramSetup(cfg, batch=B, max_tokens=B * max(prefill, 1))
+        self.prefix = cfg.prefix if not prefill else 0
+        self.pre_prefix = self.eng.ids_for("prefix", self.prefix) if self.prefix else None
+        self.pre_ids = self.eng.ids_for("prefill", prefill) if prefill else None
+        dec = self.eng.ids_for("decode", steps + 1)                                  # [B, steps + 1]
+        self.dec_ids = dec
+        self.dec_dev = torch.from_numpy(np.ascontiguousarray(dec.T).reshape(steps + 1, B, 1)).cuda()
+        self.pos0 = self.prefix + prefill
+        self.first_dec = B * prefill                    # global token index of the first decode row
+        self.h_dec0 = synth.highway(cfg, np.arange(self.first_dec, self.first_dec + B))
+
+    def _start(self):
+        """Fresh look-back (zeros, then the hashed prefix) and fresh highways."""
+        E, cfg, eng = self.E, self.cfg, self.eng
+        E.engram_hasher_reset(eng.hasher)
+        if self.prefix:
+            out = torch.empty((self.B, self.prefix, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
+            E.engram_hash(eng.hasher, torch.from_numpy(self.pre_prefix).cuda(), self.prefix, 0, out)
+        d_hp = None
+        if self.prefill:
+            d_hp = torch.empty((self.B * self.prefill, cfg.hc, cfg.dim), dtype=torch.float32, device="cuda")
+            synth.fill_highway_cuda(cfg, d_hp, 0)
+        d_hd = torch.from_numpy(self.h_dec0).cuda()
+        torch.cuda.synchronize()
+        return d_hp, d_hd
+
+    def final_state(self, d_hp, d_hd):
+        cfg, B = self.cfg, self.B
+        return {"h_dec": d_hd.clone(), "h_pre": None if d_hp is None else d_hp.clone(),
+                "kv": [self.eng.kv(B, l).clone() for l in range(cfg.n_layers)],
+                "ids": self.eng.row_ids(B).clone()}
+
+    def run_overlapped(self):
+        """Every call enqueued back to back, nothing between them (the
+        benchmark's timed loop); then one further call."""
+        d_hp, d_hd = self._start()
+        if self.prefill:
+            self.eng.forward(torch.from_numpy(self.pre_ids).cuda(), 0, d_hp)
+        for i in range(self.steps):
+            self.eng.forward(self.dec_dev[i], self.pos0 + i, d_hd)
+        torch.cuda.synchronize()
+        assert self.E.engram_check() == 0
+        final = self.final_state(d_hp, d_hd)
+        extra_h = torch.from_numpy(self.h_dec0).cuda()
+        self.eng.forward(self.dec_dev[self.steps], self.pos0 + self.steps, extra_h)
+        assert self.E.engram_check() == 0
+        extra_ids = self.eng.row_ids(self.B).cpu().numpy()
+        return final, extra_ids
+
+    def run_serialised(self, check_step):
+        """The same calls with a synchronisation after each; check_step(i,
+        h_before, d_hd) runs after step i (the prefill is step -1)."""
+        d_hp, d_hd = self._start()
+        if self.prefill:
+            self.eng.forward(torch.from_numpy(self.pre_ids).cuda(), 0, d_hp)
+            torch.cuda.synchronize()
+            check_step(-1, None, d_hp)
+        for i in range(self.steps):
+            h_before = d_hd.cpu().numpy()
+            self.eng.forward(self.dec_dev[i], self.pos0 + i, d_hd)
+            torch.cuda.synchronize()
+            check_step(i, h_before, d_hd)
+        assert self.E.engram_check() == 0
+        return self.final_state(d_hp, d_hd)
+
+
+def _same_bits(a, b):
+    return torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_back_to_back_decode_matches_serialised_and_oracle(E, name):
+    ch = Chain(E, name)
+    cfg, B, eng = ch.cfg, ch.B, ch.eng
+    overlapped, extra_ids = ch.run_overlapped()
+
+    ref = G.hash_state(cfg, B)
+    if ch.prefix:
+        ref.forward(ch.pre_prefix, 0)
+    outs = np.unique(np.concatenate([np.arange(3, cfg.N, 97), [0, cfg.dim - 1, cfg.dim, cfg.hc * cfg.dim,
+                                                                 cfg.N - 1]]))
+    w_s = [G.wkv_full(cfg, l)[outs] for l in range(cfg.n_layers)]
+    qk = [synth.qk_weights(cfg, l) for l in range(cfg.n_layers)]
+    rows = np.asarray(ch.checked)
+    worst = {"kv": 0.0, "dh": 0.0, "dh_e2e": 0.0, "margin": np.inf, "e2e_steps": 0}
+
+    def check_step(i, h_before, d_h):
+        if i < 0:                                          # the prefill: every row id
+            want = ref.forward(ch.pre_ids, 0).reshape(B * ch.prefill, cfg.n_layers, cfg.cols)
+            got = eng.row_ids(B * ch.prefill).cpu().numpy()
+            assert np.array_equal(got, want), "prefill row ids"
+            return
+        want = ref.forward(ch.dec_ids[:, i:i + 1], ch.pos0 + i).reshape(B, cfg.n_layers, cfg.cols)
+        got = eng.row_ids(B).cpu().numpy()
+        assert np.array_equal(got, want), f"step {i}: row ids"
+        e2e = i % ch.e2e_every == 0 or i == ch.steps - 1
+        h = h_before[rows].copy()
+        kv_g, kv_o = [], []
+        for l in range(cfg.n_layers):
+            kv_gpu = _u16(eng.kv(B, l))[rows]
+            x = G.x_of(cfg, l, want[rows])
+            err = G.kv_rel_err(kv_gpu[:, outs], oracle.linear_bf16(x, w_s[l]))
+            assert err <= G.KV_TOL, f"step {i} layer {l}: kv rel err {err}"
+            worst["kv"] = max(worst["kv"], err)
+            if e2e:
+                kv_o.append(G.kv(cfg, l, x))
+                kv_g.append(kv_gpu)
+            h = oracle.gate(h, kv_gpu, qk[l][0], qk[l][1], cfg.hc, cfg.dim, cfg.eps)
+        got_h = d_h[torch.as_tensor(rows, device=d_h.device)].cpu().numpy()
+        dh = float(np.abs(got_h - h).max())
+        assert dh <= G.H_TOL, f"step {i}: highway |dh| {dh}"
+        worst["dh"] = max(worst["dh"], dh)
+        if e2e:
+            dh_e2e, margin = G.e2e_highway(cfg, h_before[rows], kv_g, kv_o, got_h)
+            assert margin >= 0.0, f"step {i}: end-to-end highway outside the derived bound by {-margin}"
+            worst["dh_e2e"] = max(worst["dh_e2e"], dh_e2e)
+            worst["margin"] = min(worst["margin"], margin)
+            worst["e2e_steps"] += 1
+
+    serial = ch.run_serialised(check_step)
+
+    assert _same_bits(overlapped["h_dec"], serial["h_dec"]), "final highway: overlapped != serialised"
+    if ch.prefill:
+        assert _same_bits(overlapped["h_pre"], serial["h_pre"]), "prefill highway: overlapped != serialised"
+    for l in range(cfg.n_layers):
+        assert _same_bits(overlapped["kv"][l], serial["kv"][l]), f"last step kv {l}: overlapped != serialised"
+    assert torch.equal(overlapped["ids"], serial["ids"]), "last step row ids: overlapped != serialised"
+
+    # one call past the chain, over the cache the overlapped steps wrote
+    want = ref.forward(ch.dec_ids[:, ch.steps:ch.steps + 1], ch.pos0 + ch.steps)
+    assert np.array_equal(extra_ids, want.reshape(B, cfg.n_layers, cfg.cols)), "row ids after the chain"
+    print(f"[back-to-back] {name}: {ch.steps} steps x {B} sequences bit-identical overlapped/serialised; "
+          f"worst kv rel err {worst['kv']:.3g}, stage-wise |dh| {worst['dh']:.3g}, end-to-end |dh| "
+          f"{worst['dh_e2e']:.3g} on {worst['e2e_steps']} steps, smallest margin to the bound {worst['margin']:.3g}")

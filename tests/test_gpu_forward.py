@@ -28,9 +28,12 @@ def _u16(t):
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def _check_call(eng, ref, ids, start_pos, d_h, h0_rows, tok_sample, out_sample, first_token):
+def _check_call(eng, ref, ids, start_pos, d_h, h0_rows, tok_sample, out_sample, first_token, e2e=True):
     """Run one forward and check it.  h0_rows: f32 [len(tok_sample), hc, D] of
-    the highway rows tok_sample before the call (regenerated on the CPU)."""
+    the highway rows tok_sample before the call (regenerated on the CPU).
+    With e2e, the oracle projects the sampled tokens onto every output: kv is
+    checked on all N outputs and the highway end to end (oracle kv) against
+    the derived bound, besides stage-wise."""
     cfg = eng.cfg
     B, T = ids.shape
     M = B * T
@@ -43,18 +46,30 @@ def _check_call(eng, ref, ids, start_pos, d_h, h0_rows, tok_sample, out_sample, 
     h = h0_rows.copy()
     lay = eng.workspace_layout(M)
     x_kept = lay[1 + 2 * cfg.n_layers] > lay[1 + cfg.n_layers]     # GEMM steps keep x in the workspace
+    kv_g, kv_o = [], []
     for l in range(cfg.n_layers):
         kv_gpu = _u16(eng.kv(M, l))[tok_sample]                     # [S, N]
         x = G.x_of(cfg, l, want_ids[tok_sample])
         if x_kept:
             assert np.array_equal(_u16(eng.x(M, l))[tok_sample], x), f"layer {l} x rows"
-        want_kv = G.kv(cfg, l, x, out_sample)
-        err = G.kv_rel_err(kv_gpu[:, out_sample], want_kv)
+        if e2e:
+            want_kv = G.kv(cfg, l, x)                               # every output
+            err = G.kv_rel_err(kv_gpu, want_kv)
+            kv_o.append(want_kv)
+        else:
+            want_kv = G.kv(cfg, l, x, out_sample)
+            err = G.kv_rel_err(kv_gpu[:, out_sample], want_kv)
         assert err <= G.KV_TOL, f"layer {l} kv rel err {err}"
+        kv_g.append(kv_gpu)
         h = G.gate(cfg, l, h, kv_gpu)                               # stage-wise
     got_h = d_h.view(M, cfg.hc, cfg.dim)[torch.as_tensor(tok_sample, device=d_h.device)].cpu().numpy()
     dh = np.abs(got_h - h).max()
     assert dh <= G.H_TOL, f"highway |dh| {dh}"
+    if e2e:
+        dh_e2e, margin = G.e2e_highway(cfg, h0_rows, kv_g, kv_o, got_h)
+        print(f"[e2e] {cfg.name} T={T} B={B}: stage-wise |dh| {dh:.3g}; end-to-end |dh| {dh_e2e:.3g}, "
+              f"smallest margin to the bound {margin:.3g}")
+        assert margin >= 0.0, f"end-to-end highway outside the derived bound by {-margin}"
     return dh
 
 
@@ -125,7 +140,7 @@ def test_forward_stress_batch8_prefill_then_decode(E):
     ids = eng.ids_for("prefill", cfg.T)
     M = B * cfg.T
     d_h = _h_device(cfg, 0, M, False)
-    toks = _sample(rng, M, 16)
+    toks = _sample(rng, M, 256)
     _check_call(eng, ref, ids, 0, d_h, synth.highway(cfg, toks), toks, outs, 0)
     pos, first = cfg.T, M
     for step in range(3):                               # single-token decode of all 8 sequences

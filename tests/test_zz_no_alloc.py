@@ -1,7 +1,8 @@
 """engram_forward_noalloc: the forward for callers that cannot allocate device
 memory (a host that owns every allocation, a loop that must not enter the
-allocator).  Its scratch is the library's fixed 4 MiB device array, so its
-results must equal those of engram_forward with a caller-allocated workspace.
+allocator).  Its scratch is the library's fixed 4 MiB device array; it runs
+the kernels of engram_forward with a caller-allocated workspace, so its results
+must equal that forward's bit for bit.
 
 This file is collected last so that a stop-at-first-failure run has already
 run every other test; it also passes alone in a fresh process.
@@ -13,9 +14,6 @@ import torch
 from deepseek_v4_engram_hash_gb300 import configs, synth
 
 pytestmark = pytest.mark.gpu
-
-H_TOL = 1e-3        # the highway tolerance the other parity tests use
-
 
 @pytest.fixture(scope="module")
 def E():
@@ -38,6 +36,10 @@ def _twin_hashers(E, eng, cfg, batch, prefix):
 
 @pytest.mark.parametrize("name,batch,T", [("v41_decode_T1", 1, 1), ("tiny", 2, 5)])
 def test_noalloc_matches_forward_two_calls_in_a_row(E, name, batch, T):
+    """Both entry points run the same kernels on the same inputs; only where
+    the scratch lives differs, so the highway must agree bit for bit on each
+    of two calls in a row (a stale or misplaced scratch region would show),
+    and both hashers must carry the same look-back afterwards."""
     from deepseek_v4_engram_hash_gb300 import runner
     cfg = configs.CONFIGS[name]
     eng = runner.EngramSetup(cfg, batch=batch, max_tokens=batch * T)
@@ -52,10 +54,37 @@ def test_noalloc_matches_forward_two_calls_in_a_row(E, name, batch, T):
         E.engram_forward(eng.hasher, eng.layers, ids, T, pos, d_h_ref, cfg.eps, eng.ws, eng.ws_bytes)
         E.engram_forward_noalloc(hs2, eng.layers, ids, T, pos, d_h_new, cfg.eps)
         assert E.engram_check() == 0
-        diff = (d_h_ref - d_h_new).abs().max().item()
-        assert diff <= H_TOL, f"call {call}: |dh| {diff}"
+        assert torch.equal(d_h_ref.view(torch.int32), d_h_new.view(torch.int32)), \
+            f"call {call}: |dh| {(d_h_ref - d_h_new).abs().max().item()}"
         assert not torch.equal(d_h_new, torch.from_numpy(h0).cuda())      # the gate did run
         pos += T
+    # the look-back each hasher carries: the next window's row ids agree
+    nxt = torch.from_numpy(eng.ids_for("noalloc-next", 1)).cuda()
+    a = torch.empty((batch, 1, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
+    b = torch.empty_like(a)
+    E.engram_hash(eng.hasher, nxt, 1, pos, a)
+    E.engram_hash(hs2, nxt, 1, pos, b)
+    assert E.engram_check() == 0
+    assert torch.equal(a, b)
+
+
+def test_noalloc_zero_tokens_is_a_no_op(E):
+    """T = 0 is a valid no-op here as in engram_forward; a position past the
+    hasher's capacity is refused the same way by both."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = configs.TINY
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=cfg.T)
+    ids = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    d_h = torch.zeros((1, cfg.hc, cfg.dim), dtype=torch.float32, device="cuda")
+    E.engram_forward_noalloc(eng.hasher, eng.layers, ids, 0, 0, d_h, cfg.eps)
+    assert E.engram_check() == 0
+    assert not d_h.any().item()
+    for call in (lambda: E.engram_forward(eng.hasher, eng.layers, ids, 0, cfg.max_seq + 1, d_h, cfg.eps,
+                                          eng.ws, eng.ws_bytes),
+                 lambda: E.engram_forward_noalloc(eng.hasher, eng.layers, ids, 0, cfg.max_seq + 1, d_h, cfg.eps)):
+        with pytest.raises(E.EngramError) as e:
+            call()
+        assert e.value.code == -4
 
 
 def test_noalloc_refuses_more_than_its_scratch(E):
