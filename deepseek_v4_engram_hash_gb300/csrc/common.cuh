@@ -224,12 +224,27 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// The same test, letting the thread sleep until the phase completes or about
+// hint_ns pass (so a warp that waits long issues few instructions).
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait: false if the CTA is aborting or the wait ran out (then it
-// raises the abort flag and the device error word).
+// raises the abort flag and the device error word).  sleep_ns > 0: each test
+// may sleep that long (roles that wait for long stretches: the copy warp, the
+// reducing warp).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int *err, uint64_t limit_ns = kWaitNs) {
+                                          int *err, uint64_t limit_ns = kWaitNs, uint32_t sleep_ns = 0) {
     const uint64_t t0 = now_ns();
-    while (!mbar_try(bar, parity)) {
+    while (!(sleep_ns ? mbar_try_sleep(bar, parity, sleep_ns) : mbar_try(bar, parity))) {
         if (*abort_flag) return false;
         if (now_ns() - t0 > limit_ns) {
             *abort_flag = 1;

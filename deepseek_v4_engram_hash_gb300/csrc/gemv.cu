@@ -69,14 +69,21 @@ __device__ __forceinline__ void hash_ids(const GemvArgs &a, int T, int li, int c
 // hit distinct 16-byte bank groups) and token g's x feed two mma instructions.
 // ---------------------------------------------------------------------------
 constexpr int kMmaT = 8;
-constexpr int kMmaWarps = 16;                           // MMA warps; one more warp copies
-constexpr int kMmaThreads = (kMmaWarps + 1) * 32;
+constexpr int kMmaWarps = 16;                           // MMA warps; then a copy warp and a reducing warp
+constexpr int kMmaThreads = (kMmaWarps + 2) * 32;
 constexpr int kMmaJ = 4;                                // 32-wide k blocks a warp per stage
 constexpr int kStageKb = kMmaWarps * kMmaJ;             // 64 k blocks (2048 values) a bf16 stage
 constexpr int kMmaSubMax = 3;                           // bf16 stages a 16-row group
 static_assert(kMmaSubMax * kStageKb * 32 == kGemvMaxK, "x fragments cover K");
 constexpr uint32_t kRowBytes = kStageKb * 64 + 64;      // one row's piece + bank padding
-constexpr uint32_t kRedBytes = 2 * kMmaWarps * 32 * 16; // partial tiles, double-buffered
+// Sleep hint of the reducing warp's waits, and of the copy warp's when the MMA
+// warps are bound by the Q2_K decode (its waits are long; a sleeping warp
+// leaves the issue slots to the decode: 53.9 -> 53.5 us a step).  Streaming
+// bf16 wkv, the copy warp re-issues as soon as a stage frees: no sleep.
+constexpr uint32_t kRoleSleepNs = 20000;
+constexpr int kRedSlots = 2;                            // partial-tile slots between the MMA warps and the reducer
+constexpr uint32_t kRedSlotFloats = kMmaWarps * 32 * 4; // one 16 x 8 f32 tile a warp
+constexpr uint32_t kRedBytes = kRedSlots * kRedSlotFloats * 4;
 static_assert((size_t)kFusedHashMaxIds * 8 <= kRedBytes, "hashed ids are staged in the partial buffer");
 
 template <bool WQ2K>
@@ -95,9 +102,10 @@ struct Ring<true> {
 };
 template <bool WQ2K>
 constexpr size_t ring_smem_bytes() {
-    // ring, partials, full/empty barriers, then the abort flag and each slot's group
-    return (size_t)Ring<WQ2K>::kStages * Ring<WQ2K>::kStageBytes + kRedBytes + 2 * Ring<WQ2K>::kStages * 8 + 16 +
-           4 * Ring<WQ2K>::kStages;
+    // ring, partial slots, the ring's full/empty and the slots' full/empty barriers, then the abort
+    // and dependency flags, each ring slot's group and each partial slot's group
+    return (size_t)Ring<WQ2K>::kStages * Ring<WQ2K>::kStageBytes + kRedBytes +
+           (2 * Ring<WQ2K>::kStages + 2 * kRedSlots) * 8 + 16 + 4 * Ring<WQ2K>::kStages + 4 * kRedSlots;
 }
 static_assert(ring_smem_bytes<false>() <= 227 * 1024 && ring_smem_bytes<true>() <= 227 * 1024, "shared memory");
 
@@ -138,21 +146,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 __device__ __forceinline__ void mma_warps_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(kMmaWarps * 32) : "memory");
 }
-// The same barrier, returning whether any MMA thread passed p: a decision that
-// every MMA warp takes alike.
-__device__ __forceinline__ bool mma_warps_any(bool p) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)p), "r"(kMmaWarps * 32)
-        : "memory");
-    return r != 0;
-}
-
 // Small non-negative integer -> f32 without the quarter-rate conversion unit:
 // 2^23 + n has n in its low mantissa bits, so subtracting 2^23 is exact.
 __device__ __forceinline__ float small_u2f(uint32_t n) {
@@ -187,6 +180,18 @@ __device__ __forceinline__ Q2kHalf q2k_half(const uint8_t *blk, int half, int q)
     h.dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
     return h;
 }
+// The same table from the scale byte in place: sc & 15 and (sc & 0xF0) = 16 m
+// both become exact floats by one OR each (2^23 + n), and dmin * m is taken as
+// (dmin * 16 m) / 16 -- both products exact in f32 (11-bit dmin times at most
+// 8 bits), so the values are bit-identical to q2k_table's.
+__device__ __forceinline__ uint2 q2k_table_b(uint32_t sc, float d, float dmin) {
+    const float s_lo = __uint_as_float((sc & 0xFu) | 0x4B000000u) - 8388608.0f;
+    const float m16 = __uint_as_float((sc & 0xF0u) | 0x4B000000u) - 8388608.0f;
+    const float dl = __fmul_rn(d, s_lo);
+    const float nml = __fmul_rn(-__fmul_rn(dmin, m16), 0.0625f);
+    return make_uint2(pack_bf16x2(__fmaf_rn(dl, 0.0f, nml), __fmaf_rn(dl, 1.0f, nml)),
+                      pack_bf16x2(__fmaf_rn(dl, 2.0f, nml), __fmaf_rn(dl, 3.0f, nml)));
+}
 // v[0..3] as bf16 pairs (v0 v1, v2 v3) for the sub-block scale byte sc
 __device__ __forceinline__ uint2 q2k_table(uint32_t sc, float d, float dmin) {
     const float dl = __fmul_rn(d, small_u2f(sc & 15u));
@@ -194,7 +199,11 @@ __device__ __forceinline__ uint2 q2k_table(uint32_t sc, float d, float dmin) {
     return make_uint2(pack_bf16x2(__fmaf_rn(dl, 0.0f, nml), __fmaf_rn(dl, 1.0f, nml)),
                       pack_bf16x2(__fmaf_rn(dl, 2.0f, nml), __fmaf_rn(dl, 3.0f, nml)));
 }
-// four values v[t_0..3] as bf16 pairs, quants t one a byte
+// four values v[t_0..3] as bf16 pairs, quants t one a byte.  With A = t * 0x22
+// (< 2^31), the 64-bit t * 0x00220022 is A + A * 2^16: its high word is A >> 16
+// (the low half's carry, (A & 0xFFFF) + (A >> 16) <= 0xCCCC, never reaches
+// bit 16) and its low 16 bits are those of A -- the selectors of values 2, 3
+// and of values 0, 1, each with 0x1010 added, from one multiply-add.
 __device__ __forceinline__ uint2 q2k_pick4(uint2 v, uint32_t t) {
     const uint32_t s = t * 0x22u + 0x10101010u;
     return make_uint2(__byte_perm(v.x, v.y, s), __byte_perm(v.x, v.y, s >> 16));
@@ -327,11 +336,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     float *red = reinterpret_cast<float *>(smem_raw + R::kStages * R::kStageBytes);
     int64_t *s_ids = reinterpret_cast<int64_t *>(red);                                   // until x is gathered
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::kStages * R::kStageBytes + kRedBytes);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * R::kStages);
-    volatile int *stage_grp = abort_flag + 1;   // [kStages]: the group of the stage in the slot, -1 at the end
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * R::kStages + 2 * kRedSlots);
+    volatile int *dep_ok = abort_flag + 1;      // set once the kv stores may start (the dependency wait passed)
+    volatile int *stage_grp = abort_flag + 4;   // [kStages]: the group of the stage in the slot, -1 at the end
+    volatile int *slot_grp = stage_grp + R::kStages;   // [kRedSlots]: the group of the partials in the slot
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int b) { return bar0 + 8u * b; };
     auto empty = [&](int b) { return bar0 + 8u * (R::kStages + b); };
+    auto red_full = [&](int b) { return bar0 + 8u * (2 * R::kStages + b); };
+    auto red_empty = [&](int b) { return bar0 + 8u * (2 * R::kStages + kRedSlots + b); };
 
     const int ctas_per_layer = gridDim.x / a.L;
     const int li = blockIdx.x / ctas_per_layer;
@@ -345,13 +358,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     const int groups_total = (N + 15) / 16;
     const int spg = WQ2K ? 1 : nsub;                                     // stages a group
     const bool producer = warp == kMmaWarps;
+    const bool reducer = warp == kMmaWarps + 1;
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < R::kStages; ++b) {
             mbar_init(full(b), 1);
             mbar_init(empty(b), kMmaWarps);
         }
+        for (int b = 0; b < kRedSlots; ++b) {
+            mbar_init(red_full(b), kMmaWarps);
+            mbar_init(red_empty(b), 1);
+        }
         *abort_flag = 0;
+        *dep_ok = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -375,7 +394,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     auto issue_one = [&]() -> bool {
         const int i = issued, b = i % R::kStages;
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(empty(b), ((i / R::kStages) & 1) ^ 1, abort_flag, a.err);
+        if (lane == 0)
+            ok = mbar_wait(empty(b), ((i / R::kStages) & 1) ^ 1, abort_flag, a.err, kWaitNs, WQ2K ? kRoleSleepNs : 0);
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
             ended = true;
             return false;
@@ -434,10 +454,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     // Hashing here from a host position, the hash and the gather read only the
     // inputs, the constant tables and the cache entries of earlier steps; the
     // projection that wrote those had finished before the gate between it and
-    // this grid let this grid launch (every kernel of the step signals its
-    // dependents only after its own wait).  So they run before the wait, beside
-    // the previous step's gate, and only the kv stores (which that gate reads)
-    // wait for it.  A device position is advanced by that gate: wait first.
+    // this grid let this grid launch (that gate signals its dependents only
+    // after its own wait).  The wkv stream and the products read only
+    // constants.  So all of that runs beside the previous step's gate, and only
+    // the kv stores (which that gate reads) wait for it: the reducing warp
+    // waits, and this grid signals its own dependents only after that wait.  A
+    // device position is advanced by that gate: then everything waits first.
     const bool early = HASH && a.hash.start_pos_dev == nullptr;
     if (a.pdl && !early) {
         griddep_wait();
@@ -473,18 +495,54 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
                 atomicExch(a.sched + 2 * li + 1, 0);
             }
         }
+        if (a.pdl && early && *dep_ok) griddep_launch();
+        return;
+    }
+
+    if (reducer) {
+        // Sums each group's 16 partial tiles in warp order and stores the group's
+        // kv rows: lane l takes the four outputs of tile lane l (c0: row g,
+        // token 2q; c1: row g, token 2q + 1; c2, c3: row g + 8), g = l / 4, q = l % 4.
+        if (a.pdl && early) {
+            griddep_wait();
+            if (lane == 0) *dep_ok = 1;
+            griddep_launch();
+        }
+        const int gg = lane >> 2, qq = lane & 3;
+        for (int gi = 0;; ++gi) {
+            const int slot = gi % kRedSlots;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(red_full(slot), (gi / kRedSlots) & 1, abort_flag, a.err, kWaitNs,
+                                                   kRoleSleepNs)))
+                break;
+            const int grp = slot_grp[slot];
+            if (grp < 0) break;
+            const float4 *rb = reinterpret_cast<const float4 *>(red + slot * kRedSlotFloats);
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w = 0; w < kMmaWarps; ++w) {
+                const float4 p = rb[w * 32 + lane];
+                v[0] += p.x;
+                v[1] += p.y;
+                v[2] += p.z;
+                v[3] += p.w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(red_empty(slot));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int r = grp * 16 + gg + ((j & 2) ? 8 : 0), t = 2 * qq + (j & 1);
+                if (r < N && t < T) ly.kv[(size_t)t * N + r] = (uint16_t)f32_to_bf16_bits(v[j]);
+            }
+        }
         return;
     }
 
     uint4 xr[kMmaSubMax][kMmaJ];
     gather_x(a, ly, ids, id_stride, nsub, warp, g, q, xr);
-    mma_warps_sync();                      // every warp has read the hashed ids: the partial buffer is free
-    if (a.pdl && early) {
-        griddep_wait();
-        griddep_launch();
-    }
+    mma_warps_sync();                      // every warp has read the hashed ids: the partial slots are free
 
     bool live = true;
+    bool triggered = !(a.pdl && early);    // signalled already (or nothing to signal)
     // wait for stage i: false (for the whole warp) once the CTA is aborting
     auto acquire = [&](int i) {
         const bool ok = live && mbar_wait(full(i % R::kStages), (i / R::kStages) & 1, abort_flag, a.err);
@@ -497,94 +555,100 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     };
     const uint32_t a_off = g * kRowBytes + (warp * kMmaJ) * 64 + 16 * q;
     // Q2_K: this lane's scale byte in a scale word, and the quant shifts 2j of blocks jj = 0, 1
-    const uint32_t sc_sh = 8u * (2u * (q & 1) + (q >> 1));
+    const int sc_byte = 8 * (warp & 1) + 2 * (q & 1) + (q >> 1);
     const uint32_t q_sh0 = 2u * (q & 1), q_sh1 = 2u - q_sh0;
     for (int gi = 0;; ++gi) {
-        // the group's first stage names the group; every MMA warp leaves at the
-        // end marker, or when any of them finds the CTA aborting
+        // the group's first stage names the group (-1: the end marker, the
+        // same for every warp); a warp that finds the CTA aborting leaves
         const int i0 = gi * spg;
         const int grp = acquire(i0) ? stage_grp[i0 % R::kStages] : -1;
-        if (mma_warps_any(grp < 0)) break;
+        if (!live) break;
         float c[4] = {0.f, 0.f, 0.f, 0.f};
-        if (WQ2K) {
-            // this warp's blocks 8 s + w/2, half w % 2, of rows g and g + 8
-            const uint8_t *row_lo = smem_raw + (gi % R::kStages) * R::kStageBytes + g * q2k_row +
-                                    (warp >> 1) * 84;
-            const uint8_t *row_hi = row_lo + 8 * q2k_row;
+        if (grp >= 0) {
+            if (WQ2K) {
+                // this warp's blocks 8 s + w/2, half w % 2, of rows g and g + 8
+                const uint8_t *row_lo = smem_raw + (gi % R::kStages) * R::kStageBytes + g * q2k_row +
+                                        (warp >> 1) * 84;
+                const uint8_t *row_hi = row_lo + 8 * q2k_row;
 #pragma unroll
-            for (int sub = 0; sub < kMmaSubMax; ++sub) {
-                if (sub < nsub && sub * kStageKb + warp * kMmaJ < kblocks) {
-                    const Q2kHalf hl = q2k_half(row_lo + sub * 8 * 84, warp & 1, q);
-                    const Q2kHalf hh = q2k_half(row_hi + sub * 8 * 84, warp & 1, q);
-                    // Block jj of the lane is shift j = jj ^ q%2.  At jj = 0, 2 the lane
-                    // builds the value table of its sub-block (scale byte 2 (q%2) + q/2 of
-                    // word jj/2); at jj = 1, 3 it needs shift j ^ 1 of the same pair,
-                    // whose table lane q ^ 1 (same row, same sub-block) built at jj - 1.
-                    uint2 vl[kMmaJ], vh[kMmaJ];
+                for (int sub = 0; sub < kMmaSubMax; ++sub) {
+                    if (sub < nsub && sub * kStageKb + warp * kMmaJ < kblocks) {
+                        const uint8_t *bl = row_lo + sub * 8 * 84, *bh = row_hi + sub * 8 * 84;
+                        const Q2kHalf hl = q2k_half(bl, warp & 1, q);
+                        const Q2kHalf hh = q2k_half(bh, warp & 1, q);
+                        // Block jj of the lane is shift j = jj ^ q%2.  At jj = 0, 2 the lane
+                        // builds the value table of its sub-block (scale byte 2 (q%2) + q/2 of
+                        // word jj/2); at jj = 1, 3 it needs shift j ^ 1 of the same pair,
+                        // whose table lane q ^ 1 (same row, same sub-block) built at jj - 1.
+                        uint2 vl[kMmaJ], vh[kMmaJ];
 #pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        vl[2 * p] = q2k_table(((p ? hl.sc23 : hl.sc01) >> sc_sh) & 0xFFu, hl.d, hl.dmin);
-                        vh[2 * p] = q2k_table(((p ? hh.sc23 : hh.sc01) >> sc_sh) & 0xFFu, hh.d, hh.dmin);
-                    }
+                        for (int p = 0; p < 2; ++p) {
+                            vl[2 * p] = q2k_table_b(bl[sc_byte + 4 * p], hl.d, hl.dmin);
+                            vh[2 * p] = q2k_table_b(bh[sc_byte + 4 * p], hh.d, hh.dmin);
+                        }
 #pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        vl[2 * p + 1] = make_uint2(__shfl_xor_sync(0xFFFFFFFFu, vl[2 * p].x, 1),
-                                                   __shfl_xor_sync(0xFFFFFFFFu, vl[2 * p].y, 1));
-                        vh[2 * p + 1] = make_uint2(__shfl_xor_sync(0xFFFFFFFFu, vh[2 * p].x, 1),
-                                                   __shfl_xor_sync(0xFFFFFFFFu, vh[2 * p].y, 1));
-                    }
-#pragma unroll
-                    for (int jj = 0; jj < kMmaJ; ++jj) {
-                        const uint32_t sh = ((jj & 1) ? q_sh1 : q_sh0) + ((jj & 2) ? 4u : 0u);    // 2j
-                        const uint2 l0 = q2k_pick4(vl[jj], (hl.q0 >> sh) & 0x03030303u);
-                        const uint2 l1 = q2k_pick4(vl[jj], (hl.q1 >> sh) & 0x03030303u);
-                        const uint2 h0 = q2k_pick4(vh[jj], (hh.q0 >> sh) & 0x03030303u);
-                        const uint2 h1 = q2k_pick4(vh[jj], (hh.q1 >> sh) & 0x03030303u);
-                        const uint4 xb = xr[sub][jj];
-                        mma_16816(c, l0.x, h0.x, l0.y, h0.y, xb.x, xb.y);
-                        mma_16816(c, l1.x, h1.x, l1.y, h1.y, xb.z, xb.w);
-                    }
-                }
-            }
-            release(gi);
-        } else {
-#pragma unroll
-            for (int sub = 0; sub < kMmaSubMax; ++sub) {
-                if (sub < nsub) {
-                    const int i = i0 + sub;
-                    if (sub == 0 || acquire(i)) {
-                        const uint32_t sa = ring + (i % R::kStages) * R::kStageBytes + a_off;
+                        for (int p = 0; p < 2; ++p) {
+                            vl[2 * p + 1] = make_uint2(__shfl_xor_sync(0xFFFFFFFFu, vl[2 * p].x, 1),
+                                                       __shfl_xor_sync(0xFFFFFFFFu, vl[2 * p].y, 1));
+                            vh[2 * p + 1] = make_uint2(__shfl_xor_sync(0xFFFFFFFFu, vh[2 * p].x, 1),
+                                                       __shfl_xor_sync(0xFFFFFFFFu, vh[2 * p].y, 1));
+                        }
 #pragma unroll
                         for (int jj = 0; jj < kMmaJ; ++jj) {
-                            if (sub * kStageKb + warp * kMmaJ + jj < kblocks) {
-                                const uint32_t sj = sa + (uint32_t)((jj ^ (q & 1)) * 64);
-                                const uint4 lo = lds128(sj), hi = lds128(sj + 8 * kRowBytes);
-                                const uint4 xb = xr[sub][jj];
-                                mma_16816(c, lo.x, hi.x, lo.y, hi.y, xb.x, xb.y);
-                                mma_16816(c, lo.z, hi.z, lo.w, hi.w, xb.z, xb.w);
-                            }
+                            const uint32_t sh = ((jj & 1) ? q_sh1 : q_sh0) + ((jj & 2) ? 4u : 0u);    // 2j
+                            const uint2 l0 = q2k_pick4(vl[jj], (hl.q0 >> sh) & 0x03030303u);
+                            const uint2 l1 = q2k_pick4(vl[jj], (hl.q1 >> sh) & 0x03030303u);
+                            const uint2 h0 = q2k_pick4(vh[jj], (hh.q0 >> sh) & 0x03030303u);
+                            const uint2 h1 = q2k_pick4(vh[jj], (hh.q1 >> sh) & 0x03030303u);
+                            const uint4 xb = xr[sub][jj];
+                            mma_16816(c, l0.x, h0.x, l0.y, h0.y, xb.x, xb.y);
+                            mma_16816(c, l1.x, h1.x, l1.y, h1.y, xb.z, xb.w);
                         }
-                        release(i);
+                    }
+                }
+                release(gi);
+            } else {
+#pragma unroll
+                for (int sub = 0; sub < kMmaSubMax; ++sub) {
+                    if (sub < nsub) {
+                        const int i = i0 + sub;
+                        if (sub == 0 || acquire(i)) {
+                            const uint32_t sa = ring + (i % R::kStages) * R::kStageBytes + a_off;
+#pragma unroll
+                            for (int jj = 0; jj < kMmaJ; ++jj) {
+                                if (sub * kStageKb + warp * kMmaJ + jj < kblocks) {
+                                    const uint32_t sj = sa + (uint32_t)((jj ^ (q & 1)) * 64);
+                                    const uint4 lo = lds128(sj), hi = lds128(sj + 8 * kRowBytes);
+                                    const uint4 xb = xr[sub][jj];
+                                    mma_16816(c, lo.x, hi.x, lo.y, hi.y, xb.x, xb.y);
+                                    mma_16816(c, lo.z, hi.z, lo.w, hi.w, xb.z, xb.w);
+                                }
+                            }
+                            release(i);
+                        }
                     }
                 }
             }
+            if (!live) break;
         }
-        // Partials alternate between two buffers: the barrier of group i + 1
-        // also orders the reads of group i before the writes of group i + 2.
-        float *rb = red + (gi & 1) * (kMmaWarps * 32 * 4);
-        reinterpret_cast<float4 *>(rb)[warp * 32 + lane] = make_float4(c[0], c[1], c[2], c[3]);
-        mma_warps_sync();
-        if (threadIdx.x < 128 && live) {
-            // output (lane l, component j): c0 (row g, token 2q), c1 (row g, 2q+1), c2/c3 row g + 8
-            const int l = threadIdx.x >> 2, j = threadIdx.x & 3;
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < kMmaWarps; ++w) v += rb[(w * 32 + l) * 4 + j];
-            const int gg = l >> 2, qq = l & 3;
-            const int r = grp * 16 + gg + ((j & 2) ? 8 : 0), t = 2 * qq + (j & 1);
-            if (r < N && t < T) ly.kv[(size_t)t * N + r] = (uint16_t)f32_to_bf16_bits(v);
+        if (!triggered && *dep_ok) {
+            griddep_launch();
+            triggered = true;
         }
+        // Hand the partial tile (or the end marker) to the reducing warp through
+        // partial slot gi % kRedSlots, once the reducer has emptied its use gi - kRedSlots.
+        const int slot = gi % kRedSlots;
+        if (gi >= kRedSlots &&
+            !__all_sync(0xFFFFFFFFu, mbar_wait(red_empty(slot), ((gi / kRedSlots) & 1) ^ 1, abort_flag, a.err)))
+            break;
+        if (grp >= 0)
+            reinterpret_cast<float4 *>(red + slot * kRedSlotFloats)[warp * 32 + lane] = make_float4(c[0], c[1], c[2], c[3]);
+        if (warp == 0 && lane == 0) slot_grp[slot] = grp;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(red_full(slot));
+        if (grp < 0) break;
     }
+    if (!triggered && *dep_ok) griddep_launch();
 }
 
 template <bool HASH, bool WQ2K>
