@@ -175,22 +175,38 @@ __device__ __forceinline__ Q2kHalf q2k_half(const uint8_t *blk, int half, int q)
     h.q1 = w[5 + 8 * half + 2 * q];
     h.sc01 = w[2 * half];
     h.sc23 = w[2 * half + 1];
-    const uint32_t dw = w[20];
-    h.d = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFFu)));
-    h.dmin = __half2float(__ushort_as_half((unsigned short)(dw >> 16)));
+    const __half2 dd = *reinterpret_cast<const __half2 *>(w + 20);
+    h.d = __low2float(dd);
+    h.dmin = __high2float(dd);
     return h;
 }
-// The same table from the scale byte in place: sc & 15 and (sc & 0xF0) = 16 m
-// both become exact floats by one OR each (2^23 + n), and dmin * m is taken as
-// (dmin * 16 m) / 16 -- both products exact in f32 (11-bit dmin times at most
-// 8 bits), so the values are bit-identical to q2k_table's.
+// The same table from the scale byte in place, in the main loop: sc & 15 and
+// (sc & 0xF0) = 16 m both become exact floats by one OR each (2^23 + n), and
+// dmin * m is taken as (dmin * 16 m) * (-1/16) -- both products exact in f32
+// (11-bit dmin times at most 8 bits), v[0] as fma(dl, 0, nml) for the sign of
+// a zero -- so the values are bit-identical to q2k_table's.  Written as one
+// asm block: the decode is bound by the integer pipe, and this form issued
+// fewer of its instructions (45.4 against 46.3 us a step).
 __device__ __forceinline__ uint2 q2k_table_b(uint32_t sc, float d, float dmin) {
-    const float s_lo = __uint_as_float((sc & 0xFu) | 0x4B000000u) - 8388608.0f;
-    const float m16 = __uint_as_float((sc & 0xF0u) | 0x4B000000u) - 8388608.0f;
-    const float dl = __fmul_rn(d, s_lo);
-    const float nml = __fmul_rn(-__fmul_rn(dmin, m16), 0.0625f);
-    return make_uint2(pack_bf16x2(__fmaf_rn(dl, 0.0f, nml), __fmaf_rn(dl, 1.0f, nml)),
-                      pack_bf16x2(__fmaf_rn(dl, 2.0f, nml), __fmaf_rn(dl, 3.0f, nml)));
+    uint2 r;
+    asm("{\n\t.reg .b32 a, b;\n\t.reg .f32 lo, m16, dl, nml, y0, y1, y2, y3;\n\t"
+        "lop3.b32 a, %2, 0xF, 0x4B000000, 0xEA;\n\t"
+        "lop3.b32 b, %2, 0xF0, 0x4B000000, 0xEA;\n\t"
+        "mov.b32 lo, a;\n\t"
+        "mov.b32 m16, b;\n\t"
+        "sub.rn.f32 lo, lo, 0f4B000000;\n\t"
+        "sub.rn.f32 m16, m16, 0f4B000000;\n\t"
+        "mul.rn.f32 dl, %3, lo;\n\t"
+        "mul.rn.f32 nml, %4, m16;\n\t"
+        "mul.rn.f32 nml, nml, 0fBD800000;\n\t"
+        "fma.rn.f32 y0, dl, 0f00000000, nml;\n\t"
+        "fma.rn.f32 y1, dl, 0f3F800000, nml;\n\t"
+        "fma.rn.f32 y2, dl, 0f40000000, nml;\n\t"
+        "fma.rn.f32 y3, dl, 0f40400000, nml;\n\t"
+        "cvt.rn.bf16x2.f32 %0, y1, y0;\n\t"
+        "cvt.rn.bf16x2.f32 %1, y3, y2;\n\t}"
+        : "=r"(r.x), "=r"(r.y) : "r"(sc), "f"(d), "f"(dmin));
+    return r;
 }
 // v[0..3] as bf16 pairs (v0 v1, v2 v3) for the sub-block scale byte sc
 __device__ __forceinline__ uint2 q2k_table(uint32_t sc, float d, float dmin) {
@@ -199,11 +215,28 @@ __device__ __forceinline__ uint2 q2k_table(uint32_t sc, float d, float dmin) {
     return make_uint2(pack_bf16x2(__fmaf_rn(dl, 0.0f, nml), __fmaf_rn(dl, 1.0f, nml)),
                       pack_bf16x2(__fmaf_rn(dl, 2.0f, nml), __fmaf_rn(dl, 3.0f, nml)));
 }
-// four values v[t_0..3] as bf16 pairs, quants t one a byte.  With A = t * 0x22
-// (< 2^31), the 64-bit t * 0x00220022 is A + A * 2^16: its high word is A >> 16
-// (the low half's carry, (A & 0xFFFF) + (A >> 16) <= 0xCCCC, never reaches
-// bit 16) and its low 16 bits are those of A -- the selectors of values 2, 3
-// and of values 0, 1, each with 0x1010 added, from one multiply-add.
+// Four values v[t_0..3] as bf16 pairs from quant word w (one value a byte, its
+// quant at bits sh, sh + 1): t = (w >> sh) & 0x03030303, s = t * 0x22 +
+// 0x10101010 holds the byte-permute selectors (nibbles 2t, 2t + 1) of values 0,
+// 1 in its low half and of values 2, 3 in its high half.  Five integer-pipe
+// instructions and one multiply-add per four weights, as one asm block: the
+// same steps written in C++ issued about two more integer instructions per
+// word (ncu: 20.0 M against 16.1 M a step; 51.7 against 46.3 us).  A 64-bit
+// multiply-add giving both selectors at once measured slower (54.0 us), as did
+// the high selector by a multiply-high (50.6 us).
+__device__ __forceinline__ uint2 q2k_pick4_asm(uint2 v, uint32_t w, uint32_t sh) {
+    uint2 r;
+    asm("{\n\t.reg .b32 t, s, u;\n\t"
+        "shr.b32 t, %2, %5;\n\t"
+        "and.b32 t, t, 0x03030303;\n\t"
+        "mad.lo.u32 s, t, 0x22, 0x10101010;\n\t"
+        "shr.b32 u, s, 16;\n\t"
+        "prmt.b32 %0, %3, %4, s;\n\t"
+        "prmt.b32 %1, %3, %4, u;\n\t}"
+        : "=r"(r.x), "=r"(r.y) : "r"(w), "r"(v.x), "r"(v.y), "r"(sh));
+    return r;
+}
+// The same for quants already isolated in t (the one-time gather of x).
 __device__ __forceinline__ uint2 q2k_pick4(uint2 v, uint32_t t) {
     const uint32_t s = t * 0x22u + 0x10101010u;
     return make_uint2(__byte_perm(v.x, v.y, s), __byte_perm(v.x, v.y, s >> 16));
@@ -596,10 +629,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
 #pragma unroll
                         for (int jj = 0; jj < kMmaJ; ++jj) {
                             const uint32_t sh = ((jj & 1) ? q_sh1 : q_sh0) + ((jj & 2) ? 4u : 0u);    // 2j
-                            const uint2 l0 = q2k_pick4(vl[jj], (hl.q0 >> sh) & 0x03030303u);
-                            const uint2 l1 = q2k_pick4(vl[jj], (hl.q1 >> sh) & 0x03030303u);
-                            const uint2 h0 = q2k_pick4(vh[jj], (hh.q0 >> sh) & 0x03030303u);
-                            const uint2 h1 = q2k_pick4(vh[jj], (hh.q1 >> sh) & 0x03030303u);
+                            const uint2 l0 = q2k_pick4_asm(vl[jj], hl.q0, sh);
+                            const uint2 l1 = q2k_pick4_asm(vl[jj], hl.q1, sh);
+                            const uint2 h0 = q2k_pick4_asm(vh[jj], hh.q0, sh);
+                            const uint2 h1 = q2k_pick4_asm(vh[jj], hh.q1, sh);
                             const uint4 xb = xr[sub][jj];
                             mma_16816(c, l0.x, h0.x, l0.y, h0.y, xb.x, xb.y);
                             mma_16816(c, l1.x, h1.x, l1.y, h1.y, xb.z, xb.w);
