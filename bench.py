@@ -45,9 +45,17 @@ def _src_hash(*names) -> str:
     return h.hexdigest()[:12]
 
 
+# GB300 datasheet rates (dense bf16 tensor, HBM3e), for the fractions beside
+# the measured peaks.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 7900.0
+# Tensor pipe active share of the prefill GEMM in its ncu capture
+# (profiles/gemm_tc2_v41_prefill_T4096.md).
+TENSOR_PIPE_ACTIVE = 0.947
+
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by the
 # source hash of the kernel they were taken on; a changed kernel reports null.
-NCU_TRAFFIC = {("gemv", "8b5a623d588f"): 506475264}   # 503.43 MB read + 3.04 MB written
+NCU_TRAFFIC = {("gemv", "c45d77b3e596"): 506539264}   # 503.44 MB read + 3.10 MB written
 
 
 class Clocks:
@@ -144,21 +152,23 @@ def run_decode(args, rank, world):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     E.prepare_events([e for row in ev for e in row])
     pos = cfg.prefix
-    for i in range(args.warmup):
-        eng.forward(ids_all[i], pos, d_h)
-        pos += 1
-    assert E.engram_check() == 0
-    _barrier(world)
-    torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(torch.cuda.current_device()) as clk:
         time.sleep(0.3)                         # let the clock sampler start
+        # the W warm-up steps run right before the timed ones, so that the timed
+        # region does not start from an idle GPU
+        for i in range(args.warmup):
+            eng.forward(ids_all[i], pos, d_h)
+            pos += 1
+        _barrier(world)
+        torch.cuda.synchronize()
         t0.record()
         for i in range(args.steps):
             eng.forward(ids_all[args.warmup + i], pos, d_h)
             pos += 1
         t1.record()
         torch.cuda.synchronize()
+        assert E.engram_check() == 0
         ms = t0.elapsed_time(t1) / args.steps
         # Same steps again with an event between the stages of every step (the
         # events stop the projection -> gate launch overlap, so this pass gives
@@ -396,18 +406,63 @@ def rank_seed(rank: int) -> int:
 # CPU oracle (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_decode_rate(budget_s: float, wkv_host=None, steps=None, warm=0):
-    """Oracle decode steps (T = 1) on the host cores: for about budget_s
-    seconds, or -- with `steps` -- `warm` untimed steps and then exactly
-    `steps` timed ones.  Returns (tokens/s, threads, timed steps)."""
+def _oracle_mods():
     import oracle
     from deepseek_v4_engram_hash_gb300 import configs, synth
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle_glue as G
+    return oracle, configs, synth, G
 
+
+def host_inputs(cfg, eng=None):
+    """The oracle's stored inputs for fp8-table workloads: each layer's table
+    (codes, scales) and wkv as host arrays -- copied from a set-up workload's
+    device memory when given (the numpy twin generates the same bits), else
+    generated on the host by the seeded generator.  Input preparation, untimed."""
+    import torch
+    oracle, configs, synth, G = _oracle_mods()
+    tables, wkv = [], []
+    rows = synth.hash_tables(cfg)["rows_per_layer"]
+    for l in range(cfg.n_layers):
+        if eng is not None:
+            d = eng.layer_data[l]
+            tables.append((d["table"].cpu().numpy(), d["scales"].cpu().numpy()))
+            wkv.append(d["wkv"].view(torch.int16).cpu().numpy().view(np.uint16))
+        else:
+            tables.append(synth.table_fp8_rows(cfg, l, np.arange(rows[l])))
+            wkv.append(synth.wkv_rows(cfg, l, np.arange(cfg.N)))
+    return tables, wkv
+
+
+def oracle_forward(cfg, st, ids, pos, h, wkv, qk, tables=None):
+    """One oracle forward of ids [B, T] at position pos: the hash, every layer's
+    row gather (from the stored tables, or -- without them -- the touched rows
+    regenerated by the seeded generator and decoded by the oracle), the
+    projection and the gate, in the oracle's order.  Returns the new highway."""
+    oracle, configs, synth, G = _oracle_mods()
+    B, T = ids.shape
+    M = B * T
+    rid = st.forward(ids, pos).reshape(M, cfg.n_layers, cfg.cols)
+    for l in range(cfg.n_layers):
+        if tables is not None:
+            codes, scales = tables[l]
+            x = oracle.rows_fp8(codes, scales, cfg.head_dim, cfg.scale_block, rid[:, l, :].ravel())
+            x = x.reshape(M, cfg.K)
+        else:
+            x = G.x_of(cfg, l, rid)
+        kv = oracle.linear_bf16(x, wkv[l])
+        h = oracle.gate(h, kv, qk[l][0], qk[l][1], cfg.hc, cfg.dim, cfg.eps)
+    return h
+
+
+def oracle_decode_rate(budget_s: float, tables, wkv, steps=None, warm=0):
+    """Oracle decode steps (T = 1) of the single-token workload on the host
+    cores, each step whole (hash, row gather from the stored tables,
+    projection, gate of both layers): for about budget_s seconds, or -- with
+    `steps` -- `warm` untimed steps and then exactly `steps` timed ones.
+    Returns (tokens/s, threads, timed steps)."""
+    oracle, configs, synth, G = _oracle_mods()
     cfg = configs.V41_DECODE
-    if wkv_host is None:       # regenerate wkv on the host (input preparation, untimed)
-        wkv_host = [synth.wkv_rows(cfg, l, np.arange(cfg.N)) for l in range(cfg.n_layers)]
     qk = [synth.qk_weights(cfg, l) for l in range(cfg.n_layers)]
     total = 4096 if steps is None else warm + steps
     st = G.hash_state(cfg, 1, cfg.prefix + total + 16)
@@ -416,12 +471,8 @@ def oracle_decode_rate(budget_s: float, wkv_host=None, steps=None, warm=0):
     ids = synth.token_ids(cfg, "decode.0", total)
     pos, n, t_used = cfg.prefix, 0, 0.0
     while n < total and (steps is not None or t_used < budget_s):
-        rid = st.forward(ids[n:n + 1][None], pos)[0]          # hash [1, L, C]
-        rows = [G.rows(cfg, l, rid[:, l, :]) for l in range(cfg.n_layers)]   # includes table regen
         t = time.perf_counter()
-        for l in range(cfg.n_layers):
-            kv = oracle.linear_bf16(rows[l].reshape(1, cfg.K), wkv_host[l])
-            h = oracle.gate(h, kv, qk[l][0], qk[l][1], cfg.hc, cfg.dim, cfg.eps)
+        h = oracle_forward(cfg, st, ids[n:n + 1][None], pos, h, wkv, qk, tables)
         if n >= warm:
             t_used += time.perf_counter() - t
         pos += 1
@@ -430,42 +481,83 @@ def oracle_decode_rate(budget_s: float, wkv_host=None, steps=None, warm=0):
     return timed / t_used, oracle.num_threads(), timed
 
 
-def oracle_prefill_rate(n_tokens: int, wkv_host):
-    """Oracle prefill of the first n_tokens of the 4096-token workload on the
-    host cores: projection + gate of both layers timed (hash and row
-    regeneration untimed).  Returns (tokens/s, threads)."""
-    import oracle
-    from deepseek_v4_engram_hash_gb300 import configs, synth
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import oracle_glue as G
-
-    cfg = configs.V41_PREFILL
+def oracle_sample_rate(cfg, wkv, tables=None, prefill_tokens=0, decode_steps=0, batch=1):
+    """The oracle on a bounded sample of a workload: the first prefill_tokens
+    tokens of each sequence in one call, or (after hashing the workload's
+    prefill, untimed) decode_steps single-token steps of every sequence.
+    Returns (tokens/s over the timed calls, threads)."""
+    oracle, configs, synth, G = _oracle_mods()
     qk = [synth.qk_weights(cfg, l) for l in range(cfg.n_layers)]
-    st = G.hash_state(cfg, 1)
-    rid = st.forward(synth.token_ids(cfg, "prefill.0", cfg.T)[None, :n_tokens], 0)[0]   # [n, L, C]
-    xs = [G.x_of(cfg, l, rid) for l in range(cfg.n_layers)]
-    h = synth.highway(cfg, np.arange(n_tokens))
-    t = time.perf_counter()
-    for l in range(cfg.n_layers):
-        kv = oracle.linear_bf16(xs[l], wkv_host[l])
-        h = oracle.gate(h, kv, qk[l][0], qk[l][1], cfg.hc, cfg.dim, cfg.eps)
-    return n_tokens / (time.perf_counter() - t), oracle.num_threads()
+    st = G.hash_state(cfg, batch)
+    ids = np.stack([synth.token_ids(cfg, f"prefill.{b}", cfg.T) for b in range(batch)])
+    if prefill_tokens:
+        h = synth.highway(cfg, np.arange(batch * prefill_tokens))
+        t = time.perf_counter()
+        oracle_forward(cfg, st, ids[:, :prefill_tokens], 0, h, wkv, qk, tables)
+        return batch * prefill_tokens / (time.perf_counter() - t), oracle.num_threads()
+    st.forward(ids, 0)
+    dec = np.stack([synth.token_ids(cfg, f"decode.{b}", decode_steps) for b in range(batch)])
+    h = synth.highway(cfg, np.arange(batch))
+    t_used = 0.0
+    for k in range(decode_steps):
+        t = time.perf_counter()
+        h = oracle_forward(cfg, st, dec[:, k:k + 1], cfg.T + k, h, wkv, qk, tables)
+        t_used += time.perf_counter() - t
+    return batch * decode_steps / t_used, oracle.num_threads()
+
+
+def cpu_baselines(eng):
+    """The oracle as it stands on the host cores, on bounded samples (about
+    20 s of CPU work in all): the single-token step (all threads, then one),
+    a 256-token sample of the 4096-token prefill, a 64-token sample of the
+    Q2_K-table prefill and decode steps of the large-table workload."""
+    oracle, configs, synth, G = _oracle_mods()
+    cfg = configs.V41_DECODE
+    tables, wkv = host_inputs(cfg, eng)
+    rate, threads, n = oracle_decode_rate(8.0, tables, wkv)
+    oracle.set_num_threads(1)
+    rate1, _, n1 = oracle_decode_rate(4.0, tables, wkv)
+    oracle.set_num_threads(threads)
+    prate, _ = oracle_sample_rate(configs.V41_PREFILL, wkv, tables, prefill_tokens=256)
+    qrate, _ = oracle_sample_rate(configs.V41_Q2K, wkv, None, prefill_tokens=64)
+    srate, _ = oracle_sample_rate(configs.STRESS, wkv, None, decode_steps=3, batch=configs.STRESS.batch)
+    return {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} whole V4.1 decode steps (T=1) of the plain C oracle: hash, row gather from the "
+                      f"stored fp8 tables, projection and gate of both layers",
+            "single_thread": {"value": rate1, "unit": "tokens/s", "cores": 1, "steps": n1},
+            "prefill": {"value": prate, "unit": "tokens/s", "cores": threads,
+                        "sample": "the first 256 tokens of the 4096-token prefill in one whole call (hash, "
+                                  "row gather from the stored tables, projection, gate); every stage costs "
+                                  "the same per token, so this rate extrapolates linearly to the full prefill "
+                                  "(4096 tokens: about %.0f s)" % (4096 / prate)},
+            "v41_q2k_T512": {"value": qrate, "unit": "tokens/s", "cores": threads,
+                             "sample": "the first 64 tokens of the 512-token Q2_K-table prefill in one whole "
+                                       "call; the touched Q2_K rows regenerated by the seeded generator and "
+                                       "decoded by the oracle (no stored table); extrapolates linearly"},
+            "large_table_stress": {"value": srate, "unit": "tokens/s", "cores": threads,
+                                   "sample": "3 single-token decode steps of all 8 sequences after the "
+                                             "1536-token prefill (hashed untimed); touched rows regenerated "
+                                             "by the seeded generator"}}
 
 
 def reference_arm(args, rank, world):
     if rank != 0:
         return
-    # W untimed and K timed oracle decode steps, each one token of the
-    # single-token workload (about 21 ms a step on the 16 host cores)
-    rate, threads, n = oracle_decode_rate(0.0, steps=args.steps, warm=args.warmup)
+    # W untimed and K timed whole oracle decode steps of the single-token
+    # workload (about 21 ms a step on the 16 host cores); the stored tables
+    # and wkv are generated on the host first (input preparation, untimed)
+    oracle, configs, synth, G = _oracle_mods()
+    tables, wkv = host_inputs(configs.V41_DECODE)
+    rate, threads, n = oracle_decode_rate(0.0, tables, wkv, steps=args.steps, warm=args.warmup)
     line = {"metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 / rate, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "impl": "reference",
             "config": {"workload": "v41_decode_T1", "tokens_per_step": 1},
             "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{n} timed decode steps (after {args.warmup} untimed) of the plain C "
-                                       f"oracle (projection + gate of both layers; hash and row gather untimed)"},
+                             "sample": f"{n} timed whole decode steps (after {args.warmup} untimed) of the plain "
+                                       f"C oracle: hash, row gather from the stored fp8 tables, projection and "
+                                       f"gate of both layers"},
             "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -545,6 +637,11 @@ def main():
                             "peak": bf16_burst, "unit": "TFLOP/s",
                             "frac": gemm_flops(pc, pc.T) / (gemm_ms * 1e-3) / 1e12 / bf16_burst,
                             "peak_source": f"{peak_src} bf16 burst (GEMM timed in short back-to-back steps)",
+                            "peak_nominal": NOMINAL_BF16_TFLOPS,
+                            "frac_of_nominal": gemm_flops(pc, pc.T) / (gemm_ms * 1e-3) / 1e12 / NOMINAL_BF16_TFLOPS,
+                            "tensor_pipe_active": TENSOR_PIPE_ACTIVE,
+                            "note": "the measured peak is cuBLAS bf16 at 8192^3, so a kernel can read a little "
+                                    "above 1.0 of it; frac_of_nominal is against the dense bf16 datasheet rate",
                             "kernel": "gemm_tc2_kernel (tcgen05 on CTA pairs, both layers in one launch)"}}
 
     others = None
@@ -581,21 +678,7 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and args.only is None:
-        wkv_host = [d["eng"].layer_data[l]["wkv"].view(torch.int16).cpu().numpy().view(np.uint16)
-                    for l in range(cfg.n_layers)]
-        rate, threads, n = oracle_decode_rate(12.0, wkv_host)
-        import oracle
-        oracle.set_num_threads(1)
-        rate1, _, n1 = oracle_decode_rate(6.0, wkv_host)
-        oracle.set_num_threads(threads)
-        prate, pthreads = oracle_prefill_rate(64, wkv_host)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n} V4.1 decode steps (T=1) of the plain C oracle, projection + gate of both "
-                         f"layers timed; hash and row regeneration untimed",
-               "single_thread": {"value": rate1, "unit": "tokens/s", "cores": 1, "steps": n1},
-               "prefill": {"value": prate, "unit": "tokens/s", "cores": pthreads,
-                           "sample": "the first 64 tokens of the 4096-token prefill in one call, "
-                                     "projection + gate of both layers timed"}}
+        cpu = cpu_baselines(d["eng"])
 
     if rank == 0:
         line = {
@@ -609,7 +692,8 @@ def main():
             "roofline": {"bound": "hbm", "achieved": gemv_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": gemv_gbs / hbm, "traffic": traffic,
                          "kernel": "gemv_mma_kernel<1, 0> (fused hash, row gather and wkv GEMV, both layers)",
-                         "algorithmic_bytes": gemv_bytes(cfg, M), "peak_source": f"{peak_src} hbm_gbs"},
+                         "algorithmic_bytes": gemv_bytes(cfg, M), "peak_source": f"{peak_src} hbm_gbs",
+                         "peak_nominal": NOMINAL_HBM_GBS, "frac_of_nominal": gemv_gbs / NOMINAL_HBM_GBS},
             "step_roofline": {"achieved": step_gbs, "frac": step_gbs / hbm, "algorithmic_bytes": step_bytes(cfg, M)},
             "stage_ms": dict(zip(["hash", "gather", "gemv", "gate"], d["stage_ms"])),
             "stage_note": "per-kernel times from a second pass with events between the stages; "

@@ -165,6 +165,20 @@ def token_ids(cfg, tag: str, n: int) -> np.ndarray:
 # Tables, weights, highway (numpy twins; any subset of rows)
 # ---------------------------------------------------------------------------
 
+def _chunked(n: int, step: int, fn) -> None:
+    """fn(a, b) over [0, n) in chunks of `step`, on a few threads when there
+    are several chunks (numpy and torch release the GIL on large arrays; each
+    chunk writes its own slice, so the result does not depend on the order)."""
+    starts = list(range(0, n, step))
+    if len(starts) <= 1:
+        for a in starts:
+            fn(a, min(n, a + step))
+        return
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=min(len(starts), os.cpu_count() or 1, 16)) as ex:
+        list(ex.map(lambda a: fn(a, min(n, a + step)), starts))
+
+
 def table_fp8_rows(cfg, layer: int, rows):
     """Rows of layer `layer`'s fp8 table: codes [n, hd] u8 and scales [n, hd/blk] f32.
 
@@ -172,13 +186,21 @@ def table_fp8_rows(cfg, layer: int, rows):
     k uniform in {-4..2}, per scale_block values."""
     rows = np.atleast_1d(np.asarray(rows, dtype=np.uint64)).ravel()
     hd, nb = cfg.head_dim, cfg.head_dim // cfg.scale_block
-    idx = rows[:, None] * np.uint64(hd) + np.arange(hd, dtype=np.uint64)[None, :]
-    x = normal_f32(stream_key(cfg.seed, f"table.{layer}"), idx, 1.0)
-    codes = to_e4m3_codes(np.clip(x, -448.0, 448.0))
-    sidx = rows[:, None] * np.uint64(nb) + np.arange(nb, dtype=np.uint64)[None, :]
-    k = (splitmix64(stream_key(cfg.seed, f"scales.{layer}"), sidx) % np.uint64(7)).astype(np.int64) - 4
-    scales = ((k + 127) << 23).astype(np.uint32).view(np.float32)
-    return codes.reshape(rows.size, hd), scales.reshape(rows.size, nb)
+    codes = np.empty((rows.size, hd), dtype=np.uint8)
+    scales = np.empty((rows.size, nb), dtype=np.float32)
+    kt, ks = stream_key(cfg.seed, f"table.{layer}"), stream_key(cfg.seed, f"scales.{layer}")
+
+    def fill(a, b):
+        r = rows[a:b]
+        idx = r[:, None] * np.uint64(hd) + np.arange(hd, dtype=np.uint64)[None, :]
+        x = normal_f32(kt, idx, 1.0)
+        codes[a:b] = to_e4m3_codes(np.clip(x, -448.0, 448.0)).reshape(r.size, hd)
+        sidx = r[:, None] * np.uint64(nb) + np.arange(nb, dtype=np.uint64)[None, :]
+        k = (splitmix64(ks, sidx) % np.uint64(7)).astype(np.int64) - 4
+        scales[a:b] = ((k + 127) << 23).astype(np.uint32).view(np.float32).reshape(r.size, nb)
+
+    _chunked(rows.size, max(1, (1 << 20) // hd), fill)
+    return codes, scales
 
 
 Q2K_D_LO = np.float32(1e-3)
@@ -200,20 +222,6 @@ def table_q2k_rows(cfg, layer: int, rows, tag: str = "q2k") -> np.ndarray:
     d = (u * Q2K_D_STEP + Q2K_D_LO).astype(np.float16)
     out[:, 80:84] = np.ascontiguousarray(d).astype("<f2").view(np.uint8).reshape(rows.size, 4)
     return out
-
-
-def _chunked(n: int, step: int, fn) -> None:
-    """fn(a, b) over [0, n) in chunks of `step`, on a few threads when there
-    are several chunks (numpy and torch release the GIL on large arrays; each
-    chunk writes its own slice, so the result does not depend on the order)."""
-    starts = list(range(0, n, step))
-    if len(starts) <= 1:
-        for a in starts:
-            fn(a, min(n, a + step))
-        return
-    from concurrent.futures import ThreadPoolExecutor
-    with ThreadPoolExecutor(max_workers=min(len(starts), os.cpu_count() or 1, 16)) as ex:
-        list(ex.map(lambda a: fn(a, min(n, a + step)), starts))
 
 
 def wkv_rows(cfg, layer: int, rows, sigma: float = 0.02) -> np.ndarray:

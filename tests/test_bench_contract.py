@@ -32,7 +32,7 @@ def test_reference_arm_line():
     assert d["config"]["workload"] == "v41_decode_T1"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
-    assert cb["sample"].startswith("2 timed decode steps")
+    assert cb["sample"].startswith("2 timed whole decode steps")
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
 
