@@ -3,7 +3,7 @@
 Shapes follow DeepSeek-V4.1-Flash as the pages give them: engram before model
 layers 1 and 14, four-gram windows over eight heads (24 hash columns, 48 ids a
 token over two layers), 256-wide rows, dim 4096 and four hyper-connection
-streams (spark_model/layers/engram_v41.rs, module doc and `EngramV41`).
+streams (page "spark_model/layers/engram_v41.rs", module doc).
 Nothing here computes any part of the method.
 """
 from __future__ import annotations

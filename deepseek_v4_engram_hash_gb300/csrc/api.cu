@@ -1,6 +1,7 @@
 // api.cu -- the libengram C ABI: handles, host-side validation (before any
-// copy or launch, as spark_model/layers/engram_v41.rs checks `ensure!`s before
-// it uploads or launches), and the launch sequence of the forward.
+// copy or launch, as the GPU module page "spark_model/layers/engram_v41.rs"
+// checks its shapes before it uploads or launches), and the launch sequence of
+// the forward.
 #include "common.cuh"
 
 #include <cmath>

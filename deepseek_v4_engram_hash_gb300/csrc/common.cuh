@@ -158,13 +158,14 @@ __device__ __forceinline__ uint64_t rem_euclid_barrett(uint64_t u, uint64_t p, u
 }
 
 // Row id of (sequence b, position start_pos + s, layer li, column col):
-// `EngramHasher::hash` (spark_model/layers/engram_v41.rs) and
-// `NgramHashState::forward` (metrale_model_arch/deepseek_v41_ref/engram.rs).
-// The window holds the compressed ids at shifts 0..n (n = col / H + 1);
-// once a shift reaches before position 0 or an unmapped (-1) id, it and every
-// larger shift take pad_id.  rolling = tok0 * m0, then rolling ^= tok_k * m_k,
-// and the id is rem_euclid(rolling, prime) + offset, all i64 with wrap (the
-// remainder by Barrett reduction, rem_euclid_barrett).  Ids
+// the hash of page "metrale_model_arch/deepseek_v41_ref/engram.rs" (module doc,
+// item 1) and page "spark_model/layers/engram_v41.rs" (module doc, item 1):
+//   w_j = cache[p - j] while no shift up to j reaches before position 0 or an
+//         unmapped (-1) id, else pad_id;
+//   X_n = XOR_{j=0..n} (w_j *wrap m_j)  for the (n+1)-gram, n = col / H + 1;
+//   id  = rem_euclid(X_n, prime[col]) + offset[col],
+// all i64 with wrap; X_n is formed slot by slot as the window is read, and
+// the remainder is taken by Barrett reduction (rem_euclid_barrett).  Ids
 // of this call come from the input through token_map, older positions from
 // the cache, so no thread depends on another thread's cache write.
 __device__ __forceinline__ int64_t hash_one(const HashArgs &a, int64_t sp, int b, int s, int li, int col) {

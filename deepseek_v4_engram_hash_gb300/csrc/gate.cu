@@ -1,8 +1,9 @@
 // gate.cu -- the engram gate (stage 4) for one or more layers on one highway.
 //
-// `gate_and_add` (metrale_model_arch/deepseek_v41_ref/engram.rs) on the FP32
-// highway of spark_model/layers/engram_v41.rs (module doc, item 4), per token
-// t and stream c, with key = kv[t, c D : (c+1) D], value = kv[t, hc D : (hc+1) D]:
+// The gate of the CPU reference page "metrale_model_arch/deepseek_v41_ref/engram.rs"
+// (module doc, item 4) on the FP32 highway of the GPU module page
+// "spark_model/layers/engram_v41.rs" (module doc, item 4), per token t and
+// stream c, with key = kv[t, c D : (c+1) D], value = kv[t, hc D : (hc+1) D]:
 //   hh = sum h^2, kk = sum key^2, dot = sum (h (q k)) key
 //   s  = dot * (1/sqrt(hh/D + eps) * 1/sqrt(kk/D + eps)) * D^-1/2
 //   g  = copysign(sqrt(max(|s|, 1e-6)), s)

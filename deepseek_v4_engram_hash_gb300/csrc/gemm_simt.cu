@@ -1,6 +1,6 @@
 // gemm_simt.cu -- plain shared-memory-tiled CUDA-core GEMM for the wkv
 // projection, kv [M, N] = bf16_rne(x [M, K] . wkv [N, K]^T), f32 accumulation
-// (`linear_bf16`, metrale_model_arch/deepseek_v41_ref/engram.rs).
+// (page "metrale_model_arch/deepseek_v41_ref/engram.rs", module doc, item 3).
 //
 // 128 x 128 output tile per CTA, K in steps of 32, 256 threads with an 8 x 8
 // register tile each.  This is the simple correct path for shapes the

@@ -3,7 +3,7 @@
 // gemm_tc2.cu takes over, bit-identically).
 //
 // kv [M, N] = bf16_rne(x [M, K] . wkv [N, K]^T) with f32 accumulation
-// (`linear_bf16`, metrale_model_arch/deepseek_v41_ref/engram.rs), the dense
+// (page "metrale_model_arch/deepseek_v41_ref/engram.rs", module doc, item 3), the dense
 // contraction of the engram forward (2 x 4096 x 6144 x 20480 flop a layer at
 // the V4.1 prefill shape).
 //

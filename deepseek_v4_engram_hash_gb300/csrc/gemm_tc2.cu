@@ -1,7 +1,7 @@
 // gemm_tc2.cu -- the prefill wkv projection on CTA pairs (tcgen05 cta_group::2).
 //
 // kv [M, N] = bf16_rne(x [M, K] . wkv [N, K]^T) with f32 accumulation
-// (`linear_bf16`, metrale_model_arch/deepseek_v41_ref/engram.rs), as in
+// (page "metrale_model_arch/deepseek_v41_ref/engram.rs", module doc, item 3), as in
 // gemm_tc.cu, but a cluster of two CTAs computes one 256 x 256 tile: CTA r of
 // the pair holds x rows m0 + 128 r .. +127 and wkv rows n0 + 128 r .. +127 of
 // every 64-wide k step in its own shared memory, and one thread of CTA 0

@@ -2,10 +2,11 @@
 // the row gather and dequantisation (stage 2) fused into the x staging.
 //
 // kv[t, o] = bf16_rne(sum_i x[t, i] * wkv[o, i]), f32 accumulation
-// (`linear_bf16`, metrale_model_arch/deepseek_v41_ref/engram.rs).  At a few
+// (page "metrale_model_arch/deepseek_v41_ref/engram.rs", module doc, item 3).  At a few
 // tokens the projection is a pass over wkv (251.7 MB a layer at V4.1 shape),
 // so this kernel is shaped for HBM bandwidth, as the pages choose a GEMV over
-// a tiled GEMM at m = 1 (spark_model/layers/attn_v41.rs, `Kernels.gemv`).
+// a tiled GEMM at m = 1 (page "spark_model/layers/attn_v41.rs", the doc of its
+// kernel table: a bandwidth-bound GEMV in place of the tiled GEMM at one token).
 //
 // Grid: the layers' CTAs side by side, one an SM; the CTAs of a layer share
 // its 16-row groups of wkv (handed out by a counter).  Prologue: the CTA
@@ -15,7 +16,8 @@
 // copy warp streams the groups' wkv rows into a shared-memory ring with bulk
 // copies; 16 MMA warps multiply them by x on mma.sync m16n8k16 (bf16 in, f32
 // accumulate).  wkv may also be held as Q2_K
-// blocks (`wkv_q2k` on spark_model/layers/engram_v41.rs, 6x fewer bytes): the
+// blocks (page "spark_model/layers/engram_v41.rs", the doc of the layer weights:
+// Q2_K wkv, 6x fewer bytes a token, byte-identical results): the
 // same kernel then copies the blocks and decodes each lane's weights into its
 // mma fragments, in the same order, so kv is bit-identical to the bf16 path on
 // the dequantised weights.

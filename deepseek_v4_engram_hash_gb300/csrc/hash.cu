@@ -1,8 +1,7 @@
 // hash.cu -- the n-gram hash (stage 1).
 //
-// `EngramHasher::hash` (spark_model/layers/engram_v41.rs) and
-// `NgramHashState::forward` (metrale_model_arch/deepseek_v41_ref/engram.rs),
-// batched: for position p = start_pos + s of sequence b, the window holds the
+// Page "metrale_model_arch/deepseek_v41_ref/engram.rs", module doc, item 1 (and
+// page "spark_model/layers/engram_v41.rs", module doc, item 1), batched: for position p = start_pos + s of sequence b, the window holds the
 // compressed ids at shifts 0..ng-1; once a shift reaches before position 0 or
 // an unmapped (-1) id, that shift and every larger one take pad_id.  Per layer,
 // rolling = tok0 * m0, then rolling ^= tok_n * m_n for n = 1..ng-1, and column

@@ -2,9 +2,9 @@
 // row kernels (engram_rows_*), and the prefill kernels that hash (stage 1)
 // and gather every layer's rows in one launch.
 //
-// fp8: `regen_table` + `embed_rows` on metrale_model_arch/deepseek_v41_ref/engram.rs:
+// fp8: page "metrale_model_arch/deepseek_v41_ref/engram.rs", module doc, item 2:
 //   row(id)[d] = bf16_rne(e4m3(table[id, d]) * scales[id, d / blk]).
-// Q2_K: `rows_from_q2k` on spark_model/layers/engram_v41.rs, one 84-byte
+// Q2_K: page "spark_model/layers/engram_v41.rs", module doc, item 2: one 84-byte
 //   ggml super-block per 256-wide row.
 //
 // Layout: hd/16 consecutive threads own one row; each moves 16 fp8 codes

@@ -28,7 +28,7 @@
  *     or in page-locked host memory that the device reads in place (mapped
  *     at the same address, e.g. cudaHostAlloc): rows are then read by id over
  *     the CPU-GPU link, so a table need not fit in HBM (the page-locked,
- *     device-visible arena of spark_model/layers/deepseek_v41_layer.rs).  Any
+ *     device-visible arena of page "spark_model/layers/deepseek_v41_layer.rs").  Any
  *     other table pointer is refused with ENGRAM_E_INVALID.
  *   - T = 0 is a valid no-op for every call that takes a token count; its
  *     buffers may then be null.
@@ -79,7 +79,8 @@ typedef struct {
 typedef struct engram_tables engram_tables;   /* device copies of the hash tables */
 typedef struct engram_hasher engram_hasher;   /* per-batch look-back cache */
 
-/* Hash tables: spark_model/layers/engram_v41.rs, `EngramHashTables::from_flat`.
+/* Hash tables: page "spark_model/layers/engram_v41.rs", module doc, item 1 (the
+ * tables the hash reads; the ABI counterpart of `EngramHashTables::from_flat`).
  * Host arrays, copied to the current device:
  *   h_token_map   [vocab]                    compressed id per token, -1 = unmapped
  *   pad_token_id  pad_id = h_token_map[pad_token_id]
@@ -107,7 +108,8 @@ int engram_hasher_create(const engram_tables *t, int32_t batch, int64_t max_seq,
 int engram_hasher_reset(engram_hasher *hs, uintptr_t stream);
 void engram_hasher_destroy(engram_hasher *hs);
 
-/* Stage 1, `EngramHasher::hash` / `NgramHashState::forward`:
+/* Stage 1, the hash: page "metrale_model_arch/deepseek_v41_ref/engram.rs", module
+ * doc, item 1 (`EngramHasher::hash` / `NgramHashState::forward`):
  *   d_ids     [batch, T] int32 token ids at positions start_pos .. start_pos+T-1
  *   d_row_ids [batch, T, n_layers, C] int64 out
  * Writes the new positions into the cache.  The i64 arithmetic (wrapping
@@ -116,7 +118,8 @@ void engram_hasher_destroy(engram_hasher *hs);
 int engram_hash(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t start_pos,
                 int64_t *d_row_ids, uintptr_t stream);
 
-/* Stage 2, fp8 rows (engram.rs CPU reference, `regen_table` + `embed_rows`):
+/* Stage 2, fp8 rows (page "metrale_model_arch/deepseek_v41_ref/engram.rs", module
+ * doc, item 2):
  *   row(id)[d] = bf16_rne(e4m3(d_table[id, d]) * d_scales[id, d / scale_block])
  * for id = d_row_ids[t * id_stride + c], written to d_rows[(t * C + c), :].
  *   d_table [R, head_dim] u8 (16-byte aligned), d_scales [R, head_dim/scale_block] f32,
@@ -133,13 +136,14 @@ int engram_rows_fp8_e8m0(const uint8_t *d_table, const uint8_t *d_scales, int64_
                          int32_t scale_block, const int64_t *d_row_ids, int64_t n_tok, int64_t id_stride,
                          int32_t C, uint16_t *d_rows, uintptr_t stream);
 
-/* Stage 2, Q2_K rows (spark_model/layers/engram_v41.rs, `rows_from_q2k`;
+/* Stage 2, Q2_K rows (page "spark_model/layers/engram_v41.rs", module doc, item 2;
  * head_dim 256): d_blocks [R, 84] u8 (4-byte aligned), ggml Q2_K layout,
  * decoded y = d * (sc & 15) * q - dmin * (sc >> 4), then bf16 RNE.  Bit-exact. */
 int engram_rows_q2k(const uint8_t *d_blocks, int64_t R, const int64_t *d_row_ids, int64_t n_tok,
                     int64_t id_stride, int32_t C, uint16_t *d_rows, uintptr_t stream);
 
-/* Stage 3 (engram.rs CPU reference, `linear_bf16`): d_kv[t, o] =
+/* Stage 3 (page "metrale_model_arch/deepseek_v41_ref/engram.rs", module doc,
+ * item 3): d_kv[t, o] =
  * bf16_rne(sum_i d_x[t, i] * d_wkv[o, i]) with f32 accumulation.
  *   d_x [T, K] bf16, d_wkv [N, K] bf16, d_kv [T, N] bf16; all 16-byte aligned.
  * K % 64 == 0, N % 16 == 0.  T <= 8 with K <= 6144 runs the bandwidth-bound
@@ -148,15 +152,18 @@ int engram_rows_q2k(const uint8_t *d_blocks, int64_t R, const int64_t *d_row_ids
 int engram_project(const uint16_t *d_x, const uint16_t *d_wkv, int32_t T, int32_t K, int32_t N,
                    uint16_t *d_kv, uintptr_t stream);
 
-/* Stage 4 (engram.rs CPU reference, `gate_and_add`, on the FP32 highway):
+/* Stage 4 (page "metrale_model_arch/deepseek_v41_ref/engram.rs", module doc,
+ * item 4, on the FP32 highway of page "spark_model/layers/engram_v41.rs",
+ * module doc, item 4):
  *   d_h [T, hc, dim] f32 in/out (16-byte aligned); d_kv [T, (hc+1) dim] bf16;
  *   d_qk [hc, dim] f32 = q_weight * k_weight (exact for bf16 weights,
  *   `EngramV41::upload_qk`). */
 int engram_gate(float *d_h, const uint16_t *d_kv, const float *d_qk, int32_t T, int32_t hc,
                 int32_t dim, float eps, uintptr_t stream);
 
-/* Stage 3 at one token from Q2_K-quantised wkv (spark_model/layers/engram_v41.rs,
- * `EngramLayerWeights.wkv_q2k`: the weight as the GGUF ships it, read by the
+/* Stage 3 at one token from Q2_K-quantised wkv (page
+ * "spark_model/layers/engram_v41.rs", the doc of the layer weights: the weight
+ * as the GGUF ships it, read by the
  * single-token projection in place of the bf16 expansion, 6x fewer bytes):
  *   d_wkv_q2k [N, K / 256] 84-byte ggml Q2_K blocks (a row's blocks contiguous,
  *   16-byte aligned); d_x [1, K] bf16; d_kv [1, N] bf16.  K % 256 == 0 and
@@ -228,7 +235,7 @@ int engram_forward_dpos(engram_hasher *hs, const engram_layer *layers, const int
                         uintptr_t stream);
 
 /* The decode step as one CUDA graph (the single-token step capture of
- * spark_model/layers/deepseek_v41_layer.rs, `GraphMode`): captures
+ * page "spark_model/layers/deepseek_v41_layer.rs", the doc of its graph mode): captures
  * engram_forward_dpos with these arguments -- every pointer is baked into the
  * graph -- and replays it with engram_graph_launch.  Between replays the
  * caller updates the contents of d_ids (and of d_h if it wishes); the

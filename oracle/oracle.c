@@ -89,7 +89,8 @@ float orc_f16_to_f32(uint16_t h) {
     return sign ? -v : v;
 }
 
-/* e4m3fn decode: engram.rs (CPU reference), `e4m3_to_f32`.
+/* e4m3fn decode (page "metrale_model_arch/deepseek_v41_ref/engram.rs", module
+ * doc, item 2, and the doc of its e4m3 decoder).
  * exponent 15 with mantissa 7 is NaN; exponent 0 is subnormal m/8 * 2^-6;
  * otherwise (1 + m/8) * 2^(e-7); the sign is kept, so 0x80 is -0.0. */
 float orc_e4m3_to_f32(uint8_t b) {
@@ -101,8 +102,8 @@ float orc_e4m3_to_f32(uint8_t b) {
     return sign * (1.0f + m / 8.0f) * ldexpf(1.0f, e - 7);
 }
 
-/* f32 -> e4m3fn, round to nearest even: engram.rs (CPU reference),
- * `f32_to_e4m3_rne`.  NaN -> 0x7F; |x| > 448 saturates to 0x7E; an f32 with
+/* f32 -> e4m3fn, round to nearest even (the same page, the doc of its e4m3
+ * encoder).  NaN -> 0x7F; |x| > 448 saturates to 0x7E; an f32 with
  * exponent field 0 (zero or f32 subnormal) -> signed zero; e4m3 subnormals
  * are RNE(|x| * 512); a mantissa that rounds up to 8 carries into the
  * exponent. */
@@ -121,8 +122,8 @@ uint8_t orc_f32_to_e4m3(float x) {
     return sign | (uint8_t)(((e + 7) << 3) | mant);
 }
 
-/* f32 -> e8m0 as a power of two: engram.rs (CPU reference),
- * `f32_to_e8m0_rne`.  The nearest exponent; a mantissa of exactly one half
+/* f32 -> e8m0 as a power of two (the same page, the doc of its e8m0 scale
+ * encoder).  The nearest exponent; a mantissa of exactly one half
  * (x = 1.5 * 2^e) rounds up only when the biased exponent field is odd, so
  * the stored 8-bit code of a tie is even.  The sign is dropped. */
 float orc_f32_to_e8m0(float x) {
@@ -241,7 +242,7 @@ int orc_hash(const int64_t *token_map, int64_t vocab, int64_t pad_id,
 /* Stage 2: table rows                                                  */
 /* ------------------------------------------------------------------ */
 
-/* engram.rs (CPU reference), `regen_table` + `embed_rows`, for a table that
+/* Page "metrale_model_arch/deepseek_v41_ref/engram.rs", module doc, item 2, for a table that
  * is already stored as e4m3 codes:
  *   row(id)[d] = bf16_rne( e4m3_to_f32(table[id][d]) * scales[id][d / blk] )
  * table [R, hd] u8, scales [R, hd / blk] f32, out [n, hd] bf16 bits. */
@@ -283,8 +284,8 @@ int orc_rows_fp8_e8m0(const uint8_t *table, const uint8_t *scales, int64_t R, in
     return ORC_OK;
 }
 
-/* One 84-byte Q2_K block per 256-wide row (spark_model/layers/engram_v41.rs,
- * `ENGRAM_ROW_BYTES` and `rows_from_q2k`), in the ggml super-block layout:
+/* One 84-byte Q2_K block per 256-wide row (page "spark_model/layers/engram_v41.rs",
+ * module doc, item 2), in the ggml super-block layout:
  *   bytes  0..15  scales[16]: low nibble = sub-block scale, high = sub-block min
  *   bytes 16..79  qs[64]: 2-bit quants, four per byte
  *   bytes 80..81  d    (binary16, little-endian)
@@ -319,7 +320,7 @@ int orc_rows_q2k(const uint8_t *blocks, int64_t R, const int64_t *ids, int64_t n
 /* Stage 3: the wkv projection                                          */
 /* ------------------------------------------------------------------ */
 
-/* engram.rs (CPU reference), `linear_bf16`:
+/* Page "metrale_model_arch/deepseek_v41_ref/engram.rs", module doc, item 3:
  *   y[r][o] = bf16_rne( sum_{i = 0 .. in-1} x[r][i] * w[o][i] ),
  * accumulated in f32 in index order.  x [rows, in] and w [out, in] are bf16
  * bits; y [rows, out] bf16 bits; acc (optional) receives the f32 sums before
@@ -344,7 +345,8 @@ void orc_linear_bf16(const uint16_t *x, int64_t rows, int64_t in_f, const uint16
 /* Stage 4: the gate                                                    */
 /* ------------------------------------------------------------------ */
 
-/* engram.rs (CPU reference), `gate_and_add`, on the FP32 highway:
+/* Page "metrale_model_arch/deepseek_v41_ref/engram.rs", module doc, item 4, on
+ * the FP32 highway:
  *   h  [T, hc, D] f32, updated in place
  *   kv [T, (hc + 1) * D] bf16 bits: key c = columns [c D, (c+1) D),
  *                                   value  = columns [hc D, (hc+1) D)
