@@ -574,7 +574,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-others", action="store_true", help="skip the Q2_K and large-table lines")
-    ap.add_argument("--only", choices=["decode", "prefill", "wkvq2k", "wkvq2k8", "decode8", "q2k512"], default=None,
+    ap.add_argument("--only", choices=["decode", "prefill", "wkvq2k", "wkvq2k8", "decode8", "q2k512", "stress"],
+                    default=None,
                     help="run one workload only (for profiling); prints its own JSON line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -603,10 +604,11 @@ def main():
         r = run_decode_only(configs.V41_DECODE_WKVQ2K, args.steps, batch=8 if args.only == "wkvq2k8" else 1)
         print(json.dumps(r), flush=True)
         return
-    if args.only == "q2k512":
+    if args.only in ("q2k512", "stress"):
         from deepseek_v4_engram_hash_gb300 import configs
-        r = run_other(configs.V41_Q2K, args.prefill_steps, 0)
-        r["workload"] = configs.V41_Q2K.name
+        c = configs.V41_Q2K if args.only == "q2k512" else configs.STRESS
+        r = run_other(c, args.prefill_steps, 0)
+        r["workload"] = c.name
         print(json.dumps(r), flush=True)
         return
     if args.only == "prefill":

@@ -468,6 +468,8 @@ int engram_workspace_layout(const engram_geom *geom, int64_t tokens, size_t *off
         off[1 + g.n_layers + l] = p;
         if (need_x) p += up256((size_t)tokens * K * 2);
     }
+    // from 256 tokens (the CTA-pair GEMM): partial tiles of its last wave, at the end
+    if (tokens >= 256) p += up256(kTailPartBytes);
     off[1 + 2 * g.n_layers] = p;   // total (caller's array is sized 2 + 2 L by engram_workspace_bytes)
     return ENGRAM_OK;
 }
@@ -625,7 +627,9 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
             // every layer's tiles in one persistent tensor-core launch
             // after the fused gather, launched early (see gemm_tc2.cu): 4096 tokens 1.221 ->
             // 1.215 ms a step, 512 tokens with Q2_K tables 0.1992 -> 0.1967 ms
-            e = launch_gemm_tc(L, xs, ws_, kvs, (int)M, N, K, err, s, hash_in_rows);
+            GemmTail tail{M >= 256 ? reinterpret_cast<float *>(ws + off[1 + 2 * L] - up256(kTailPartBytes))
+                                   : nullptr};
+            e = launch_gemm_tc(L, xs, ws_, kvs, (int)M, N, K, err, s, hash_in_rows, M >= 256 ? &tail : nullptr);
 
             if (e != cudaSuccess) return ENGRAM_E_CUDA;
         } else {

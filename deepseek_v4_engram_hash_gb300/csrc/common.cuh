@@ -327,14 +327,24 @@ cudaError_t launch_tile_wkv(const uint16_t *wkv, int N, int K, uint16_t *tiled, 
 cudaError_t launch_gemm(const uint16_t *x, const uint16_t *wkv, uint16_t *kv, int M, int N, int K,
                         int *err, cudaStream_t s);
 bool gemm_tc_supported(int M, int N, int K);
+// Scratch that lets the CTA-pair GEMM cut the tiles of its partial last wave
+// along K (engram_forward supplies it): f32 partial tiles, added up by a
+// fix-up launch right after the GEMM.
+constexpr int kTailItems = 96;                          // >= the CTA pairs of the GPU
+constexpr size_t kTailPartBytes = (size_t)kTailItems * 256 * 256 * 4;
+struct GemmTail {
+    float *part;                                        // [kTailItems][256][256]
+};
 // pdl: launched as a programmatic dependent of the kernel before it (which
 // writes x); the GEMM waits for it after its set-up (TMEM, barriers).  Pair
-// kernel only (256 tokens and up).
+// kernel only (256 tokens and up), as is `tail`.
 cudaError_t launch_gemm_tc(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
-                           int M, int N, int K, int *err, cudaStream_t s, bool pdl = false);
+                           int M, int N, int K, int *err, cudaStream_t s, bool pdl = false,
+                           const GemmTail *tail = nullptr);
 // The same on CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles).
 cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
-                           int M, int N, int K, int *err, cudaStream_t s, bool pdl = false);
+                           int M, int N, int K, int *err, cudaStream_t s, bool pdl = false,
+                           const GemmTail *tail = nullptr);
 cudaError_t launch_gemm_simt(const uint16_t *x, const uint16_t *wkv, uint16_t *kv, int M, int N,
                              int K, cudaStream_t s);
 

@@ -263,11 +263,12 @@ bool gemm_tc_supported(int M, int N, int K) {
 
 // L layers: x[l] [M, K] and wkv[l] [N, K] -> kv[l] [M, N], one persistent launch.
 cudaError_t launch_gemm_tc(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
-                           int M, int N, int K, int *err, cudaStream_t s, bool pdl) {
+                           int M, int N, int K, int *err, cudaStream_t s, bool pdl, const GemmTail *tail) {
     using namespace tc;
     if (L < 1 || L > kMaxL) return cudaErrorInvalidValue;
     // 256 tokens and up: 256 x 256 tiles on CTA pairs (gemm_tc2.cu), bit-identical
-    if (M >= 256) return launch_gemm_tc2(L, x, wkv, kv, M, N, K, err, s, pdl);
+    // except for tiles of a last wave cut along K (only with `tail`)
+    if (M >= 256) return launch_gemm_tc2(L, x, wkv, kv, M, N, K, err, s, pdl, tail);
     Params p{};
     for (int l = 0; l < L; ++l) {
         if (!make_map(&p.ta[l], x[l], (uint64_t)K, (uint64_t)M, BM)) return cudaErrorInvalidValue;

@@ -52,24 +52,45 @@ struct Params {
     int m_tiles, n_tiles, group_m;                  // m_tiles: 256-row pair tiles
     int full_per_pair;                              // whole tiles every pair takes first
     int tail_tiles, split;                          // the last tiles, each cut into `split` column parts
+    int ksplit, kb_per;                             // or (ksplit > 1) into ksplit K ranges of kb_per k steps
+    float *part;                                    // K-split partials [tail tile][ksplit][256 columns][256 rows]
+    int n_pairs;                                    // CTA pairs of the launch
     int pdl;                                        // wait for the previous kernel after the set-up
     int *err;
 };
 
 // Work item k of a pair: its whole tiles first (tile pair + k P, P pairs),
-// then column parts u = pair + j P of the last tail_tiles tiles (split parts
-// of BN / split columns each), so the partial last wave is spread over every
-// pair.  A part keeps every output's K order, so results do not depend on it.
+// then the last tail_tiles tiles spread over every pair, either as column
+// parts u = pair + j P (split parts of BN / split columns each: a part keeps
+// every output's K order, so results do not depend on it) or, with ksplit > 1,
+// as K ranges: item u = pair is range u % ksplit of tail tile u / ksplit (at
+// most one an item a pair, since tail_tiles * ksplit <= P).  A K range's
+// product goes to an f32 partial tile; gemm_tail_fixup_kernel, launched next,
+// adds each tile's ranges in range order and stores its bf16 kv.
 struct Work {
     int l, mt, nt, n0, width;                      // n0: first column of the item
+    int kb0, kb1;                                  // the item's k steps
+    int tail, j;                                   // K-split item: tail tile and range (tail < 0 otherwise)
 };
 __device__ __forceinline__ bool work_item(const Params &p, int pair, int n_pairs, int k, Work &w) {
     const int tiles_per_layer = p.m_tiles * p.n_tiles;
     int tile, part = 0;
     w.width = BN;
+    w.kb0 = 0;
+    w.kb1 = p.K / BK;
+    w.tail = -1;
+    w.j = 0;
     if (k < p.full_per_pair) {
         tile = pair + k * n_pairs;
         if (tile >= tiles_per_layer * p.L) return false;
+    } else if (p.ksplit > 1) {
+        const int u = pair + (k - p.full_per_pair) * n_pairs;
+        if (u >= p.tail_tiles * p.ksplit) return false;
+        w.tail = u / p.ksplit;
+        w.j = u % p.ksplit;
+        tile = p.full_per_pair * n_pairs + w.tail;
+        w.kb0 = w.j * p.kb_per;
+        w.kb1 = min(w.kb1, w.kb0 + p.kb_per);
     } else {
         const int u = pair + (k - p.full_per_pair) * n_pairs;
         if (u >= p.tail_tiles * p.split) return false;
@@ -190,7 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int m0 = w.mt * 2 * BMC + (int)rank * BMC, n0 = w.n0 + (int)rank * half;
                 const CUtensorMap *mb = w.width == BN ? &p.tb[w.l] : &p.tbs[w.l];
                 const uint32_t bytes = kStageA + (uint32_t)half * BK * 2;
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(empty(s), ((it / STAGES) & 1) ^ 1, abort_flag, p.err)) break;
                     if (rank == 0) mbar_expect_tx(full(s), 2 * bytes);
@@ -219,7 +240,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem + acc * BN;
                 const uint32_t idesc = idesc_bf16(2 * BMC, w.width);
                 bool ok = true;
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(full(s), (it / STAGES) & 1, abort_flag, p.err)) { ok = false; break; }
                     tc_fence_after();
@@ -227,7 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint64_t da = sdesc(sa), db = sdesc(sa + kStageA);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)              // +32 bytes = 2 in the address field
-                        mma_pair(d, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
+                        mma_pair(d, da + 2u * kk, db + 2u * kk, idesc, (kb != w.kb0) | (kk != 0));
                     commit_both(empty(s));
                 }
                 if (!ok) break;
@@ -252,6 +273,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int m = w.mt * 2 * BMC + row, n0 = w.n0;
             uint16_t *out = p.kv[w.l] + (size_t)m * p.N;
+            if (w.tail >= 0) {
+                // K-split item: this CTA's 128 rows of the f32 partial, column-major
+                // ([column][row]: a warp's 32 rows of one column are one 128-byte
+                // line); gemm_tail_fixup_kernel adds the ranges after the launch
+                float *pcol = p.part + (size_t)(w.tail * p.ksplit + w.j) * BN * (2 * BMC) + row;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + acc * BN + c, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) pcol[(size_t)(c + j) * (2 * BMC)] = __uint_as_float(v[j]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa(tempty(acc), 0));
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < w.width; c += 32) {
                 uint32_t v[32];
@@ -288,12 +326,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 }
 
+// The K-split tiles of the last wave: kv = bf16(sum of the ksplit partials in
+// range order) -- a fixed order, so the result does not depend on timing.  A
+// thread takes 8 columns of one row; the 32 threads of a warp take 32
+// consecutive rows, so every partial load is a 128-byte line.
+__global__ void __launch_bounds__(256) gemm_tail_fixup_kernel(const __grid_constant__ Params p) {
+    const int tpt = BN / 8 * (2 * BMC);                              // threads a tail tile
+    const int gid = blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= p.tail_tiles * tpt) return;
+    const int tail = gid / tpt, r = gid % tpt;
+    const int row = r % (2 * BMC), c0 = (r / (2 * BMC)) * 8;
+    const int tile = p.full_per_pair * p.n_pairs + tail;
+    const int tiles_per_layer = p.m_tiles * p.n_tiles;
+    const int l = tile / tiles_per_layer;
+    int mt, nt;
+    tile_coords(tile % tiles_per_layer, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+    const int m = mt * 2 * BMC + row, n = nt * BN + c0;
+    if (m >= p.M || n >= p.N) return;
+    const float *src = p.part + (size_t)tail * p.ksplit * BN * (2 * BMC) + (size_t)c0 * (2 * BMC) + row;
+    float a[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a[e] = __ldcg(src + e * (2 * BMC));
+    for (int j = 1; j < p.ksplit; ++j) {
+        const float *pj = src + (size_t)j * BN * (2 * BMC);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a[e] += __ldcg(pj + e * (2 * BMC));
+    }
+    *reinterpret_cast<uint4 *>(p.kv[l] + (size_t)m * p.N + n) =
+        make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                   pack_bf16x2(a[6], a[7]));
+}
+
 }  // namespace tc2
 
 // L layers: x[l] [M, K] and wkv[l] [N, K] -> kv[l] [M, N], one persistent
 // launch of CTA pairs.
 cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *const *wkv, uint16_t *const *kv,
-                            int M, int N, int K, int *err, cudaStream_t s, bool pdl) {
+                            int M, int N, int K, int *err, cudaStream_t s, bool pdl, const GemmTail *tail) {
     using namespace tc2;
     if (L < 1 || L > kMaxL || M < 1 || K < BK || K % BK || N < 8 || N % 8) return cudaErrorInvalidValue;
     Params p{};
@@ -329,7 +398,24 @@ cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *con
     // 6/8 of a whole tile, a quarter part 5/8 (measured: quarter parts made the
     // 4096-token GEMM's 52-tile tail slower, the 512-token one's faster).
     const int R = tiles % pairs;
-    int split = 1, best = R > 0 ? 8 : 0;
+    // With partial-tile scratch, a last wave of at most half the pairs is cut
+    // along K instead: each of its R tiles into ksplit ranges (ksplit <= 8, so
+    // the fix-up reads at most eight partials), one range a pair; the wave then
+    // costs about 1 / ksplit of a round plus the fix-up.
+    const int kblocks = K / BK;
+    if (tail && tail->part && R > 0 && 2 * R <= pairs && R <= kTailItems) {
+        int ks = pairs / R;
+        ks = ks > 8 ? 8 : ks;
+        ks = ks > kblocks ? kblocks : ks;
+        const int kb_per = (kblocks + ks - 1) / ks;
+        p.ksplit = (kblocks + kb_per - 1) / kb_per;              // no empty range
+        p.kb_per = kb_per;
+        p.part = tail->part;
+        p.split = 1;
+        p.full_per_pair = (tiles - R) / pairs;
+        p.tail_tiles = R;
+    }
+    int split = 1, best = R > 0 && p.ksplit < 2 ? 8 : 0;
     for (int c = 2; c <= 4 && R > 0; c *= 2) {
         const int cost = ((R * c + pairs - 1) / pairs) * (c == 2 ? 6 : 5);
         if (cost < best) {
@@ -337,8 +423,9 @@ cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *con
             split = c;
         }
     }
-    p.split = split;
-    if (split > 1) {
+    if (p.ksplit >= 2) {
+        // set above
+    } else if ((p.split = split) > 1) {
         p.full_per_pair = (tiles - R) / pairs;
         p.tail_tiles = R;
         for (int l = 0; l < L; ++l)
@@ -349,6 +436,7 @@ cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *con
         p.tail_tiles = 0;
     }
     p.pdl = pdl ? 1 : 0;
+    p.n_pairs = pairs;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(kThreads);
@@ -359,7 +447,11 @@ cudaError_t launch_gemm_tc2(int L, const uint16_t *const *x, const uint16_t *con
     la[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = la;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, p);
+    if (e != cudaSuccess || p.ksplit < 2) return e;
+    const int threads = p.tail_tiles * (BN / 8) * (2 * BMC);
+    gemm_tail_fixup_kernel<<<(threads + 255) / 256, 256, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace engram

@@ -104,7 +104,7 @@ void engram_tables_destroy(engram_tables *t);
 int engram_hasher_create(const engram_tables *t, int32_t batch, int64_t max_seq,
                          engram_hasher **out);
 /* `EngramHasher::reset`: the cache returns to zeros (enqueued on `stream`);
- * the projection's work counters too (after ENGRAM_E_TIMEOUT they may not be). */
+ * the projection's counters too (after ENGRAM_E_TIMEOUT they may not be). */
 int engram_hasher_reset(engram_hasher *hs, uintptr_t stream);
 void engram_hasher_destroy(engram_hasher *hs);
 
@@ -289,7 +289,11 @@ size_t engram_workspace_bytes(const engram_geom *geom, int64_t max_tokens);
 /* Byte offsets inside the workspace for `tokens` tokens: off[0] = row ids,
  * off[1 + l] = kv of layer l, off[1 + n_layers + l] = gathered rows x of
  * layer l (present only when the projection runs as a GEMM: tokens > 8, or
- * C * head_dim > 6144), off[1 + 2 n_layers] = total bytes.
+ * C * head_dim > 6144), off[1 + 2 n_layers] = total bytes.  From 256 tokens
+ * the total also covers, at the end, 24 MiB of f32 partial tiles for the
+ * tensor-core GEMM's last wave, which it may cut along K (the tiles of that
+ * wave are then summed from K ranges in a fixed order: deterministic, but not
+ * bit-identical to the unsplit accumulation).
  * off must hold 2 + 2 * n_layers entries. */
 int engram_workspace_layout(const engram_geom *geom, int64_t tokens, size_t *off);
 

@@ -54,9 +54,12 @@ def test_workspace_layout(E):
     assert off[1] == 256 * ((1 * 2 * C * 8 + 255) // 256)
     assert off[2] - off[1] == 256 * ((N * 2 + 255) // 256)
     assert off[-1] == E.engram_workspace_bytes(g, 1)
-    # prefill adds the gathered x per layer
+    # prefill adds the gathered x per layer, and (from 256 tokens) the CTA-pair
+    # GEMM's 24 MiB of last-wave partial tiles at the end
     big = E.engram_workspace_layout(g, 4096)
-    assert big[-1] - big[3] == 2 * 4096 * C * 256 * 2
+    assert big[-1] - big[3] == 2 * 4096 * C * 256 * 2 + 96 * 256 * 256 * 4
+    small = E.engram_workspace_layout(g, 255)
+    assert small[-1] - small[3] == 2 * 255 * C * 256 * 2
     assert E.engram_workspace_bytes(_geom(E, hc=5), 1) == 0
 
 
