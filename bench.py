@@ -335,32 +335,35 @@ def run_decode_only(cfg, steps, warm=10, tables_on_host=False, batch=1):
             "step_algorithmic_bytes": sb, "step_gbs": sb / (ms * 1e-3) / 1e9}
 
 
-def run_decode_graph(cfg, steps, warm=10):
-    """Single-token decode steps replayed from one captured graph; the next
-    ids are copied into the graph's id buffer on the device before each replay."""
+def run_decode_graph(cfg, steps, warm=32, per_graph=32):
+    """Single-token decode steps replayed from one captured graph of
+    `per_graph` consecutive steps; each replay's ids are copied into the
+    graph's id buffer on the device first."""
     import torch
     from deepseek_v4_engram_hash_gb300 import _lib as E
     from deepseek_v4_engram_hash_gb300 import runner, synth
 
+    steps = max(per_graph, steps // per_graph * per_graph)
+    warm = max(per_graph, warm // per_graph * per_graph)
     cfg = cfg.with_(decode_steps=steps + warm + 8)
     eng = runner.EngramSetup(cfg, batch=1, max_tokens=1)
     pre = torch.from_numpy(eng.ids_for("prefix", cfg.prefix)).cuda()
     out = torch.empty((1, cfg.prefix, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
     E.engram_hash(eng.hasher, pre, cfg.prefix, 0, out)
     n = warm + steps
-    ids = torch.from_numpy(eng.ids_for("decode", n).reshape(n, 1, 1)).cuda()
-    d_ids = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    ids = torch.from_numpy(eng.ids_for("decode", n).reshape(n // per_graph, per_graph, 1, 1)).cuda()
+    d_ids = torch.zeros((per_graph, 1, 1), dtype=torch.int32, device="cuda")
     d_pos = torch.tensor([cfg.prefix], dtype=torch.int64, device="cuda")
-    d_h = torch.from_numpy(synth.highway(cfg, [cfg.prefix])).cuda()
-    graph = E.Graph(eng.hasher, eng.layers, d_ids, 1, d_pos, d_h, cfg.eps, eng.ws, eng.ws_bytes)
-    for i in range(warm):
+    d_h = torch.from_numpy(synth.highway(cfg, np.arange(per_graph))).cuda().view(per_graph, 1, cfg.hc, cfg.dim)
+    graph = E.Graph(eng.hasher, eng.layers, d_ids, 1, d_pos, d_h, cfg.eps, eng.ws, eng.ws_bytes, steps=per_graph)
+    for i in range(warm // per_graph):
         d_ids.copy_(ids[i])
         graph.launch()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
-    for i in range(steps):
-        d_ids.copy_(ids[warm + i])
+    for i in range(steps // per_graph):
+        d_ids.copy_(ids[warm // per_graph + i])
         graph.launch()
     t1.record()
     torch.cuda.synchronize()
@@ -370,7 +373,8 @@ def run_decode_graph(cfg, steps, warm=10):
     del eng
     torch.cuda.empty_cache()
     return {"tokens_per_step": 1, "ms_per_step": ms, "tokens_per_s": 1.0 / (ms * 1e-3),
-            "note": "one graph replay a step plus a device copy of the next id"}
+            "note": f"graphs of {per_graph} consecutive steps, one replay plus a device copy of its ids "
+                    f"every {per_graph} steps"}
 
 
 def _barrier(world):
@@ -660,6 +664,8 @@ def main():
         r["note"] = "one-byte e8m0 table scales (264 B a row instead of 288 B)"
         others[configs.V41_DECODE_E8M0.name] = r
         r = run_decode_graph(configs.V41_DECODE, 2000)
+        r1 = run_decode_graph(configs.V41_DECODE, 2000, per_graph=1)
+        r["single_step_graph"] = {"ms_per_step": r1["ms_per_step"], "tokens_per_s": r1["tokens_per_s"]}
         r["workload"] = "v41_decode_T1_graph"
         others["v41_decode_T1_graph"] = r
         r = run_decode_only(configs.V41_DECODE, 2000, tables_on_host=True)

@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
                                      P, sz, st], ctypes.c_int),
             "engram_graph_create": ([P, ctypes.POINTER(engram_layer), P, i32, P, P, ctypes.c_float,
                                      P, sz, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
+            "engram_graph_create_steps": ([P, ctypes.POINTER(engram_layer), P, i32, i32, P, P, ctypes.c_float,
+                                           P, sz, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
             "engram_graph_launch": ([P, st], ctypes.c_int),
             "engram_graph_destroy": ([P], None),
             "engram_workspace_bytes": ([ctypes.POINTER(engram_geom), i64], sz),
@@ -271,14 +273,21 @@ def engram_forward_dpos(hs: Hasher, layers, d_ids, T, d_start_pos, d_h, eps, d_w
 
 
 class Graph:
-    """A captured decode step (`engram_graph_create`); replay with launch()."""
+    """Captured decode steps (`engram_graph_create_steps`; steps = 1 is
+    `engram_graph_create`); replay with launch()."""
 
-    def __init__(self, hs: Hasher, layers, d_ids, T, d_start_pos, d_h, eps, d_ws, ws_bytes):
+    def __init__(self, hs: Hasher, layers, d_ids, T, d_start_pos, d_h, eps, d_ws, ws_bytes, steps: int = 1):
         self._keep = (hs, layers if isinstance(layers, ctypes.Array) else layers_array(layers))
         g = ctypes.c_void_p()
-        _ok(lib().engram_graph_create(hs.handle, self._keep[1], _ptr(d_ids), int(T), _ptr(d_start_pos),
-                                      _ptr(d_h), float(eps), _ptr(d_ws), int(ws_bytes), ctypes.byref(g)),
-            "engram_graph_create")
+        if steps == 1:
+            _ok(lib().engram_graph_create(hs.handle, self._keep[1], _ptr(d_ids), int(T), _ptr(d_start_pos),
+                                          _ptr(d_h), float(eps), _ptr(d_ws), int(ws_bytes), ctypes.byref(g)),
+                "engram_graph_create")
+        else:
+            _ok(lib().engram_graph_create_steps(hs.handle, self._keep[1], _ptr(d_ids), int(T), int(steps),
+                                                _ptr(d_start_pos), _ptr(d_h), float(eps), _ptr(d_ws),
+                                                int(ws_bytes), ctypes.byref(g)),
+                "engram_graph_create_steps")
         self.handle = g
 
     def launch(self, stream=None):

@@ -261,7 +261,7 @@ int engram_check(uintptr_t stream) {
 namespace {
 
 HashArgs hash_args(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t start_pos,
-                   int64_t *d_row_ids, const int64_t *d_pos = nullptr) {
+                   int64_t *d_row_ids, const int64_t *d_pos = nullptr, bool pos_stable = false) {
     const engram_tables *t = hs->t;
     HashArgs a;
     a.ids = d_ids;
@@ -269,6 +269,7 @@ HashArgs hash_args(engram_hasher *hs, const int32_t *d_ids, int32_t T, int64_t s
     a.T = T;
     a.start_pos = start_pos;
     a.start_pos_dev = d_pos;
+    a.pos_stable = pos_stable ? 1 : 0;
     a.token_map = t->token_map;
     a.vocab = t->g.vocab;
     a.pad_id = t->pad_id;
@@ -484,12 +485,22 @@ size_t engram_workspace_bytes(const engram_geom *geom, int64_t max_tokens) {
 
 namespace {
 
+// How a step reads a device-resident position: at *d_pos + offset; the step's
+// gate then adds advance (0: leaves it); stable: nothing writes it before
+// this step's own gate.
+struct DevPos {
+    int64_t offset, advance;
+    bool stable;
+};
+
 // The forward; d_pos (device memory) replaces start_pos when set, and is then
-// advanced by T at the end of the step.
+// advanced by T at the end of the step (or as `dp` says).
 int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
                  int64_t start_pos, int64_t *d_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes,
-                 uintptr_t stream, cudaEvent_t gate_wait = nullptr) {
+                 uintptr_t stream, cudaEvent_t gate_wait = nullptr, const DevPos *dp = nullptr) {
     if (!hs || !layers) return ENGRAM_E_NULL;
+    const DevPos dpos = dp ? *dp : DevPos{0, T, false};
+    if (d_pos) start_pos = dpos.offset;
     int rc = check_hash(hs, d_ids, T, d_pos ? 0 : start_pos, d_ws);
     if (rc || T == 0) return rc;                  // T == 0: a valid no-op
     if (d_pos && !aligned(d_pos, 8)) return ENGRAM_E_ALIGN;
@@ -550,7 +561,7 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
     record(0, s);
     cudaError_t e = cudaSuccess;
     if (!fuse_hash && !hash_in_rows) {
-        e = launch_hash(hash_args(hs, d_ids, T, start_pos, ids, d_pos), s);
+        e = launch_hash(hash_args(hs, d_ids, T, start_pos, ids, d_pos, dpos.stable), s);
         if (e != cudaSuccess) return ENGRAM_E_CUDA;
     }
     record(1, s);
@@ -563,8 +574,8 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
     ga.D = g.dim;
     ga.eps = eps;
     ga.inv_sqrt_dim = powf((float)g.dim, -0.5f);
-    ga.advance_pos = d_pos;
-    ga.advance_by = T;
+    ga.advance_pos = dpos.advance ? d_pos : nullptr;
+    ga.advance_by = dpos.advance;
     for (int l = 0; l < L; ++l) {
         ga.kv[l] = reinterpret_cast<uint16_t *>(ws + off[1 + l]);
         ga.qk[l] = layers[l].qk;
@@ -596,7 +607,7 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
         a.id_stride = (int64_t)L * C;
         a.gather = 1;
         a.fuse_hash = fuse_hash ? 1 : 0;
-        a.hash = hash_args(hs, d_ids, T, start_pos, ids, d_pos);
+        a.hash = hash_args(hs, d_ids, T, start_pos, ids, d_pos, dpos.stable);
         a.pdl = 1;
         a.sched = hs->sched;
         a.err = err;
@@ -606,7 +617,7 @@ int forward_impl(engram_hasher *hs, const engram_layer *layers, const int32_t *d
         record(3, s);
     } else {
         if (hash_in_rows) {
-            e = launch_hash_rows(hr, hash_args(hs, d_ids, T, start_pos, ids, d_pos), s);
+            e = launch_hash_rows(hr, hash_args(hs, d_ids, T, start_pos, ids, d_pos, dpos.stable), s);
             if (e != cudaSuccess) return ENGRAM_E_CUDA;
         } else {
             for (int l = 0; l < L; ++l) {
@@ -667,13 +678,15 @@ int engram_forward_dpos(engram_hasher *hs, const engram_layer *layers, const int
     return forward_impl(hs, layers, d_ids, T, 0, d_start_pos, d_h, eps, d_ws, ws_bytes, stream);
 }
 
-int engram_graph_create(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
-                        int64_t *d_start_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes,
-                        engram_graph **out) {
+int engram_graph_create_steps(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
+                              int32_t steps, int64_t *d_start_pos, float *d_h, float eps, void *d_ws,
+                              size_t ws_bytes, engram_graph **out) {
     if (!out) return ENGRAM_E_NULL;
     *out = nullptr;
-    if (!hs || !layers || !d_start_pos) return ENGRAM_E_NULL;
-    if (T < 1) return ENGRAM_E_INVALID;
+    if (!hs || !layers || !d_start_pos || !d_ids || !d_h) return ENGRAM_E_NULL;
+    if (T < 1 || steps < 1 || steps > 4096 || (int64_t)steps * T > hs->max_seq) return ENGRAM_E_INVALID;
+    const engram_geom &geo = hs->t->g;
+    const int64_t M = (int64_t)hs->batch * T;
     if (!err_ptr()) return ENGRAM_E_CUDA;            // looked up before the capture
     cudaStream_t cs;
     if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return ENGRAM_E_CUDA;
@@ -684,8 +697,15 @@ int engram_graph_create(engram_hasher *hs, const engram_layer *layers, const int
     if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
         rc = ENGRAM_E_CUDA;
     } else {
-        rc = forward_impl(hs, layers, d_ids, T, 0, d_start_pos, d_h, eps, d_ws, ws_bytes,
-                          reinterpret_cast<uintptr_t>(cs));
+        // Step k reads the position at *d_start_pos + k T; only the last step's
+        // gate advances it (by steps T), so every step may hash ahead of the
+        // previous step's gate, as eager calls from host positions do.
+        for (int k = 0; k < steps && rc == ENGRAM_OK; ++k) {
+            const DevPos dp{(int64_t)k * T, k == steps - 1 ? (int64_t)steps * T : 0, true};
+            rc = forward_impl(hs, layers, d_ids + (int64_t)k * M, T, 0, d_start_pos,
+                              d_h + (size_t)k * M * geo.hc * geo.dim, eps, d_ws, ws_bytes,
+                              reinterpret_cast<uintptr_t>(cs), nullptr, &dp);
+        }
         if (cudaStreamEndCapture(cs, &graph) != cudaSuccess && rc == ENGRAM_OK) rc = ENGRAM_E_CUDA;
     }
     g_prof_events = prof;
@@ -703,6 +723,12 @@ int engram_graph_create(engram_hasher *hs, const engram_layer *layers, const int
     }
     *out = g;
     return ENGRAM_OK;
+}
+
+int engram_graph_create(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
+                        int64_t *d_start_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes,
+                        engram_graph **out) {
+    return engram_graph_create_steps(hs, layers, d_ids, T, 1, d_start_pos, d_h, eps, d_ws, ws_bytes, out);
 }
 
 int engram_graph_launch(engram_graph *g, uintptr_t stream) {

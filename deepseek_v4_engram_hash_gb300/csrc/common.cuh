@@ -105,8 +105,9 @@ __device__ __forceinline__ uint4 q2k_lane_decode(uint32_t word, int lane) {
 struct HashArgs {
     const int32_t *ids;
     int32_t B, T;
-    int64_t start_pos;
+    int64_t start_pos;              // the start position, or (with start_pos_dev) an offset added to it
     const int64_t *start_pos_dev;   // when set, the start position is read here (device memory)
+    int32_t pos_stable;             // the device position is not written before this step's own gate
     const int64_t *token_map;
     int64_t vocab, pad_id;
     const int64_t *mult, *primes, *offsets;
@@ -120,11 +121,12 @@ struct HashArgs {
 };
 cudaError_t launch_hash(const HashArgs &a, cudaStream_t s);
 
-// The call's start position: the host value, or the device-resident one.
+// The call's start position: the host value, or the device-resident one plus
+// the host offset (steps after the first of a multi-step graph).
 // A device position that does not fit the cache raises ENGRAM_E_CAPACITY;
 // the caller then skips every cache access (false).
 __device__ __forceinline__ bool hash_start(const HashArgs &a, int64_t &sp) {
-    sp = a.start_pos_dev ? *a.start_pos_dev : a.start_pos;
+    sp = a.start_pos_dev ? *a.start_pos_dev + a.start_pos : a.start_pos;
     if (sp < 0 || sp + a.T > a.max_seq) {
         set_err(a.err, ENGRAM_E_CAPACITY);
         return false;

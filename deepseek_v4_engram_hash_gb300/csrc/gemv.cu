@@ -494,8 +494,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     // constants.  So all of that runs beside the previous step's gate, and only
     // the kv stores (which that gate reads) wait for it: the reducing warp
     // waits, and this grid signals its own dependents only after that wait.  A
-    // device position is advanced by that gate: then everything waits first.
-    const bool early = HASH && a.hash.start_pos_dev == nullptr;
+    // device position is advanced by that gate (one step a launch): then
+    // everything waits first -- unless the position stays put until this
+    // step's own gate (the steps of a multi-step graph after the first).
+    const bool early = HASH && (a.hash.start_pos_dev == nullptr || a.hash.pos_stable);
     if (a.pdl && !early) {
         griddep_wait();
         griddep_launch();

@@ -245,6 +245,18 @@ typedef struct engram_graph engram_graph;
 int engram_graph_create(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
                         int64_t *d_start_pos, float *d_h, float eps, void *d_ws, size_t ws_bytes,
                         engram_graph **out);
+/* The same for `steps` consecutive decode steps in one graph (1 <= steps <=
+ * 4096, steps * T <= max_seq): d_ids [steps, batch, T] and d_h [steps,
+ * batch * T, hc, dim], step k reading ids k and updating highway rows k at
+ * position *d_start_pos + k T; the last step's gate advances the position by
+ * steps * T.  Inside a replay the steps overlap as eager calls do (each step's
+ * hash, row gather and wkv stream run beside the previous step's gate), so one
+ * replay costs about `steps` eager steps plus one graph launch.  Replays give
+ * bit-identical results to `steps` eager engram_forward calls at the same
+ * positions.  engram_graph_create is this with steps = 1. */
+int engram_graph_create_steps(engram_hasher *hs, const engram_layer *layers, const int32_t *d_ids, int32_t T,
+                              int32_t steps, int64_t *d_start_pos, float *d_h, float eps, void *d_ws,
+                              size_t ws_bytes, engram_graph **out);
 int engram_graph_launch(engram_graph *g, uintptr_t stream);
 void engram_graph_destroy(engram_graph *g);
 
