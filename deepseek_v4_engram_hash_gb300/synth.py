@@ -11,11 +11,20 @@ with key `k` is the mix of `k + (i + 1) * 0x9E3779B97F4A7C15`.  Any single
 element of any input can therefore be regenerated on its own, which lets the
 oracle rebuild only the table rows and weight rows it checks.
 
-Normal variates are the centred sum of the four 16-bit fields of one output
-(Irwin-Hall, n = 4: mean 0, variance 4 * (2^32 - 1) / 12), scaled to the
-requested sigma by one f32 multiply.  Every step is integer or a single
-correctly-rounded IEEE operation, so the numpy and CUDA twins produce the same
-bits on any machine.
+Normal variates are N(0, 1) by the Box-Muller transform (Box & Muller, "A note
+on the generation of random normal deviates", Ann. Math. Stat. 1958) of one
+64-bit output: u1 = (high 32 bits + 1) / 2^32 in (0, 1], u2 = low 32 bits /
+2^32, z = sqrt(-2 ln u1) cos(2 pi u2), so |z| <= 6.66.  The logarithm and the
+cosine are evaluated here in float64 from their series with a fixed sequence of
+correctly rounded IEEE operations (no fused multiply-add) -- ln m = 2 atanh(s),
+s = (m - 1) / (m + 1), after an exact reduction of u1 to m in [sqrt(1/2),
+sqrt(2)); cos and sin of (pi/2) f, |f| <= 1/2, after an exact reduction of
+4 u2 by its nearest integer -- so that the CUDA twin, doing the same
+operations, gets the same bits; the result is rounded to f32 and scaled to the
+requested sigma by one f32 multiply.  (Library log and cos may differ in the
+last place between machines; these do not.)  Every other step is integer or a
+single correctly rounded IEEE operation, so the numpy and CUDA twins produce
+the same bits on any machine.
 """
 from __future__ import annotations
 
@@ -27,8 +36,26 @@ import numpy as np
 
 GAMMA = 0x9E3779B97F4A7C15
 _M64 = (1 << 64) - 1
-IH_STD = math.sqrt((2.0 ** 32 - 1.0) / 3.0)     # std of the centred 4 x u16 sum
-IH_CENTRE = 2 * 65535
+
+# Float64 constants of the Box-Muller evaluation, written as exact binary
+# values (the CUDA twin holds the same literals): ln 2, pi / 2, sqrt(1/2), and
+# the series coefficients 1 / (2k + 1) (atanh), (-1)^k / (2k)! (cos) and
+# (-1)^k / (2k + 1)! (sin), each the double nearest the exact rational.
+_LN2 = float.fromhex("0x1.62e42fefa39efp-1")
+_PI_2 = float.fromhex("0x1.921fb54442d18p+0")
+_SQRT_HALF = float.fromhex("0x1.6a09e667f3bcdp-1")
+_ATANH = [float.fromhex(h) for h in (
+    "0x1.0000000000000p+0", "0x1.5555555555555p-2", "0x1.999999999999ap-3", "0x1.2492492492492p-3",
+    "0x1.c71c71c71c71cp-4", "0x1.745d1745d1746p-4", "0x1.3b13b13b13b14p-4", "0x1.1111111111111p-4",
+    "0x1.e1e1e1e1e1e1ep-5", "0x1.af286bca1af28p-5", "0x1.8618618618618p-5")]
+_COS = [float.fromhex(h) for h in (
+    "0x1.0000000000000p+0", "-0x1.0000000000000p-1", "0x1.5555555555555p-5", "-0x1.6c16c16c16c17p-10",
+    "0x1.a01a01a01a01ap-16", "-0x1.27e4fb7789f5cp-22", "0x1.1eed8eff8d898p-29", "-0x1.93974a8c07c9dp-37",
+    "0x1.ae7f3e733b81fp-45", "-0x1.6827863b97d97p-53")]
+_SIN = [float.fromhex(h) for h in (
+    "0x1.0000000000000p+0", "-0x1.5555555555555p-3", "0x1.1111111111111p-7", "-0x1.a01a01a01a01ap-13",
+    "0x1.71de3a556c734p-19", "-0x1.ae64567f544e4p-26", "0x1.6124613a86d09p-33", "-0x1.ae7f3e733b81fp-41",
+    "0x1.952c77030ad4ap-49", "-0x1.2f49b46814157p-57")]
 
 
 # ---------------------------------------------------------------------------
@@ -64,16 +91,64 @@ def splitmix64(key: int, idx) -> np.ndarray:
 
 
 def normal_scale(sigma: float) -> np.float32:
-    """The f32 constant that scales a centred Irwin-Hall sum to std `sigma`."""
-    return np.float32(sigma / IH_STD)
+    """The f32 constant that scales a standard normal to std `sigma`."""
+    return np.float32(sigma)
+
+
+def std_normal_f64(z) -> np.ndarray:
+    """N(0, 1) from SplitMix64 outputs z (uint64) by Box-Muller, in float64 with
+    the fixed operation sequence the CUDA twin repeats (in-place numpy ops
+    round exactly as the separate ones would)."""
+    z = np.asarray(z, dtype=np.uint64)
+    # -2 ln u1, u1 = (a + 1) 2^-32: n = a + 1 = m0 2^e exactly, m0 in [sqrt(1/2), sqrt(2))
+    nd = ((z >> np.uint64(32)) + np.uint64(1)).astype(np.float64)
+    m0, e = np.frexp(nd)
+    low = m0 < _SQRT_HALF
+    m0[low] *= 2.0
+    e = e.astype(np.float64)
+    e[low] -= 1.0
+    s = m0 - 1.0
+    m0 += 1.0
+    s /= m0
+    s2 = s * s
+    p = np.full_like(s, _ATANH[10])
+    for k in range(9, -1, -1):
+        p *= s2
+        p += _ATANH[k]
+    p *= s
+    p *= 2.0                          # ln m
+    e -= 32.0
+    e *= _LN2
+    e += p                            # ln u1
+    e *= -2.0
+    r = np.sqrt(e, out=e)
+    # cos(2 pi u2) = cos((pi/2) w), w = 4 u2 = b 2^-30 = q + f, q the nearest integer
+    w = (z & np.uint64(0xFFFFFFFF)).astype(np.float64)
+    w *= 2.0 ** -30
+    q = np.floor(w + 0.5)
+    w -= q                            # f
+    w *= _PI_2                        # x
+    x2 = w * w
+    c = np.full_like(w, _COS[9])
+    sn = np.full_like(w, _SIN[9])
+    for k in range(8, -1, -1):
+        c *= x2
+        c += _COS[k]
+        sn *= x2
+        sn += _SIN[k]
+    sn *= w
+    qi = q.astype(np.int64)
+    odd = (qi & 1).astype(bool)
+    c[odd] = sn[odd]
+    neg = (qi == 1) | (qi == 2)
+    c[neg] = -c[neg]
+    r *= c
+    return r
 
 
 def normal_f32(key: int, idx, sigma: float) -> np.ndarray:
-    z = splitmix64(key, idx)
-    m = np.uint64(0xFFFF)
-    s = (z & m) + ((z >> np.uint64(16)) & m) + ((z >> np.uint64(32)) & m) + (z >> np.uint64(48))
-    n = s.astype(np.int64) - IH_CENTRE
-    return n.astype(np.float32) * normal_scale(sigma)
+    """N(0, sigma^2) as f32: the float64 standard normal rounded to f32, times sigma."""
+    return std_normal_f64(splitmix64(key, idx)).astype(np.float32) * normal_scale(sigma)
 
 
 def _torch():

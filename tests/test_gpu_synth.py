@@ -45,3 +45,16 @@ def test_wkv_and_highway():
     synth.fill_highway_cuda(cfg, h, first_token=17)
     assert np.array_equal(h.cpu().numpy().view(np.uint32),
                           synth.highway(cfg, np.arange(17, 57)).view(np.uint32))
+
+
+def test_normals_bit_identical_at_scale():
+    """Four million N(0, 1) f32 values (the Box-Muller series evaluation in
+    float64) agree bit for bit between the twins, tails included."""
+    cfg = configs.TINY
+    n_tok = 16384                                          # x hc 2 x dim 128 = 4.2 M values
+    h = torch.empty((n_tok, cfg.hc, cfg.dim), dtype=torch.float32, device="cuda")
+    synth.fill_highway_cuda(cfg, h, first_token=3)
+    want = synth.highway(cfg, np.arange(3, 3 + n_tok))
+    got = h.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    assert np.abs(want).max() > 4.5
