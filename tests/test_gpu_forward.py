@@ -393,3 +393,34 @@ def test_forward_is_bit_reproducible(E, name, T):
     assert torch.equal(outs[0][0], outs[1][0])
     for a, b in zip(outs[0][1], outs[1][1]):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# One layer, N = 20480 (80 column tiles of 256) at 256 tokens: 80 pair tiles on
+# the GPU's pairs leave a last wave of 4 tiles, which the forward cuts along K
+# (K = 512: 8 ranges of one k step); every output of every token is checked.
+KSPLIT = configs.TINY.with_(name="ksplit_tail", layer_ids=(0,), max_ngram=3, n_heads=1, prime_target=509,
+                            head_dim=256, scale_block=32, dim=4096, hc=4, batch=1, T=256, seed=13)
+
+
+def test_forward_ksplit_last_wave(E):
+    """The CTA-pair GEMM's last wave cut along K (f32 partial tiles added in
+    range order by the fix-up launch): kv within tolerance of the oracle on
+    every output, the highway stage-wise and end to end, and two runs
+    bit-identical (the fix-up's order is fixed)."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = KSPLIT
+    outs = []
+    for rep in range(2):
+        eng = runner.EngramSetup(cfg, batch=1, max_tokens=cfg.T)
+        ids = eng.ids_for("ksplit", cfg.T)
+        d_h = _h_device(cfg, 0, cfg.T, True)
+        if rep == 0:
+            _check_call(eng, G.hash_state(cfg, 1), ids, 0, d_h, d_h.cpu().numpy(), np.arange(cfg.T),
+                        np.arange(cfg.N), 0)
+        else:
+            eng.forward(ids, 0, d_h)
+            assert E.engram_check() == 0
+        outs.append((d_h.clone(), eng.kv(cfg.T, 0).clone()))
+        del eng
+    assert torch.equal(outs[0][0].view(torch.int32), outs[1][0].view(torch.int32))
+    assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
