@@ -199,7 +199,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // beside the GEMM's made the 512-token step 2 % slower.)
     if (p.pdl) griddep_wait();
 
-    const int kblocks = p.K / BK;
     const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
     Work w;
 
