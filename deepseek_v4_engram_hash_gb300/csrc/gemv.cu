@@ -15,7 +15,8 @@
 // into registers -- the [T * C, head_dim] rows never touch HBM.  Main loop: a
 // copy warp streams the groups' wkv rows into a shared-memory ring with bulk
 // copies; 16 MMA warps multiply them by x on mma.sync m16n8k16 (bf16 in, f32
-// accumulate).  wkv may also be held as Q2_K
+// accumulate) and hand their partial tiles to a reducing warp, which sums
+// them and stores kv.  wkv may also be held as Q2_K
 // blocks (page "spark_model/layers/engram_v41.rs", the doc of the layer weights:
 // Q2_K wkv, 6x fewer bytes a token, byte-identical results): the
 // same kernel then copies the blocks and decodes each lane's weights into its
@@ -358,8 +359,8 @@ __device__ __forceinline__ void gather_x(const GemvArgs &a, const GemvLayer &ly,
 // 8 s + w / 2 -- lane q in the order j = 0 ^ q%2, 1 ^ q%2, 2 ^ q%2, 3 ^ q%2
 // (K is a multiple of 64 on every path, so a warp's blocks in a stage are
 // all valid, the first pair only, or none, alike for every lane), and the 16
-// partial 16 x 8 tiles of a group are summed in warp order through shared
-// memory; both weight formats follow this order exactly.  bf16: stage i is
+// partial 16 x 8 tiles of a group are summed in warp order by the reducing
+// warp; both weight formats follow this order exactly.  bf16: stage i is
 // the CTA's group i / nsub, k blocks 64 (i % nsub) .. +63.  Q2_K: stage i is
 // its group i.
 template <bool HASH, bool WQ2K>
