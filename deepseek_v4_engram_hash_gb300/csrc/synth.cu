@@ -62,14 +62,12 @@ __device__ double std_normal(uint64_t z) {
     const double q = floor(__dadd_rn(w, 0.5));
     const double x = __dmul_rn(__dadd_rn(w, -q), kPi2);
     const double x2 = __dmul_rn(x, x);
-    double c = kCos[9], sn = kSin[9];
-    for (int k = 8; k >= 0; --k) {
-        c = __dadd_rn(__dmul_rn(c, x2), kCos[k]);
-        sn = __dadd_rn(__dmul_rn(sn, x2), kSin[k]);
-    }
-    sn = __dmul_rn(sn, x);
+    // only the series the quadrant needs (the same operations as either of the twin's)
     const int qi = (int)q;
-    double v = (qi & 1) ? sn : c;
+    const double *coef = (qi & 1) ? kSin : kCos;
+    double v = coef[9];
+    for (int k = 8; k >= 0; --k) v = __dadd_rn(__dmul_rn(v, x2), coef[k]);
+    if (qi & 1) v = __dmul_rn(v, x);
     if (qi == 1 || qi == 2) v = -v;
     return __dmul_rn(r, v);
 }
