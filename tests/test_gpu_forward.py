@@ -424,3 +424,48 @@ def test_forward_ksplit_last_wave(E):
         del eng
     assert torch.equal(outs[0][0].view(torch.int32), outs[1][0].view(torch.int32))
     assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
+
+
+# Two layers, N = 4000 (a 160-column last column tile), 768 tokens (three pair
+# rows): 96 pair tiles leave a last wave of 20 tiles, cut into K ranges; the
+# fix-up must stop at column N.
+KSPLIT_RAGGED = configs.TINY.with_(name="ksplit_ragged", layer_ids=(0, 3), max_ngram=3, n_heads=1,
+                                   prime_target=509, head_dim=128, scale_block=32, dim=1000, hc=3,
+                                   batch=3, T=256, seed=14)
+
+
+def test_forward_ksplit_ragged_columns_two_layers(E):
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = KSPLIT_RAGGED
+    eng = runner.EngramSetup(cfg, batch=cfg.batch, max_tokens=cfg.batch * cfg.T)
+    ids = eng.ids_for("ksplit-ragged", cfg.T)
+    M = cfg.batch * cfg.T
+    d_h = _h_device(cfg, 0, M, True)
+    _check_call(eng, G.hash_state(cfg, cfg.batch), ids, 0, d_h, d_h.cpu().numpy(), np.arange(M),
+                np.arange(cfg.N), 0)
+
+
+def test_forward_ksplit_inside_a_multi_step_graph(E):
+    """Two 256-token steps captured in one graph: the pair GEMM's K-split last
+    wave and its fix-up launch replay bit-identically to eager calls."""
+    from deepseek_v4_engram_hash_gb300 import runner
+    cfg = KSPLIT
+    K = 2
+    eng = runner.EngramSetup(cfg, batch=1, max_tokens=cfg.T)
+    hs2 = E.Hasher(eng.tables, 1, cfg.max_seq)
+    ws2 = torch.empty_like(eng.ws)
+    ids = np.stack([eng.ids_for(f"ksg{k}", cfg.T) for k in range(K)])                   # [K, 1, T]
+    h0 = torch.from_numpy(synth.highway(cfg, np.arange(K * cfg.T))).view(K, cfg.T, cfg.hc, cfg.dim)
+    d_he = [h0[k].clone().cuda() for k in range(K)]
+    for k in range(K):
+        eng.forward(ids[k], k * cfg.T, d_he[k])
+    d_pos = torch.zeros((1,), dtype=torch.int64, device="cuda")
+    d_ids = torch.from_numpy(ids).cuda()
+    d_hg = h0.clone().cuda()
+    graph = E.Graph(hs2, eng.layers, d_ids, cfg.T, d_pos, d_hg, cfg.eps, ws2, eng.ws_bytes, steps=K)
+    graph.launch()
+    assert E.engram_check() == 0
+    for k in range(K):
+        assert torch.equal(d_he[k].view(torch.int32), d_hg[k].view(torch.int32)), f"step {k}"
+    assert d_pos.item() == K * cfg.T
+    graph.close()
