@@ -38,3 +38,23 @@ def test_extremes_of_the_transform():
     assert abs(x[1] - r) < 1e-13                            # cos 0 = 1
     assert abs(x[2]) < 1e-13                                # cos(pi/2) = 0 at 4 u2 = 1
     assert abs(x[3] + r) < 1e-13                            # cos(pi) = -1
+
+
+def test_cuda_twin_holds_the_same_constants():
+    """The CUDA twin's series coefficients and constants are the numpy twin's
+    (read from its source: the two evaluate the same operations on the same
+    doubles)."""
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(synth.__file__), "csrc", "synth.cu")).read()
+
+    def arr(name):
+        body = re.search(name + r"\[\d+\] = \{(.*?)\};", src, re.S).group(1)
+        return [float.fromhex(t.strip()) for t in body.split(",") if t.strip()]
+
+    assert arr("kAtanh") == synth._ATANH
+    assert arr("kCos") == synth._COS
+    assert arr("kSin") == synth._SIN
+    for name, val in (("kLn2", synth._LN2), ("kPi2", synth._PI_2), ("kSqrtHalf", synth._SQRT_HALF)):
+        lit = re.search(name + r" = (0x[0-9a-fp.+-]+)", src).group(1)
+        assert float.fromhex(lit) == val, name
