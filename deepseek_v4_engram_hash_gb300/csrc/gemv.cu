@@ -183,32 +183,37 @@ __device__ __forceinline__ Q2kHalf q2k_half(const uint8_t *blk, int half, int q)
     h.dmin = __high2float(dd);
     return h;
 }
+// (d, -dmin/16) as an f32 pair (both exact)
+__device__ __forceinline__ uint64_t q2k_dnm(const Q2kHalf &h) {
+    return (uint64_t)__float_as_uint(h.d) | ((uint64_t)__float_as_uint(h.dmin * -0.0625f) << 32);
+}
 // The same table from the scale byte in place, in the main loop: sc & 15 and
-// (sc & 0xF0) = 16 m both become exact floats by one OR each (2^23 + n), and
-// dmin * m is taken as (dmin * 16 m) * (-1/16) -- both products exact in f32
-// (11-bit dmin times at most 8 bits), v[0] as fma(dl, 0, nml) for the sign of
-// a zero -- so the values are bit-identical to q2k_table's.  Written as one
-// asm block: the decode is bound by the integer pipe, and this form issued
-// fewer of its instructions (45.4 against 46.3 us a step).
-__device__ __forceinline__ uint2 q2k_table_b(uint32_t sc, float d, float dmin) {
+// (sc & 0xF0) = 16 m both become exact floats by one OR each (2^23 + n, then
+// one paired subtraction of 2^23), and one paired multiply by dnm = (d,
+// -dmin/16) gives dl = d * sc and nml = -dmin * m -- both products exact in f32
+// (11-bit d, dmin times at most 8 bits; -dmin/16 is exact), v[0] as fma(dl, 0,
+// nml) for the sign of a zero -- so the values are bit-identical to
+// q2k_table's.  Written as one asm block: the decode is bound by the integer
+// pipe and the issue slots, and this form issued fewer instructions (one asm
+// block: 45.4 against 46.3 us a step; the paired f32x2 steps: 42.9 against
+// 43.8).
+__device__ __forceinline__ uint2 q2k_table_b(uint32_t sc, uint64_t dnm) {
     uint2 r;
-    asm("{\n\t.reg .b32 a, b;\n\t.reg .f32 lo, m16, dl, nml, y0, y1, y2, y3;\n\t"
+    asm("{\n\t.reg .b32 a, b;\n\t.reg .b64 ab, lm, k;\n\t.reg .f32 dl, nml, y0, y1, y2, y3;\n\t"
         "lop3.b32 a, %2, 0xF, 0x4B000000, 0xEA;\n\t"
         "lop3.b32 b, %2, 0xF0, 0x4B000000, 0xEA;\n\t"
-        "mov.b32 lo, a;\n\t"
-        "mov.b32 m16, b;\n\t"
-        "sub.rn.f32 lo, lo, 0f4B000000;\n\t"
-        "sub.rn.f32 m16, m16, 0f4B000000;\n\t"
-        "mul.rn.f32 dl, %3, lo;\n\t"
-        "mul.rn.f32 nml, %4, m16;\n\t"
-        "mul.rn.f32 nml, nml, 0fBD800000;\n\t"
+        "mov.b64 ab, {a, b};\n\t"
+        "mov.b64 k, 0x4B0000004B000000;\n\t"
+        "sub.rn.f32x2 lm, ab, k;\n\t"
+        "mul.rn.f32x2 lm, %3, lm;\n\t"
+        "mov.b64 {dl, nml}, lm;\n\t"
         "fma.rn.f32 y0, dl, 0f00000000, nml;\n\t"
         "fma.rn.f32 y1, dl, 0f3F800000, nml;\n\t"
         "fma.rn.f32 y2, dl, 0f40000000, nml;\n\t"
         "fma.rn.f32 y3, dl, 0f40400000, nml;\n\t"
         "cvt.rn.bf16x2.f32 %0, y1, y0;\n\t"
         "cvt.rn.bf16x2.f32 %1, y3, y2;\n\t}"
-        : "=r"(r.x), "=r"(r.y) : "r"(sc), "f"(d), "f"(dmin));
+        : "=r"(r.x), "=r"(r.y) : "r"(sc), "l"(dnm));
     return r;
 }
 // v[0..3] as bf16 pairs (v0 v1, v2 v3) for the sub-block scale byte sc
@@ -358,7 +363,8 @@ __device__ __forceinline__ void gather_x(const GemvArgs &a, const GemvLayer &ly,
 // every row group -- for Q2_K weights the four shifts of half w % 2 of block
 // 8 s + w / 2 -- lane q in the order j = 0 ^ q%2, 1 ^ q%2, 2 ^ q%2, 3 ^ q%2
 // (K is a multiple of 64 on every path, so a warp's blocks in a stage are
-// all valid, the first pair only, or none, alike for every lane), and the 16
+// all valid, the first pair only, or none, alike for every lane; at Q2_K
+// weights a warp with none multiplies zeros, which adds nothing), and the 16
 // partial 16 x 8 tiles of a group are summed in warp order by the reducing
 // warp; both weight formats follow this order exactly.  bf16: stage i is
 // the CTA's group i / nsub, k blocks 64 (i % nsub) .. +63.  Q2_K: stage i is
@@ -595,6 +601,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
     // Q2_K: this lane's scale byte in a scale word, and the quant shifts 2j of blocks jj = 0, 1
     const int sc_byte = 8 * (warp & 1) + 2 * (q & 1) + (q >> 1);
     const uint32_t q_sh0 = 2u * (q & 1), q_sh1 = 2u - q_sh0;
+    const int nblk_q = K >> 8;                                           // Q2_K blocks a row
     for (int gi = 0;; ++gi) {
         // the group's first stage names the group (-1: the end marker, the
         // same for every warp); a warp that finds the CTA aborting leaves
@@ -605,43 +612,46 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const __grid_c
         if (grp >= 0) {
             if (WQ2K) {
                 // this warp's blocks 8 s + w/2, half w % 2, of rows g and g + 8
-                const uint8_t *row_lo = smem_raw + (gi % R::kStages) * R::kStageBytes + g * q2k_row +
-                                        (warp >> 1) * 84;
+                const uint8_t *row_lo = smem_raw + (gi % R::kStages) * R::kStageBytes + g * q2k_row;
                 const uint8_t *row_hi = row_lo + 8 * q2k_row;
+                // No test between the stages (their decode work then interleaves:
+                // 43.8 against 45.2 us a step): a warp past the last block of a
+                // narrower K decodes the row's last block instead, against x = 0
+                // (its fragments are zero), adding exact zeros.
 #pragma unroll
                 for (int sub = 0; sub < kMmaSubMax; ++sub) {
-                    if (sub < nsub && sub * kStageKb + warp * kMmaJ < kblocks) {
-                        const uint8_t *bl = row_lo + sub * 8 * 84, *bh = row_hi + sub * 8 * 84;
-                        const Q2kHalf hl = q2k_half(bl, warp & 1, q);
-                        const Q2kHalf hh = q2k_half(bh, warp & 1, q);
-                        // Block jj of the lane is shift j = jj ^ q%2.  At jj = 0, 2 the lane
-                        // builds the value table of its sub-block (scale byte 2 (q%2) + q/2 of
-                        // word jj/2); at jj = 1, 3 it needs shift j ^ 1 of the same pair,
-                        // whose table lane q ^ 1 (same row, same sub-block) built at jj - 1.
-                        uint2 vl[kMmaJ], vh[kMmaJ];
+                    const int blk = min(sub * 8 + (warp >> 1), nblk_q - 1);
+                    const uint8_t *bl = row_lo + blk * 84, *bh = row_hi + blk * 84;
+                    const Q2kHalf hl = q2k_half(bl, warp & 1, q);
+                    const Q2kHalf hh = q2k_half(bh, warp & 1, q);
+                    const uint64_t dl_ = q2k_dnm(hl), dh_ = q2k_dnm(hh);
+                    // Block jj of the lane is shift j = jj ^ q%2.  At jj = 0, 2 the lane
+                    // builds the value table of its sub-block (scale byte 2 (q%2) + q/2 of
+                    // word jj/2); at jj = 1, 3 it needs shift j ^ 1 of the same pair,
+                    // whose table lane q ^ 1 (same row, same sub-block) built at jj - 1.
+                    uint2 vl[kMmaJ], vh[kMmaJ];
 #pragma unroll
-                        for (int p = 0; p < 2; ++p) {
-                            vl[2 * p] = q2k_table_b(bl[sc_byte + 4 * p], hl.d, hl.dmin);
-                            vh[2 * p] = q2k_table_b(bh[sc_byte + 4 * p], hh.d, hh.dmin);
-                        }
+                    for (int p = 0; p < 2; ++p) {
+                        vl[2 * p] = q2k_table_b(bl[sc_byte + 4 * p], dl_);
+                        vh[2 * p] = q2k_table_b(bh[sc_byte + 4 * p], dh_);
+                    }
 #pragma unroll
-                        for (int p = 0; p < 2; ++p) {
-                            vl[2 * p + 1] = make_uint2(__shfl_xor_sync(0xFFFFFFFFu, vl[2 * p].x, 1),
-                                                       __shfl_xor_sync(0xFFFFFFFFu, vl[2 * p].y, 1));
-                            vh[2 * p + 1] = make_uint2(__shfl_xor_sync(0xFFFFFFFFu, vh[2 * p].x, 1),
-                                                       __shfl_xor_sync(0xFFFFFFFFu, vh[2 * p].y, 1));
-                        }
+                    for (int p = 0; p < 2; ++p) {
+                        vl[2 * p + 1] = make_uint2(__shfl_xor_sync(0xFFFFFFFFu, vl[2 * p].x, 1),
+                                                   __shfl_xor_sync(0xFFFFFFFFu, vl[2 * p].y, 1));
+                        vh[2 * p + 1] = make_uint2(__shfl_xor_sync(0xFFFFFFFFu, vh[2 * p].x, 1),
+                                                   __shfl_xor_sync(0xFFFFFFFFu, vh[2 * p].y, 1));
+                    }
 #pragma unroll
-                        for (int jj = 0; jj < kMmaJ; ++jj) {
-                            const uint32_t sh = ((jj & 1) ? q_sh1 : q_sh0) + ((jj & 2) ? 4u : 0u);    // 2j
-                            const uint2 l0 = q2k_pick4_asm(vl[jj], hl.q0, sh);
-                            const uint2 l1 = q2k_pick4_asm(vl[jj], hl.q1, sh);
-                            const uint2 h0 = q2k_pick4_asm(vh[jj], hh.q0, sh);
-                            const uint2 h1 = q2k_pick4_asm(vh[jj], hh.q1, sh);
-                            const uint4 xb = xr[sub][jj];
-                            mma_16816(c, l0.x, h0.x, l0.y, h0.y, xb.x, xb.y);
-                            mma_16816(c, l1.x, h1.x, l1.y, h1.y, xb.z, xb.w);
-                        }
+                    for (int jj = 0; jj < kMmaJ; ++jj) {
+                        const uint32_t sh = ((jj & 1) ? q_sh1 : q_sh0) + ((jj & 2) ? 4u : 0u);    // 2j
+                        const uint2 l0 = q2k_pick4_asm(vl[jj], hl.q0, sh);
+                        const uint2 l1 = q2k_pick4_asm(vl[jj], hl.q1, sh);
+                        const uint2 h0 = q2k_pick4_asm(vh[jj], hh.q0, sh);
+                        const uint2 h1 = q2k_pick4_asm(vh[jj], hh.q1, sh);
+                        const uint4 xb = xr[sub][jj];
+                        mma_16816(c, l0.x, h0.x, l0.y, h0.y, xb.x, xb.y);
+                        mma_16816(c, l1.x, h1.x, l1.y, h1.y, xb.z, xb.w);
                     }
                 }
                 release(gi);
@@ -694,7 +704,8 @@ static cudaError_t launch_mma(const GemvArgs &a, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (a.T < 1 || a.T > kMmaT || a.K % (WQ2K ? 256 : 64) || a.K > kGemvMaxK) return cudaErrorInvalidValue;
+    if (a.T < 1 || a.T > kMmaT || a.K % (WQ2K ? 256 : 64) || a.K > kGemvMaxK || (WQ2K && a.K < 256))
+        return cudaErrorInvalidValue;
     if (HASH && (size_t)a.T * a.C > (size_t)kFusedHashMaxIds) return cudaErrorInvalidValue;
     for (int l = 0; l < a.L; ++l) {
         const void *w = WQ2K ? static_cast<const void *>(a.layer[l].wkv_q2k) : static_cast<const void *>(a.layer[l].wkv);

@@ -50,7 +50,7 @@ def test_project_q2k_bit_identical_to_bf16_on_dequantised(E, K, N):
     assert G.kv_rel_err(_u16(kv_q)[:, rows], want) <= G.KV_TOL
 
 
-@pytest.mark.parametrize("B", [1, 3, 8])
+@pytest.mark.parametrize("B", [1, 2, 3, 8])
 def test_forward_wkv_q2k_matches_bf16_path_and_oracle(E, B):
     """Decode steps of B sequences (B tokens a call): the projection from Q2_K
     wkv gives the bf16 path's kv and highway bit for bit, and the oracle's
