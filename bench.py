@@ -56,6 +56,37 @@ TENSOR_PIPE_ACTIVE = 0.947
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by the
 # source hash of the kernel they were taken on; a changed kernel reports null.
 NCU_TRAFFIC = {("gemv", "a87084ccbf2f"): 506553088}   # 503.45 MB read + 3.10 MB written
+# Integer-pipe (ALU) warp instructions of one Q2_K-weight decode launch (T = 1,
+# both layers) from one ncu capture (sm__inst_executed_pipe_alu.sum), keyed the same way.
+NCU_ALU = {("gemv_q2k", "a87084ccbf2f"): 15024147}
+
+
+def _sm_count() -> int:
+    import torch
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+
+def q2k_alu_roofline(r, clocks, hbm, sms):
+    """The Q2_K-weight decode is bound by its integer pipe, not by HBM: its
+    ALU instructions (ncu, one launch) over the launch's event-timed duration,
+    against the pipe's peak -- 16 lanes a cycle in each of the 4 sub-partitions
+    of every SM (one warp instruction every 2 cycles) at the SM clock sampled
+    during the benchmark.  The HBM fraction of the same launch beside it."""
+    mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    peak = sms * 4 * 0.5 * mhz * 1e6 / 1e12                       # T warp instructions / s
+    gemv_s = r["stage_ms"]["gemv"] * 1e-3
+    n = NCU_ALU.get(("gemv_q2k", _src_hash("gemv.cu", "common.cuh")))
+    wbytes = r["step_algorithmic_bytes"]
+    out = {"bound": "alu", "unit": "T integer-pipe warp instructions/s", "peak": peak,
+           "peak_source": f"{sms} SMs x 4 sub-partitions x 0.5 warp instructions a cycle x {mhz:.0f} MHz",
+           "kernel": "gemv_mma_kernel<1, 1> (fused hash, row gather, Q2_K decode and wkv GEMV, both layers)",
+           "kernel_ms": r["stage_ms"]["gemv"],
+           "hbm_frac": wbytes / gemv_s / 1e9 / hbm}
+    if n is None:                       # the kernel changed since the count was taken
+        out.update(achieved=None, frac=None, instructions=None)
+    else:
+        out.update(achieved=n / gemv_s / 1e12, frac=n / gemv_s / 1e12 / peak, instructions=n)
+    return out
 
 
 class Clocks:
@@ -298,19 +329,20 @@ def run_other(cfg, prefill_steps, decode_steps, warm=3, tables_on_host=False):
     return out
 
 
-def run_decode_only(cfg, steps, warm=10, tables_on_host=False, batch=1):
-    """Single-token decode steps of `batch` sequences after the configured look-back."""
+def run_decode_only(cfg, steps, warm=10, tables_on_host=False, batch=1, stage_steps=0):
+    """Single-token decode steps of `batch` sequences after the configured look-back
+    (and, with stage_steps, as many more with events between the stages)."""
     import torch
     from deepseek_v4_engram_hash_gb300 import _lib as E
     from deepseek_v4_engram_hash_gb300 import runner, synth
 
-    cfg = cfg.with_(decode_steps=steps + warm + 8, batch=batch)
+    cfg = cfg.with_(decode_steps=steps + warm + stage_steps + 8, batch=batch)
     eng = runner.EngramSetup(cfg, batch=batch, max_tokens=batch, tables_on_host=tables_on_host)
     if cfg.prefix:
         pre = torch.from_numpy(eng.ids_for("prefix", cfg.prefix)).cuda()
         out = torch.empty((batch, cfg.prefix, cfg.n_layers, cfg.cols), dtype=torch.int64, device="cuda")
         E.engram_hash(eng.hasher, pre, cfg.prefix, 0, out)
-    n = warm + steps
+    n = warm + steps + stage_steps
     ids = torch.from_numpy(eng.ids_for("decode", n).T.copy().reshape(n, batch, 1)).cuda()
     d_h = torch.from_numpy(synth.highway(cfg, np.arange(batch))).cuda()
     pos = cfg.prefix
@@ -327,12 +359,26 @@ def run_decode_only(cfg, steps, warm=10, tables_on_host=False, batch=1):
     torch.cuda.synchronize()
     assert E.engram_check() == 0
     ms = t0.elapsed_time(t1) / steps
+    out = {}
+    if stage_steps:
+        # the projection's own duration: further steps with an event between the stages
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(stage_steps)]
+        E.prepare_events([e for row in ev for e in row])
+        for i in range(stage_steps):
+            E.engram_set_profile_events(ev[i])
+            eng.forward(ids[warm + steps + i], pos, d_h)
+            pos += 1
+        torch.cuda.synchronize()
+        E.engram_set_profile_events(None)
+        assert E.engram_check() == 0
+        stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in ev])  # ms
+        out["stage_ms"] = dict(zip(["hash", "gather", "gemv", "gate"], stage.mean(0).tolist()))
     wbytes = cfg.n_layers * cfg.N * (cfg.K // 256) * 84 if cfg.wkv_fmt == "q2k" else cfg.n_layers * cfg.N * cfg.K * 2
     sb = step_bytes(cfg, batch) - cfg.n_layers * cfg.N * cfg.K * 2 + wbytes
     del eng
     torch.cuda.empty_cache()
     return {"tokens_per_step": batch, "ms_per_step": ms, "tokens_per_s": batch / (ms * 1e-3),
-            "step_algorithmic_bytes": sb, "step_gbs": sb / (ms * 1e-3) / 1e9}
+            "step_algorithmic_bytes": sb, "step_gbs": sb / (ms * 1e-3) / 1e9, **out}
 
 
 def run_decode_graph(cfg, steps, warm=32, per_graph=32):
@@ -605,7 +651,10 @@ def main():
         return
     if args.only in ("wkvq2k", "wkvq2k8"):
         from deepseek_v4_engram_hash_gb300 import configs
-        r = run_decode_only(configs.V41_DECODE_WKVQ2K, args.steps, batch=8 if args.only == "wkvq2k8" else 1)
+        r = run_decode_only(configs.V41_DECODE_WKVQ2K, args.steps, batch=8 if args.only == "wkvq2k8" else 1,
+                            stage_steps=min(args.steps, 100))
+        if args.only == "wkvq2k":
+            r["roofline"] = q2k_alu_roofline(r, None, hbm, _sm_count())
         print(json.dumps(r), flush=True)
         return
     if args.only in ("q2k512", "stress"):
@@ -675,9 +724,10 @@ def main():
         r = run_other(configs.V41_PREFILL, 5, 0, tables_on_host=True)
         r["workload"] = "v41_prefill_T4096_host_tables"
         others["v41_prefill_T4096_host_tables"] = r
-        r = run_decode_only(configs.V41_DECODE_WKVQ2K, 2000)
+        r = run_decode_only(configs.V41_DECODE_WKVQ2K, 2000, stage_steps=200)
         r["workload"] = configs.V41_DECODE_WKVQ2K.name
         r["note"] = "projection read from Q2_K-quantised wkv (82.6 MB a step instead of 503.3 MB)"
+        r["roofline"] = q2k_alu_roofline(r, d["clocks"], hbm, _sm_count())
         others[configs.V41_DECODE_WKVQ2K.name] = r
         r = run_decode_only(configs.V41_DECODE_WKVQ2K, 1000, batch=8)
         r["workload"] = "v41_decode_B8_wkv_q2k"

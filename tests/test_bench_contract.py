@@ -42,3 +42,31 @@ def test_reference_arm_other_ranks_exit_quietly():
              {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, timeout=120)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_q2k_alu_roofline_arithmetic():
+    """The Q2_K decode's integer-pipe roofline: the counted ALU warp
+    instructions over the launch's event time, against 152 SMs x 4
+    sub-partitions x one warp instruction every 2 cycles at the sampled clock;
+    a changed kernel (no stored count) reports null, not a stale figure."""
+    sys.path.insert(0, ROOT)
+    import bench
+    r = {"stage_ms": {"gemv": 0.04}, "step_algorithmic_bytes": 82_851_340}
+    key = ("gemv_q2k", bench._src_hash("gemv.cu", "common.cuh"))
+    saved = dict(bench.NCU_ALU)
+    try:
+        bench.NCU_ALU.clear()
+        bench.NCU_ALU[key] = 15_000_000
+        o = bench.q2k_alu_roofline(r, {"sm_mhz": 2000.0}, 6794.5, 152)
+        assert o["bound"] == "alu"
+        assert abs(o["peak"] - 152 * 4 * 0.5 * 2000e6 / 1e12) < 1e-12           # 0.608 T/s
+        assert abs(o["achieved"] - 15e6 / 40e-6 / 1e12) < 1e-12                  # 0.375 T/s
+        assert abs(o["frac"] - o["achieved"] / o["peak"]) < 1e-12
+        assert abs(o["hbm_frac"] - 82_851_340 / 40e-6 / 1e9 / 6794.5) < 1e-12
+        bench.NCU_ALU.clear()
+        o = bench.q2k_alu_roofline(r, None, 6794.5, 152)
+        assert o["achieved"] is None and o["frac"] is None and o["instructions"] is None
+        assert abs(o["peak"] - 152 * 4 * 0.5 * 2070e6 / 1e12) < 1e-12           # default clock
+    finally:
+        bench.NCU_ALU.clear()
+        bench.NCU_ALU.update(saved)
