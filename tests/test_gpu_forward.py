@@ -151,24 +151,38 @@ def test_forward_stress_batch8_prefill_then_decode(E):
         first += B
 
 
-def test_forward_fused_gemv_matches_staged_calls(E):
+@pytest.mark.parametrize("tables,weights", [("fp8", "bf16"), ("q2k", "bf16"), ("q2k", "q2k")])
+def test_forward_fused_gemv_matches_staged_calls(E, tables, weights):
     """At one token the forward's fused gather + GEMV gives the same kv bits
-    as engram_rows_fp8 followed by engram_project."""
+    as the row kernel (engram_rows_fp8 or engram_rows_q2k) followed by
+    engram_project (or engram_project_q2k): the rows decoded into the mma
+    fragments in registers equal the row kernel's, bit for bit."""
     from deepseek_v4_engram_hash_gb300 import runner
-    cfg = configs.V41_DECODE
+    cfg = configs.V41_DECODE if tables == "fp8" else configs.V41_Q2K.with_(T=1)
+    if weights == "q2k":
+        cfg = cfg.with_(wkv_fmt="q2k")
     eng = runner.EngramSetup(cfg, batch=1, max_tokens=1)
     ids = eng.ids_for("fused", 1)
     d_h = _h_device(cfg, 0, 1, True)
     eng.forward(ids, 7, d_h)
+    assert E.engram_check() == 0
     row_ids = eng.row_ids(1).clone()
     for l in range(cfg.n_layers):
         d = eng.layer_data[l]
         x = torch.empty((cfg.cols, cfg.head_dim), dtype=torch.bfloat16, device="cuda")
-        E.engram_rows_fp8(d["table"], d["scales"], d["rows"], cfg.head_dim, cfg.scale_block,
-                          row_ids[:, l, :].contiguous(), 1, cfg.cols, cfg.cols, x)
+        rid = row_ids[:, l, :].contiguous()
+        if tables == "fp8":
+            E.engram_rows_fp8(d["table"], d["scales"], d["rows"], cfg.head_dim, cfg.scale_block, rid, 1,
+                              cfg.cols, cfg.cols, x)
+        else:
+            E.engram_rows_q2k(d["table"], d["rows"], rid, 1, cfg.cols, cfg.cols, x)
         kv = torch.empty((1, cfg.N), dtype=torch.bfloat16, device="cuda")
-        E.engram_project(x, d["wkv"], 1, cfg.K, cfg.N, kv)
-        assert torch.equal(kv.view(torch.int16), eng.kv(1, l).view(torch.int16))
+        if weights == "q2k":
+            E.engram_project_q2k(x, d["wkv_q2k"], cfg.K, cfg.N, kv)
+        else:
+            E.engram_project(x, d["wkv"], 1, cfg.K, cfg.N, kv)
+        assert E.engram_check() == 0
+        assert torch.equal(kv.view(torch.int16), eng.kv(1, l).view(torch.int16)), f"layer {l}"
 
 
 @pytest.mark.parametrize("name", ["v41", "odd_n", "wide_c"])
