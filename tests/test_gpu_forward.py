@@ -151,14 +151,15 @@ def test_forward_stress_batch8_prefill_then_decode(E):
         first += B
 
 
-@pytest.mark.parametrize("tables,weights", [("fp8", "bf16"), ("q2k", "bf16"), ("q2k", "q2k")])
+@pytest.mark.parametrize("tables,weights", [("fp8", "bf16"), ("e8m0", "bf16"), ("q2k", "bf16"), ("q2k", "q2k"),
+                                            ("fp8", "q2k")])
 def test_forward_fused_gemv_matches_staged_calls(E, tables, weights):
     """At one token the forward's fused gather + GEMV gives the same kv bits
-    as the row kernel (engram_rows_fp8 or engram_rows_q2k) followed by
+    as the row kernel (engram_rows_fp8, engram_rows_fp8_e8m0 or engram_rows_q2k) followed by
     engram_project (or engram_project_q2k): the rows decoded into the mma
     fragments in registers equal the row kernel's, bit for bit."""
     from deepseek_v4_engram_hash_gb300 import runner
-    cfg = configs.V41_DECODE if tables == "fp8" else configs.V41_Q2K.with_(T=1)
+    cfg = {"fp8": configs.V41_DECODE, "e8m0": configs.V41_DECODE_E8M0, "q2k": configs.V41_Q2K.with_(T=1)}[tables]
     if weights == "q2k":
         cfg = cfg.with_(wkv_fmt="q2k")
     eng = runner.EngramSetup(cfg, batch=1, max_tokens=1)
@@ -174,6 +175,9 @@ def test_forward_fused_gemv_matches_staged_calls(E, tables, weights):
         if tables == "fp8":
             E.engram_rows_fp8(d["table"], d["scales"], d["rows"], cfg.head_dim, cfg.scale_block, rid, 1,
                               cfg.cols, cfg.cols, x)
+        elif tables == "e8m0":
+            E.engram_rows_fp8_e8m0(d["table"], d["scales"], d["rows"], cfg.head_dim, cfg.scale_block, rid, 1,
+                                   cfg.cols, cfg.cols, x)
         else:
             E.engram_rows_q2k(d["table"], d["rows"], rid, 1, cfg.cols, cfg.cols, x)
         kv = torch.empty((1, cfg.N), dtype=torch.bfloat16, device="cuda")
