@@ -151,42 +151,48 @@ def test_forward_stress_batch8_prefill_then_decode(E):
         first += B
 
 
-@pytest.mark.parametrize("tables,weights", [("fp8", "bf16"), ("e8m0", "bf16"), ("q2k", "bf16"), ("q2k", "q2k"),
-                                            ("fp8", "q2k")])
-def test_forward_fused_gemv_matches_staged_calls(E, tables, weights):
-    """At one token the forward's fused gather + GEMV gives the same kv bits
-    as the row kernel (engram_rows_fp8, engram_rows_fp8_e8m0 or engram_rows_q2k) followed by
-    engram_project (or engram_project_q2k): the rows decoded into the mma
-    fragments in registers equal the row kernel's, bit for bit."""
+@pytest.mark.parametrize("tables,weights,B", [("fp8", "bf16", 1), ("e8m0", "bf16", 1), ("q2k", "bf16", 1),
+                                              ("q2k", "q2k", 1), ("fp8", "q2k", 1), ("fp8", "bf16", 8),
+                                              ("q2k", "q2k", 8)])
+def test_forward_fused_gemv_matches_staged_calls(E, tables, weights, B):
+    """A decode step of B sequences (B tokens, the GEMV path): the forward's
+    fused gather + GEMV gives the same kv bits as the row kernel
+    (engram_rows_fp8, engram_rows_fp8_e8m0 or engram_rows_q2k) followed by
+    engram_project (or engram_project_q2k, one token a call): the rows decoded
+    into the mma fragments in registers equal the row kernel's, bit for bit,
+    and each token's column of the mma is independent of the others."""
     from deepseek_v4_engram_hash_gb300 import runner
     cfg = {"fp8": configs.V41_DECODE, "e8m0": configs.V41_DECODE_E8M0, "q2k": configs.V41_Q2K.with_(T=1)}[tables]
     if weights == "q2k":
         cfg = cfg.with_(wkv_fmt="q2k")
-    eng = runner.EngramSetup(cfg, batch=1, max_tokens=1)
-    ids = eng.ids_for("fused", 1)
-    d_h = _h_device(cfg, 0, 1, True)
+    cfg = cfg.with_(batch=B)
+    eng = runner.EngramSetup(cfg, batch=B, max_tokens=B)
+    ids = eng.ids_for("fused", 1)                                            # [B, 1]
+    d_h = _h_device(cfg, 0, B, True)
     eng.forward(ids, 7, d_h)
     assert E.engram_check() == 0
-    row_ids = eng.row_ids(1).clone()
+    row_ids = eng.row_ids(B).clone()                                         # [B, L, C]
     for l in range(cfg.n_layers):
         d = eng.layer_data[l]
-        x = torch.empty((cfg.cols, cfg.head_dim), dtype=torch.bfloat16, device="cuda")
+        x = torch.empty((B * cfg.cols, cfg.head_dim), dtype=torch.bfloat16, device="cuda")
         rid = row_ids[:, l, :].contiguous()
         if tables == "fp8":
-            E.engram_rows_fp8(d["table"], d["scales"], d["rows"], cfg.head_dim, cfg.scale_block, rid, 1,
+            E.engram_rows_fp8(d["table"], d["scales"], d["rows"], cfg.head_dim, cfg.scale_block, rid, B,
                               cfg.cols, cfg.cols, x)
         elif tables == "e8m0":
-            E.engram_rows_fp8_e8m0(d["table"], d["scales"], d["rows"], cfg.head_dim, cfg.scale_block, rid, 1,
+            E.engram_rows_fp8_e8m0(d["table"], d["scales"], d["rows"], cfg.head_dim, cfg.scale_block, rid, B,
                                    cfg.cols, cfg.cols, x)
         else:
-            E.engram_rows_q2k(d["table"], d["rows"], rid, 1, cfg.cols, cfg.cols, x)
-        kv = torch.empty((1, cfg.N), dtype=torch.bfloat16, device="cuda")
+            E.engram_rows_q2k(d["table"], d["rows"], rid, B, cfg.cols, cfg.cols, x)
+        xt = x.view(B, cfg.K)
+        kv = torch.empty((B, cfg.N), dtype=torch.bfloat16, device="cuda")
         if weights == "q2k":
-            E.engram_project_q2k(x, d["wkv_q2k"], cfg.K, cfg.N, kv)
+            for t in range(B):
+                E.engram_project_q2k(xt[t:t + 1], d["wkv_q2k"], cfg.K, cfg.N, kv[t:t + 1])
         else:
-            E.engram_project(x, d["wkv"], 1, cfg.K, cfg.N, kv)
+            E.engram_project(xt, d["wkv"], B, cfg.K, cfg.N, kv)
         assert E.engram_check() == 0
-        assert torch.equal(kv.view(torch.int16), eng.kv(1, l).view(torch.int16)), f"layer {l}"
+        assert torch.equal(kv.view(torch.int16), eng.kv(B, l).view(torch.int16)), f"layer {l}"
 
 
 @pytest.mark.parametrize("name", ["v41", "odd_n", "wide_c"])
