@@ -1,7 +1,7 @@
 """Seeded random geometries through the whole forward, every output checked
 against the oracle: layers 1..4, n-grams 2..16, 1..8 heads, head_dim 16..256
 with its scale blocks, dim a multiple of 8, hc 1..4, fp8 / e8m0 / Q2_K tables,
-batch 1..5, and a call sequence that crosses the GEMV (<= 8 tokens) and the
+bf16 or (where K is a multiple of 256) Q2_K-quantised wkv, batch 1..5, and a call sequence that crosses the GEMV (<= 8 tokens) and the
 GEMM paths.  Row ids must be bit-exact, kv within 2e-2, the highway within
 1e-3 (stage-wise)."""
 import numpy as np
@@ -40,15 +40,17 @@ def _geometry(seed: int):
         hc = int(rng.integers(1, 5))
         B = int(rng.integers(1, 6))
         T = int(rng.integers(9, 40))
+        # Q2_K-quantised wkv (the <= 8-token projection reads its blocks) where K allows it
+        wkv_fmt = "q2k" if (C * hd) % 256 == 0 and C * hd <= 6144 and int(rng.integers(0, 2)) else "bf16"
         return configs.TINY.with_(
             name=f"rand{seed}", vocab=int(rng.integers(50, 3000)), n_compressed=int(rng.integers(20, 2000)),
             unmapped_5pct=bool(rng.integers(0, 2)), pad_token_id=int(rng.integers(0, 20)),
             layer_ids=tuple(range(L)), max_ngram=ng, n_heads=H, prime_target=int(rng.integers(50, 400)),
             head_dim=hd, scale_block=blk, dim=dim, hc=hc, fmt=fmt, batch=B, T=T, ids="uniform",
-            seed=seed)
+            seed=seed, wkv_fmt=wkv_fmt)
 
 
-@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("seed", range(16))
 def test_forward_random_geometry(E, seed):
     from deepseek_v4_engram_hash_gb300 import runner
     cfg = _geometry(seed)
