@@ -642,7 +642,13 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     import __graft_entry__
+    # one build a node: local rank 0 compiles (when anything is stale), the
+    # others wait for it and then only load the libraries
+    if world > 1 and local != 0:
+        dist.barrier()
     __graft_entry__.build()
+    if world > 1 and local == 0:
+        dist.barrier()
 
     hbm, bf16_burst, bf16_sust, peak_src = _peaks()
     if args.only == "decode8":
