@@ -187,7 +187,7 @@ def run_decode(args, rank, world):
     with Clocks(torch.cuda.current_device()) as clk:
         time.sleep(0.3)                         # let the clock sampler start
         # the W warm-up steps run right before the timed ones, so that the timed
-        # region does not start from an idle GPU
+        # region starts from a GPU whose clocks are up
         for i in range(args.warmup):
             eng.forward(ids_all[i], pos, d_h)
             pos += 1
@@ -199,6 +199,7 @@ def run_decode(args, rank, world):
             pos += 1
         t1.record()
         torch.cuda.synchronize()
+        _barrier(world)
         assert E.engram_check() == 0
         ms = t0.elapsed_time(t1) / args.steps
         # Same steps again with an event between the stages of every step (the
