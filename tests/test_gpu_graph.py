@@ -82,8 +82,10 @@ def test_device_position_past_the_cache_is_reported(E, T):
 
 
 @pytest.mark.parametrize("cfg,B,T,K", [(configs.V41_DECODE, 1, 1, 8), (configs.TINY, 2, 3, 4),
-                                       (configs.TINY, 1, 12, 3)],
-                         ids=["v41_T1_8steps", "tiny_B2_T3_4steps", "tiny_T12_gemm_3steps"])
+                                       (configs.TINY, 1, 12, 3), (configs.V41_DECODE_WKVQ2K, 1, 1, 8),
+                                       (configs.V41_DECODE_E8M0, 2, 1, 4)],
+                         ids=["v41_T1_8steps", "tiny_B2_T3_4steps", "tiny_T12_gemm_3steps", "v41_q2k_wkv_8steps",
+                              "v41_e8m0_B2_4steps"])
 def test_multi_step_graph_bit_identical_to_eager(E, cfg, B, T, K):
     """K decode steps in one graph (each step hashing at *d_pos + k T, only the
     last step's gate advancing the position): every step's highway rows equal
