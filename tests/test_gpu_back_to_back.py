@@ -58,6 +58,7 @@ CASES = {
     "v41_decode_B8": (configs.V41_DECODE, 8, 64, 0, (0, 7), 16),
     "large_table_stress": (configs.STRESS, 8, 512, 1536, (0, 7), 64),
     "v41_prefill_then_decode": (configs.V41_PREFILL, 1, 64, 4096, (0,), 16),
+    "v41_q2k_tables_prefill_then_decode": (configs.V41_Q2K, 1, 64, 512, (0,), 16),
 }
 
 
